@@ -1,0 +1,596 @@
+// api.cu: the C-ABI (include/gemm.h): handle, argument checks, tile picker,
+// TMA descriptor encoding with a small cache, and kernel dispatch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "../../include/gemm.h"
+#include "internal.h"
+
+namespace dg {
+
+constexpr int kMaxTileN = 256;
+constexpr int kTicketCap = 16384;     // split tiles one launch may have
+constexpr int kTmapCacheSize = 32;
+constexpr int64_t kMaxCoord = (int64_t(1) << 31) - 1024;  // TMA coordinates are int32
+
+struct Options {
+  int force_kernel = -1;
+  int force_tile_n = -1;
+  int force_grid = -1;
+  int min_split_iters = 2;
+  int force_swap = -1;
+  int group_m = 16;
+  uint64_t wait_limit_ns = 2000000000ull;
+};
+
+struct TmapKey {
+  const void* ptr;
+  int64_t rows, k;
+  int mn_major, box_rows;
+  bool operator==(const TmapKey& o) const {
+    return ptr == o.ptr && rows == o.rows && k == o.k && mn_major == o.mn_major &&
+           box_rows == o.box_rows;
+  }
+};
+
+struct TmapEntry {
+  TmapKey key;
+  CUtensorMap map;
+  bool valid = false;
+};
+
+namespace {
+
+bool log_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("GEMM_LOG");
+    return v && v[0] && v[0] != '0';
+  }();
+  return on;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------ tile picker --
+// Chooses kernel, tile, split and grid for a shape.  Rules:
+//  * fp32 inputs -> CUDA-core kernel, 128x128 tiles.
+//  * fp16 inputs -> tcgen05 kernel.  Skinny M (M <= 128, N >= 2M, A row-major)
+//    swaps the operands so N fills the 128-row MMA side and M becomes the MMA
+//    N side (16/32/64/128 columns).  Otherwise the tile is 128x256 (128x128
+//    when N <= 128).
+//  * Decomposition (the Stream-K rule of the leiblog.wang Stream-K post: keep
+//    every SM busy when the tile count leaves waves part-empty):
+//      tiles >= SMs, count a multiple of the SMs or >= 4 full waves: whole tiles;
+//      tiles >= SMs otherwise: whole tiles for all but the last full wave, the
+//        rest (between 1 and 2 waves' worth) split evenly over all SMs;
+//      tiles < SMs: all k-blocks split evenly over up to one CTA per SM, at
+//        least min_split_iters k-blocks each.
+int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
+             const Options& o, gemm_plan_t* p) {
+  if (!p) return GEMM_ERR_INVALID_ARG;
+  std::memset(p, 0, sizeof(*p));
+  if (M < 0 || N < 0 || K < 0 || num_sms <= 0) return GEMM_ERR_INVALID_ARG;
+  if (L.a_major > 1 || L.b_major > 1 || L.in_dtype > 1 || L.out_dtype > 1)
+    return GEMM_ERR_INVALID_ARG;
+  if (L.in_dtype == GEMM_F32 && L.out_dtype == GEMM_F16) return GEMM_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) {
+    p->kernel = GEMM_KERNEL_NONE;
+    return GEMM_OK;
+  }
+  if (K == 0) {
+    p->kernel = GEMM_KERNEL_FILL;
+    p->grid = 1;
+    return GEMM_OK;
+  }
+  if (L.in_dtype == GEMM_F32) {
+    if (o.force_kernel >= 0 && o.force_kernel != GEMM_KERNEL_SIMT) return GEMM_ERR_UNSUPPORTED;
+    if (ceil_div(M, kSimtBM) > 65535) return GEMM_ERR_UNSUPPORTED;
+    p->kernel = GEMM_KERNEL_SIMT;
+    p->tile_m = kSimtBM;
+    p->tile_n = kSimtBN;
+    p->tile_k = kSimtBK;
+    p->stages = 2;
+    p->tiles_m = int32_t(ceil_div(M, kSimtBM));
+    p->tiles_n = int32_t(ceil_div(N, kSimtBN));
+    p->grid = p->tiles_m * p->tiles_n;
+    p->k_iters = int32_t(std::min<int64_t>(ceil_div(K, kSimtBK), INT32_MAX));
+    p->dp_tiles = p->grid;
+    return GEMM_OK;
+  }
+  // fp16: tensor-core path.
+  if (o.force_kernel == GEMM_KERNEL_SIMT) return GEMM_ERR_UNSUPPORTED;
+  if (M > kMaxCoord || N > kMaxCoord || K > kMaxCoord) return GEMM_ERR_UNSUPPORTED;
+  const int64_t lda = L.a_major == GEMM_ROW_MAJOR ? K : M;
+  const int64_t ldb = L.b_major == GEMM_ROW_MAJOR ? N : K;
+  if (lda % 8 != 0 || ldb % 8 != 0) return GEMM_ERR_UNSUPPORTED;  // TMA stride rule
+
+  const bool swap = o.force_swap >= 0 ? (o.force_swap != 0)
+                                      : (L.a_major == GEMM_ROW_MAJOR && M <= 128 && N >= 2 * M);
+  const int64_t Mm = swap ? N : M;
+  const int64_t Nm = swap ? M : N;
+  const int a_mn = swap ? (L.b_major == GEMM_ROW_MAJOR) : (L.a_major == GEMM_COL_MAJOR);
+  const int b_mn = swap ? (L.a_major == GEMM_COL_MAJOR) : (L.b_major == GEMM_ROW_MAJOR);
+
+  int bn;
+  if (o.force_tile_n > 0) {
+    bn = o.force_tile_n;
+  } else if (swap) {
+    bn = Nm <= 16 ? 16 : Nm <= 32 ? 32 : Nm <= 64 ? 64 : 128;
+    if (b_mn && bn < 64) bn = 64;
+  } else {
+    bn = Nm <= 128 ? 128 : 256;
+  }
+  const bool bn_ok = swap ? (bn == 16 || bn == 32 || bn == 64 || bn == 128)
+                          : (bn == 128 || bn == 256);
+  if (!bn_ok || (b_mn && bn % 64 != 0)) return GEMM_ERR_UNSUPPORTED;
+
+  const int64_t tiles_m = ceil_div(Mm, kBM);
+  const int64_t tiles_n = ceil_div(Nm, bn);
+  const int64_t T = tiles_m * tiles_n;
+  const int64_t I = ceil_div(K, kBK);
+  if (T > INT32_MAX / 2 || I > INT32_MAX / 2 || T * I > (int64_t(1) << 40))
+    return GEMM_ERR_UNSUPPORTED;
+  const int64_t G = num_sms;
+  int64_t dp = 0, sk = 0, grid = 0;
+  const int64_t max_grid = o.force_grid > 0 ? std::min<int64_t>(o.force_grid, G) : G;
+
+  if (o.force_kernel == GEMM_KERNEL_TC) {
+    dp = T;
+    grid = std::min(max_grid, T);
+  } else if (o.force_kernel == GEMM_KERNEL_STREAMK) {
+    sk = T;
+    grid = std::min(max_grid, T * I);
+  } else if (T >= G) {
+    const int64_t full = T / G, rem = T % G;
+    if (rem == 0 || full >= 4) {
+      dp = T;
+    } else {
+      dp = (full - 1) * G;
+      sk = T - dp;
+    }
+    grid = G;
+    if (max_grid < G) {  // a forced smaller grid: split everything over it
+      dp = 0;
+      sk = T;
+      grid = max_grid;
+    }
+  } else {
+    const int64_t total = T * I;
+    const int64_t want = std::max<int64_t>(T, total / std::max(1, o.min_split_iters));
+    grid = std::min(max_grid, want);
+    if (grid == T) {
+      dp = T;  // one whole tile per CTA
+    } else {
+      sk = T;
+    }
+  }
+  if (sk > kTicketCap) return GEMM_ERR_UNSUPPORTED;
+
+  p->kernel = sk > 0 ? GEMM_KERNEL_STREAMK : GEMM_KERNEL_TC;
+  p->swap_ab = swap ? 1 : 0;
+  p->tile_m = kBM;
+  p->tile_n = bn;
+  p->tile_k = kBK;
+  p->stages = tc_stages_for(bn);
+  p->grid = int32_t(grid);
+  p->tiles_m = int32_t(tiles_m);
+  p->tiles_n = int32_t(tiles_n);
+  p->k_iters = int32_t(I);
+  p->dp_tiles = int32_t(dp);
+  p->sk_tiles = int32_t(sk);
+  p->a_mn_major = a_mn;
+  p->b_mn_major = b_mn;
+  p->group_m = std::max(1, o.group_m);
+  p->workspace_bytes = sk > 0 ? int64_t(2) * grid * kBM * bn * 4 : 0;
+  return GEMM_OK;
+}
+
+WorkSpec spec_of(const gemm_plan_t& p) {
+  WorkSpec w;
+  w.tiles_m = p.tiles_m;
+  w.tiles_n = p.tiles_n;
+  w.k_iters = p.k_iters;
+  w.dp_tiles = p.dp_tiles;
+  w.sk_tiles = p.sk_tiles;
+  w.grid = p.grid;
+  w.group_m = p.group_m;
+  return w;
+}
+
+// ------------------------------------------------------------- TMA maps --
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+}  // namespace
+}  // namespace dg
+
+struct gemm_ctx {
+  int device = 0;
+  int num_sms = 0;
+  float* workspace = nullptr;
+  size_t workspace_bytes = 0;
+  int* tickets = nullptr;
+  int* status = nullptr;
+  int last_detail = 0;
+  dg::Options opt;
+  std::mutex mu;  // guards the tensor-map cache
+  dg::TmapEntry cache[dg::kTmapCacheSize];
+  int cache_next = 0;
+};
+
+namespace dg {
+namespace {
+
+// An fp16 operand with `rows` rows (MMA view) and depth K:
+//   K-major  (K contiguous):      dims {K, rows}, box {64, box_rows}
+//   MN-major (rows contiguous):   dims {rows, K}, box {64, 64}
+// 128-byte swizzle; out-of-range elements read as zero.
+int encode_operand(gemm_ctx* h, CUtensorMap* out, const void* ptr, int64_t rows, int64_t K,
+                   int mn_major, int box_rows) {
+  const TmapKey key{ptr, rows, K, mn_major, box_rows};
+  {
+    std::lock_guard<std::mutex> g(h->mu);
+    for (auto& e : h->cache)
+      if (e.valid && e.key == key) {
+        *out = e.map;
+        return GEMM_OK;
+      }
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return GEMM_ERR_CUDA;
+  cuuint64_t dims[2], strides[1];
+  cuuint32_t box[2], estr[2] = {1, 1};
+  if (!mn_major) {
+    dims[0] = cuuint64_t(K);
+    dims[1] = cuuint64_t(rows);
+    strides[0] = cuuint64_t(K) * 2;
+    box[0] = kBK;
+    box[1] = cuuint32_t(box_rows);
+  } else {
+    dims[0] = cuuint64_t(rows);
+    dims[1] = cuuint64_t(K);
+    strides[0] = cuuint64_t(rows) * 2;
+    box[0] = 64;
+    box[1] = kBK;
+  }
+  CUtensorMap map;
+  const CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return GEMM_ERR_CUDA;
+  std::lock_guard<std::mutex> g(h->mu);
+  TmapEntry& e = h->cache[h->cache_next];
+  h->cache_next = (h->cache_next + 1) % kTmapCacheSize;
+  e.key = key;
+  e.map = map;
+  e.valid = true;
+  *out = map;
+  return GEMM_OK;
+}
+
+// Runs `f` with the handle's device current, restoring the caller's.
+template <class F>
+int on_device(int device, F&& f) {
+  int prev = -1;
+  if (cudaGetDevice(&prev) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (prev != device && cudaSetDevice(device) != cudaSuccess) return GEMM_ERR_CUDA;
+  const int rc = f();
+  if (prev != device) cudaSetDevice(prev);
+  return rc;
+}
+
+void log_plan(const gemm_plan_t& p, int64_t M, int64_t N, int64_t K) {
+  std::fprintf(stderr,
+               "[gemm] M=%lld N=%lld K=%lld kernel=%d swap=%d tile=%dx%dx%d stages=%d "
+               "grid=%d tiles=%dx%d k_iters=%d dp=%d sk=%d a_mn=%d b_mn=%d\n",
+               (long long)M, (long long)N, (long long)K, p.kernel, p.swap_ab, p.tile_m,
+               p.tile_n, p.tile_k, p.stages, p.grid, p.tiles_m, p.tiles_n, p.k_iters,
+               p.dp_tiles, p.sk_tiles, p.a_mn_major, p.b_mn_major);
+}
+
+}  // namespace
+
+cudaError_t launch_tc(const TcLaunch& L) {
+  if (L.bn == 256) return launch_tc_n256(L);
+  if (L.bn == 128) return launch_tc_n128(L);
+  return launch_tc_small(L);
+}
+
+int tc_stages_for(int bn) {
+  switch (bn) {
+    case 256: return TcConfig<256>::kStages;
+    case 128: return TcConfig<128>::kStages;
+    case 64: return TcConfig<64>::kStages;
+    case 32: return TcConfig<32>::kStages;
+    default: return TcConfig<16>::kStages;
+  }
+}
+
+int tc_smem_bytes_for(int bn) {
+  switch (bn) {
+    case 256: return TcConfig<256>::kSmemBytes;
+    case 128: return TcConfig<128>::kSmemBytes;
+    case 64: return TcConfig<64>::kSmemBytes;
+    case 32: return TcConfig<32>::kSmemBytes;
+    default: return TcConfig<16>::kSmemBytes;
+  }
+}
+
+}  // namespace dg
+
+// ================================================================== C-ABI ==
+extern "C" {
+
+const char* gemm_strerror(int code) {
+  switch (code) {
+    case GEMM_OK: return "GEMM_OK";
+    case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG: invalid argument";
+    case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED: shape/layout/alignment not supported";
+    case GEMM_ERR_ALLOC: return "GEMM_ERR_ALLOC: allocation failed";
+    case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: CUDA call failed";
+    case GEMM_ERR_DEVICE_TIMEOUT: return "GEMM_ERR_DEVICE_TIMEOUT: a device-side wait expired";
+    default: return "unknown gemm status";
+  }
+}
+
+int gemm_plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t layout, int num_sms,
+                  gemm_plan_t* out) {
+  return dg::plan_for(M, N, K, layout, num_sms, dg::Options(), out);
+}
+
+int gemm_work_units(const gemm_plan_t* plan, int cta, int32_t* out, int max_units) {
+  if (!plan || cta < 0 || cta >= plan->grid || max_units < 0 || (max_units > 0 && !out))
+    return GEMM_ERR_INVALID_ARG;
+  if (plan->kernel != GEMM_KERNEL_TC && plan->kernel != GEMM_KERNEL_STREAMK)
+    return GEMM_ERR_INVALID_ARG;
+  const dg::WorkSpec w = dg::spec_of(*plan);
+  dg::WorkIter it;
+  it.init(w, cta);
+  dg::Unit u;
+  int n = 0;
+  while (it.next(w, u)) {
+    if (n < max_units) {
+      out[3 * n] = u.tile;
+      out[3 * n + 1] = u.kb0;
+      out[3 * n + 2] = u.kb1;
+    }
+    ++n;
+  }
+  return n;
+}
+
+int gemm_split_contributors(const gemm_plan_t* plan, int sk_tile, int32_t* first,
+                            int32_t* last) {
+  if (!plan || !first || !last || sk_tile < 0 || sk_tile >= plan->sk_tiles)
+    return GEMM_ERR_INVALID_ARG;
+  const dg::WorkSpec w = dg::spec_of(*plan);
+  dg::split_contributors(w, sk_tile, *first, *last);
+  return GEMM_OK;
+}
+
+int gemm_simt_smem_strides(int32_t* a_stride, int32_t* b_stride) {
+  if (!a_stride || !b_stride) return GEMM_ERR_INVALID_ARG;
+  *a_stride = dg::simt_a_stride();
+  *b_stride = dg::simt_b_stride();
+  return GEMM_OK;
+}
+
+int gemm_create(gemm_handle_t* out, int device) {
+  if (!out) return GEMM_ERR_INVALID_ARG;
+  *out = nullptr;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (device < 0 || device >= ndev) return GEMM_ERR_INVALID_ARG;
+  gemm_ctx* h = new (std::nothrow) gemm_ctx();
+  if (!h) return GEMM_ERR_ALLOC;
+  h->device = device;
+  const int rc = dg::on_device(device, [&]() -> int {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return GEMM_ERR_UNSUPPORTED;
+    h->num_sms = prop.multiProcessorCount;
+    h->workspace_bytes = size_t(2) * h->num_sms * dg::kBM * dg::kMaxTileN * sizeof(float);
+    if (cudaMalloc(&h->workspace, h->workspace_bytes) != cudaSuccess) return GEMM_ERR_ALLOC;
+    if (cudaMalloc(&h->tickets, sizeof(int) * dg::kTicketCap) != cudaSuccess)
+      return GEMM_ERR_ALLOC;
+    if (cudaMalloc(&h->status, sizeof(int)) != cudaSuccess) return GEMM_ERR_ALLOC;
+    if (cudaMemset(h->tickets, 0, sizeof(int) * dg::kTicketCap) != cudaSuccess ||
+        cudaMemset(h->status, 0, sizeof(int)) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    return GEMM_OK;
+  });
+  if (rc != GEMM_OK) {
+    gemm_destroy(h);
+    return rc;
+  }
+  *out = h;
+  return GEMM_OK;
+}
+
+int gemm_destroy(gemm_handle_t h) {
+  if (!h) return GEMM_OK;
+  dg::on_device(h->device, [&]() -> int {
+    if (h->workspace) cudaFree(h->workspace);
+    if (h->tickets) cudaFree(h->tickets);
+    if (h->status) cudaFree(h->status);
+    return GEMM_OK;
+  });
+  delete h;
+  return GEMM_OK;
+}
+
+int gemm_set_option(gemm_handle_t h, int option, int64_t value) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  dg::Options& o = h->opt;
+  const dg::Options d;
+  switch (option) {
+    case GEMM_OPT_FORCE_KERNEL:
+      if (value >= 0 && value != GEMM_KERNEL_TC && value != GEMM_KERNEL_STREAMK &&
+          value != GEMM_KERNEL_SIMT)
+        return GEMM_ERR_INVALID_ARG;
+      o.force_kernel = value < 0 ? d.force_kernel : int(value);
+      return GEMM_OK;
+    case GEMM_OPT_FORCE_TILE_N:
+      if (value >= 0 && value != 16 && value != 32 && value != 64 && value != 128 &&
+          value != 256)
+        return GEMM_ERR_INVALID_ARG;
+      o.force_tile_n = value < 0 ? d.force_tile_n : int(value);
+      return GEMM_OK;
+    case GEMM_OPT_FORCE_GRID:
+      o.force_grid = value <= 0 ? d.force_grid : int(std::min<int64_t>(value, INT32_MAX));
+      return GEMM_OK;
+    case GEMM_OPT_WAIT_LIMIT_NS:
+      o.wait_limit_ns = value <= 0 ? d.wait_limit_ns : uint64_t(value);
+      return GEMM_OK;
+    case GEMM_OPT_MIN_SPLIT_ITERS:
+      o.min_split_iters = value <= 0 ? d.min_split_iters : int(std::min<int64_t>(value, 1 << 20));
+      return GEMM_OK;
+    case GEMM_OPT_FORCE_SWAP_AB:
+      if (value > 1) return GEMM_ERR_INVALID_ARG;
+      o.force_swap = value < 0 ? d.force_swap : int(value);
+      return GEMM_OK;
+    case GEMM_OPT_GROUP_M:
+      o.group_m = value <= 0 ? d.group_m : int(std::min<int64_t>(value, 1 << 16));
+      return GEMM_OK;
+    default:
+      return GEMM_ERR_INVALID_ARG;
+  }
+}
+
+int gemm_query_plan(gemm_handle_t h, int64_t M, int64_t N, int64_t K, gemm_layout_t layout,
+                    gemm_plan_t* out) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  return dg::plan_for(M, N, K, layout, h->num_sms, h->opt, out);
+}
+
+int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, const void* B,
+             const float* bias, void* C, gemm_layout_t layout, void* stream_ptr) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  gemm_plan_t plan;
+  int rc = dg::plan_for(M, N, K, layout, h->num_sms, h->opt, &plan);
+  if (rc != GEMM_OK) return rc;
+  if (dg::log_enabled()) dg::log_plan(plan, M, N, K);
+  if (plan.kernel == GEMM_KERNEL_NONE) return GEMM_OK;
+  if (!C) return GEMM_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
+  if (plan.kernel == GEMM_KERNEL_FILL) {
+    return dg::on_device(h->device, [&]() -> int {
+      return dg::launch_fill(M, N, bias, C, layout.out_dtype == GEMM_F16, stream) == cudaSuccess
+                 ? GEMM_OK
+                 : GEMM_ERR_CUDA;
+    });
+  }
+  if (!A || !B) return GEMM_ERR_INVALID_ARG;
+
+  if (plan.kernel == GEMM_KERNEL_SIMT) {
+    dg::SimtLaunch L;
+    L.M = M; L.N = N; L.K = K;
+    L.A = static_cast<const float*>(A);
+    L.B = static_cast<const float*>(B);
+    L.bias = bias;
+    L.C = static_cast<float*>(C);
+    L.a_major = layout.a_major;
+    L.b_major = layout.b_major;
+    L.stream = stream;
+    return dg::on_device(h->device, [&]() -> int {
+      return dg::launch_simt(L) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    });
+  }
+
+  // tensor-core path: TMA reads need 16-byte aligned bases
+  if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15))
+    return GEMM_ERR_UNSUPPORTED;
+  const bool swap = plan.swap_ab != 0;
+  const void* opA = swap ? B : A;  // MMA-view A operand (rows Mm)
+  const void* opB = swap ? A : B;  // MMA-view B operand (rows Nm)
+  const int64_t Mm = swap ? N : M;
+  const int64_t Nm = swap ? M : N;
+
+  dg::TcLaunch L;
+  L.bn = plan.tile_n;
+  L.out_f16 = layout.out_dtype == GEMM_F16;
+  L.trans = swap;
+  L.grid = plan.grid;
+  L.stream = stream;
+  rc = dg::encode_operand(h, &L.tmA, opA, Mm, K, plan.a_mn_major, dg::kBM);
+  if (rc != GEMM_OK) return rc;
+  rc = dg::encode_operand(h, &L.tmB, opB, Nm, K, plan.b_mn_major, plan.tile_n);
+  if (rc != GEMM_OK) return rc;
+  dg::TcArgs& a = L.args;
+  a.work = dg::spec_of(plan);
+  a.Mm = int32_t(Mm);
+  a.Nm = int32_t(Nm);
+  a.C = C;
+  a.ldc = N;
+  a.bias = bias;
+  a.workspace = h->workspace;
+  a.tickets = h->tickets;
+  a.status = h->status;
+  a.wait_limit_ns = h->opt.wait_limit_ns;
+  a.a_mn = plan.a_mn_major;
+  a.b_mn = plan.b_mn_major;
+  a.idesc = dg::make_idesc_f16(dg::kBM, plan.tile_n, plan.a_mn_major, plan.b_mn_major);
+  return dg::on_device(h->device, [&]() -> int {
+    return dg::launch_tc(L) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+  });
+}
+
+int gemm_status(gemm_handle_t h, void* stream_ptr) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
+  return dg::on_device(h->device, [&]() -> int {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpy(&word, h->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    h->last_detail = word;
+    if (word == 0) return GEMM_OK;
+    // a kernel stopped early: clear the word and the split counters it may
+    // have left behind, so the handle is usable again
+    if (cudaMemset(h->status, 0, sizeof(int)) != cudaSuccess ||
+        cudaMemset(h->tickets, 0, sizeof(int) * dg::kTicketCap) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    return GEMM_ERR_DEVICE_TIMEOUT;
+  });
+}
+
+int gemm_status_detail(gemm_handle_t h) { return h ? h->last_detail : 0; }
+
+int gemm_selftest_wait_timeout(gemm_handle_t h, int64_t limit_ns, void* stream_ptr) {
+  if (!h || limit_ns <= 0) return GEMM_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
+  return dg::on_device(h->device, [&]() -> int {
+    return dg::launch_wait_selftest(uint64_t(limit_ns), h->status, stream) == cudaSuccess
+               ? GEMM_OK
+               : GEMM_ERR_CUDA;
+  });
+}
+
+}  // extern "C"

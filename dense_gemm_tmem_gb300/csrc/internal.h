@@ -1,0 +1,58 @@
+// internal.h: host-side declarations shared by the API and the kernel launch
+// files (not part of the public C-ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "tc_kernel.cuh"
+
+namespace dg {
+
+// One tensor-core launch, fully described.
+struct TcLaunch {
+  int bn;             // MMA N tile: 16, 32, 64, 128 or 256
+  bool out_f16;
+  bool trans;         // swapped operands, transposed store
+  int grid;
+  CUtensorMap tmA;
+  CUtensorMap tmB;
+  TcArgs args;
+  cudaStream_t stream;
+};
+
+// Launches the matching tc_gemm_kernel instantiation (sets its shared-memory
+// attribute on first use).  Returns cudaErrorInvalidValue for a combination
+// that has no instantiation.
+cudaError_t launch_tc(const TcLaunch& L);
+cudaError_t launch_tc_n256(const TcLaunch& L);
+cudaError_t launch_tc_n128(const TcLaunch& L);
+cudaError_t launch_tc_small(const TcLaunch& L);
+int tc_stages_for(int bn);
+int tc_smem_bytes_for(int bn);
+
+// fp32 CUDA-core GEMM (simt.cu).
+struct SimtLaunch {
+  int64_t M, N, K;
+  const float* A;
+  const float* B;
+  const float* bias;
+  float* C;
+  int a_major, b_major;  // 0 row, 1 column
+  cudaStream_t stream;
+};
+cudaError_t launch_simt(const SimtLaunch& L);
+constexpr int kSimtBM = 128, kSimtBN = 128, kSimtBK = 8, kSimtThreads = 256;
+int simt_a_stride();
+int simt_b_stride();
+
+// K == 0: C = bias (or 0) (fill.cu).
+cudaError_t launch_fill(int64_t M, int64_t N, const float* bias, void* C, bool out_f16,
+                        cudaStream_t stream);
+
+// One CTA whose bounded wait never completes (selftest.cu).
+cudaError_t launch_wait_selftest(uint64_t limit_ns, int* status, cudaStream_t stream);
+
+}  // namespace dg

@@ -1,0 +1,451 @@
+// tc_kernel.cuh: the tcgen05/TMEM tensor-core GEMM for sm_103a.
+//
+//   D[Mm x Nm] = Aop[Mm x K] · Bop[Nm x K]ᵀ   (fp16 in, fp32 accumulate in TMEM)
+//
+// then C = D (+bias) rounded once to fp16 or kept in fp32.  With TRANS the
+// kernel has been handed swapped operands (Aop = Bᵀ, Bop = A) and writes Dᵀ,
+// so a skinny M lands on the MMA's N side.
+//
+// Design, per CTA (192 threads, one CTA per SM, persistent over work units):
+//   warp 0, one lane   TMA producer: 128x64 A block and BNx64 B block per
+//                      k-block into an S-stage ring of 128B-swizzled shared
+//                      memory (the swizzle takes the place of the padding the
+//                      leiblog.wang bank-conflict post adds to a 128x256x32 tile).
+//   warp 1, one lane   MMA issuer: 4 x tcgen05.mma (K = 16 each) per k-block into
+//                      one of two TMEM accumulators (BN fp32 columns each);
+//                      tcgen05.commit frees the stage and, after the unit's last
+//                      k-block, hands the accumulator to the epilogue.  Warp 1
+//                      also allocates and frees TMEM.
+//   warps 2-5          epilogue: tcgen05.ld 32 lanes x 32 columns, + bias[n] in
+//                      fp32, one rounding to the output type, store.  For a
+//                      Stream-K partial unit: publish the fp32 partial, take a
+//                      ticket, and the last contributor sums all partials in
+//                      ascending k order before the same epilogue.
+// The pipeline overlap of the A500 ladder's software-pipelining step
+// (kimm240.github.io/tvm, Step 5) is the S-stage ring plus the two accumulators:
+// the MMA of tile i+1 runs while the epilogue drains tile i.
+//
+// Every wait is bounded (wait_bounded): on expiry the CTA raises an abort flag,
+// records the site in the device status word, waits (bounded) for its own copies
+// and MMAs in flight, frees TMEM and returns.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+#include "work.cuh"
+
+namespace dg {
+
+constexpr int kBM = 128;          // MMA M (TMEM lanes)
+constexpr int kBK = 64;           // fp16 k-elements per stage = one 128-byte swizzle row
+constexpr int kTcThreads = 192;   // 6 warps
+constexpr int kEpiThreads = 128;  // warps 2-5
+
+template <int BN>
+struct TcConfig {
+  static constexpr int kStages = BN == 256 ? 4 : BN == 128 ? 6 : BN == 64 ? 8 : 10;
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;  // power of two >= 32
+  static constexpr int kChunk = BN < 32 ? BN : 32;             // TMEM columns per load
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128");
+  static_assert((2 * kStages + 5) * 8 + 16 <= kBarBytes, "barrier area");
+};
+
+struct TcArgs {
+  WorkSpec work;
+  int32_t Mm, Nm;         // MMA-view extents
+  void* C;                // output, row-major, ldc elements per row
+  int64_t ldc;
+  const float* bias;      // NULL or one fp32 per output column of C
+  float* workspace;       // split partials: 2 slots per CTA of kBM x BN fp32
+  int* tickets;           // one arrival counter per split tile (left at 0)
+  int* status;            // device status word
+  uint64_t wait_limit_ns;
+  int32_t a_mn, b_mn;     // operand majors in the MMA view (1 = MN-major)
+  uint32_t idesc;         // tcgen05 instruction descriptor
+};
+
+__device__ __forceinline__ void epi_bar_sync() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// AND of `v` over the 128 epilogue threads (also a barrier among them).
+__device__ __forceinline__ bool epi_all(bool v) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.and.pred po, 1, 128, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(out)
+      : "r"(uint32_t(v))
+      : "memory");
+  return out != 0;
+}
+
+template <int CW>
+__device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float (&v)[CW]) {
+  if constexpr (CW == 32) {
+    uint32_t r[32];
+    tmem_ld32(taddr, r);
+    tmem_wait_ld32(r);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+  } else {
+    static_assert(CW == 16, "chunk width");
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+          "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+          "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+  }
+}
+
+// Writes one chunk of CW accumulator columns held by this thread.
+// Not TRANS: C[mm][nn0 + j] = v[j] + bias[nn0 + j]  (thread = output row).
+// TRANS:     C[nn0 + j][mm] = v[j] + bias[mm]       (thread = output column).
+template <int CW, bool OUT_F16, bool TRANS>
+__device__ __forceinline__ void store_chunk(const TcArgs& a, int32_t mm, int32_t nn0,
+                                            const float (&v)[CW]) {
+  if (mm >= a.Mm || nn0 >= a.Nm) return;
+  const int32_t ncols = (a.Nm - nn0) < CW ? (a.Nm - nn0) : CW;
+  if constexpr (!TRANS) {
+    float o[CW];
+    const float* bp = a.bias ? a.bias + nn0 : nullptr;
+    const bool full = ncols == CW;
+    if (bp && full && (reinterpret_cast<uintptr_t>(bp) & 15) == 0) {
+#pragma unroll
+      for (int j = 0; j < CW; j += 4) {
+        const float4 b4 = __ldg(reinterpret_cast<const float4*>(bp + j));
+        o[j] = v[j] + b4.x; o[j + 1] = v[j + 1] + b4.y;
+        o[j + 2] = v[j + 2] + b4.z; o[j + 3] = v[j + 3] + b4.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < CW; ++j) o[j] = v[j] + ((bp && j < ncols) ? __ldg(bp + j) : 0.f);
+    }
+    if constexpr (OUT_F16) {
+      __half* row = reinterpret_cast<__half*>(a.C) + int64_t(mm) * a.ldc + nn0;
+      if (full && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+#pragma unroll
+        for (int j = 0; j < CW; j += 8) {
+          uint4 pk;
+          __half2 h0 = __floats2half2_rn(o[j], o[j + 1]);
+          __half2 h1 = __floats2half2_rn(o[j + 2], o[j + 3]);
+          __half2 h2 = __floats2half2_rn(o[j + 4], o[j + 5]);
+          __half2 h3 = __floats2half2_rn(o[j + 6], o[j + 7]);
+          pk.x = *reinterpret_cast<uint32_t*>(&h0);
+          pk.y = *reinterpret_cast<uint32_t*>(&h1);
+          pk.z = *reinterpret_cast<uint32_t*>(&h2);
+          pk.w = *reinterpret_cast<uint32_t*>(&h3);
+          *reinterpret_cast<uint4*>(row + j) = pk;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < CW; ++j)
+          if (j < ncols) row[j] = __float2half_rn(o[j]);
+      }
+    } else {
+      float* row = reinterpret_cast<float*>(a.C) + int64_t(mm) * a.ldc + nn0;
+      if (full && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+#pragma unroll
+        for (int j = 0; j < CW; j += 4)
+          *reinterpret_cast<float4*>(row + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < CW; ++j)
+          if (j < ncols) row[j] = o[j];
+      }
+    }
+  } else {
+    const float bv = a.bias ? __ldg(a.bias + mm) : 0.f;
+#pragma unroll
+    for (int j = 0; j < CW; ++j) {
+      if (j < ncols) {
+        const int64_t off = int64_t(nn0 + j) * a.ldc + mm;
+        if constexpr (OUT_F16)
+          reinterpret_cast<__half*>(a.C)[off] = __float2half_rn(v[j] + bv);
+        else
+          reinterpret_cast<float*>(a.C)[off] = v[j] + bv;
+      }
+    }
+  }
+}
+
+template <int BN, bool OUT_F16, bool TRANS>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmB, const TcArgs args) {
+  using Cfg = TcConfig<BN>;
+  constexpr int S = Cfg::kStages;
+  constexpr int CW = Cfg::kChunk;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;                         // S x 16 KiB
+  uint8_t* sB = smem + S * Cfg::kABytes;      // S x BN*128 B
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * Cfg::kBBytes);
+  uint64_t* full = bars;                      // TMA bytes landed in stage s
+  uint64_t* empty = bars + S;                 // MMAs reading stage s are done
+  uint64_t* acc_full = bars + 2 * S;          // accumulator b finished
+  uint64_t* acc_empty = acc_full + 2;         // accumulator b drained by the epilogue
+  uint64_t* drain = acc_empty + 2;            // clean-up after an abort
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&acc_full[b]), 1);
+      mbar_init(smem_u32(&acc_empty[b]), kEpiThreads);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtl wc{args.wait_limit_ns, args.status, abort_flag};
+  const WorkSpec& W = args.work;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      WorkIter it;
+      it.init(W, blockIdx.x);
+      Unit u;
+      int s = 0;
+      uint32_t ph = 0, issued = 0, issued_par = 0;
+      bool ok = true;
+      while (ok && it.next(W, u)) {
+        int32_t tm, tn;
+        tile_coords(W, u.tile, tm, tn);
+        for (int32_t kb = u.kb0; kb < u.kb1; ++kb) {
+          if (!wait_bounded(smem_u32(&empty[s]), ph ^ 1, wc, kSiteProducer)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full[s]);
+          mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
+          const uint32_t a_dst = smem_u32(sA + s * Cfg::kABytes);
+          const uint32_t b_dst = smem_u32(sB + s * Cfg::kBBytes);
+          const int32_t k0 = kb * kBK;
+          if (!args.a_mn) {
+            tma_load_2d(a_dst, &tmA, fb, k0, tm * kBM);
+          } else {
+            tma_load_2d(a_dst, &tmA, fb, tm * kBM, k0);
+            tma_load_2d(a_dst + 8192, &tmA, fb, tm * kBM + 64, k0);
+          }
+          if (!args.b_mn) {
+            tma_load_2d(b_dst, &tmB, fb, k0, tn * BN);
+          } else {
+            if constexpr (BN >= 64) {
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j)
+                tma_load_2d(b_dst + j * 8192, &tmB, fb, tn * BN + 64 * j, k0);
+            }
+          }
+          issued |= 1u << s;
+          issued_par = (issued_par & ~(1u << s)) | (ph << s);
+          if (++s == S) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      if (!ok) {  // let the copies still in flight land before the CTA exits
+        for (int t = 0; t < S; ++t)
+          if ((issued >> t) & 1) wait_drain(smem_u32(&full[t]), (issued_par >> t) & 1, wc);
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      WorkIter it;
+      it.init(W, blockIdx.x);
+      Unit u;
+      int s = 0, b = 0;
+      uint32_t ph = 0, aph = 0;
+      bool ok = true, any = false;
+      const uint32_t a_lbo = args.a_mn ? 8192u : 16u;
+      const uint32_t b_lbo = args.b_mn ? 8192u : 16u;
+      // advance per 16-deep k slice: 32 B along a K-major row, 16 rows (2 KiB) MN-major
+      const uint32_t a_step = args.a_mn ? (2048u >> 4) : (32u >> 4);
+      const uint32_t b_step = args.b_mn ? (2048u >> 4) : (32u >> 4);
+      while (ok && it.next(W, u)) {
+        if (!wait_bounded(smem_u32(&acc_empty[b]), aph ^ 1, wc, kSiteMmaAccum)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + uint32_t(b * BN);
+        for (int32_t kb = u.kb0; kb < u.kb1; ++kb) {
+          if (!wait_bounded(smem_u32(&full[s]), ph, wc, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = make_sdesc_sw128(smem_u32(sA + s * Cfg::kABytes), a_lbo, 1024);
+          const uint64_t bdesc = make_sdesc_sw128(smem_u32(sB + s * Cfg::kBBytes), b_lbo, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            tc_mma_f16(d_tmem, adesc + uint64_t(kk * a_step), bdesc + uint64_t(kk * b_step),
+                       args.idesc, (kb > u.kb0 || kk > 0) ? 1u : 0u);
+          any = true;
+          tc_commit(smem_u32(&empty[s]));
+          if (++s == S) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&acc_full[b]));
+        if (++b == 2) {
+          b = 0;
+          aph ^= 1;
+        }
+      }
+      if (!ok && any) {  // every MMA issued so far must finish before TMEM is freed
+        tc_commit(smem_u32(drain));
+        wait_drain(smem_u32(drain), 0, wc);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue --
+    const int q = warp & 3;            // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;     // accumulator row inside the tile
+    const int et = threadIdx.x - 64;   // 0..127
+    WorkIter it;
+    it.init(W, blockIdx.x);
+    Unit u;
+    int b = 0;
+    uint32_t aph = 0;
+    while (it.next(W, u)) {
+      const bool got = wait_bounded(smem_u32(&acc_full[b]), aph, wc, kSiteEpilogue);
+      if (!epi_all(got)) break;
+      tc_fence_after();
+      int32_t tm, tn;
+      tile_coords(W, u.tile, tm, tn);
+      const int32_t mm = tm * kBM + row;
+      const int32_t nbase = tn * BN;
+      const uint32_t taddr = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(b * BN);
+
+      if (!unit_is_partial(W, u)) {
+#pragma unroll 1
+        for (int c = 0; c < BN / CW; ++c) {
+          float v[CW];
+          __syncwarp();
+          tmem_load_chunk<CW>(taddr + c * CW, v);
+          store_chunk<CW, OUT_F16, TRANS>(args, mm, nbase + c * CW, v);
+        }
+      } else {
+        const int32_t st = u.tile - W.dp_tiles;  // split-tile index
+        const int32_t me = blockIdx.x;
+        const size_t slot_elems = size_t(kBM) * BN;
+        float* mine = args.workspace + size_t(split_slot(W, me, st)) * slot_elems;
+        // publish this CTA's fp32 partial (thread-contiguous: 128 B per thread per chunk)
+#pragma unroll 1
+        for (int c = 0; c < BN / CW; ++c) {
+          float v[CW];
+          __syncwarp();
+          tmem_load_chunk<CW>(taddr + c * CW, v);
+          float4* dst = reinterpret_cast<float4*>(mine + (size_t(c) * kBM + row) * CW);
+#pragma unroll
+          for (int j = 0; j < CW / 4; ++j)
+            __stcg(dst + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+        }
+        __threadfence();
+        epi_bar_sync();
+        int32_t first, last;
+        split_contributors(W, st, first, last);
+        if (et == 0) {
+          const int old = atomicAdd(&args.tickets[st], 1);
+          *last_flag = (old == last - first) ? 1 : 0;
+        }
+        epi_bar_sync();
+        if (*last_flag) {
+          __threadfence();
+#pragma unroll 1
+          for (int c = 0; c < BN / CW; ++c) {
+            float own[CW], acc[CW];
+            __syncwarp();
+            tmem_load_chunk<CW>(taddr + c * CW, own);
+#pragma unroll 1
+            for (int32_t r = first; r <= last; ++r) {
+              float v[CW];
+              if (r == me) {
+#pragma unroll
+                for (int j = 0; j < CW; ++j) v[j] = own[j];
+              } else {
+                const float4* src = reinterpret_cast<const float4*>(
+                    args.workspace + size_t(split_slot(W, r, st)) * slot_elems +
+                    (size_t(c) * kBM + row) * CW);
+#pragma unroll
+                for (int j = 0; j < CW / 4; ++j) {
+                  const float4 t = __ldcg(src + j);
+                  v[4 * j] = t.x; v[4 * j + 1] = t.y; v[4 * j + 2] = t.z; v[4 * j + 3] = t.w;
+                }
+              }
+              if (r == first) {
+#pragma unroll
+                for (int j = 0; j < CW; ++j) acc[j] = v[j];
+              } else {
+#pragma unroll
+                for (int j = 0; j < CW; ++j) acc[j] += v[j];
+              }
+            }
+            store_chunk<CW, OUT_F16, TRANS>(args, mm, nbase + c * CW, acc);
+          }
+          if (et == 0) atomicExch(&args.tickets[st], 0);  // ready for the next launch
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&acc_empty[b]));
+      if (++b == 2) {
+        b = 0;
+        aph ^= 1;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+}  // namespace dg

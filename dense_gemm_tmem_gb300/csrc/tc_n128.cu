@@ -1,0 +1,10 @@
+// Instantiations with a 128-column MMA tile (mid shapes; swapped M <= 128).
+#include "tc_launch.cuh"
+
+namespace dg {
+cudaError_t launch_tc_n128(const TcLaunch& L) {
+  if (L.trans)
+    return L.out_f16 ? launch_tc_inst<128, true, true>(L) : launch_tc_inst<128, false, true>(L);
+  return L.out_f16 ? launch_tc_inst<128, true, false>(L) : launch_tc_inst<128, false, false>(L);
+}
+}  // namespace dg

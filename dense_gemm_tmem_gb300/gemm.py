@@ -1,0 +1,98 @@
+"""Torch-facing wrapper over the C-ABI: tensors -> pointers, sizes, layout and
+the current CUDA stream.  PyTorch supplies device memory and streams only."""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+_DT = {torch.float16: B.GEMM_F16, torch.float32: B.GEMM_F32}
+ROW, COL = B.GEMM_ROW_MAJOR, B.GEMM_COL_MAJOR
+
+
+def problem_dims(A: torch.Tensor, Bm: torch.Tensor, a_major: int, b_major: int):
+    """(M, N, K) from storage tensors: A is (M, K) row-major or (K, M)
+    column-major; B is (K, N) row-major or (N, K) column-major."""
+    if A.dim() != 2 or Bm.dim() != 2:
+        raise ValueError("A and B must be 2-D")
+    M, K = (A.shape[0], A.shape[1]) if a_major == ROW else (A.shape[1], A.shape[0])
+    Kb, N = (Bm.shape[0], Bm.shape[1]) if b_major == ROW else (Bm.shape[1], Bm.shape[0])
+    if K != Kb:
+        raise ValueError("inner dimensions differ: %d vs %d" % (K, Kb))
+    return int(M), int(N), int(K)
+
+
+class Gemm:
+    """One library handle on one CUDA device."""
+
+    def __init__(self, device=0):
+        dev = torch.device("cuda", device) if isinstance(device, int) else torch.device(device)
+        self.device = dev
+        self.handle = B.gemm_create(dev.index if dev.index is not None else 0)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            torch.cuda.synchronize(self.device)
+            B.gemm_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            if getattr(self, "handle", None):
+                B.gemm_destroy(self.handle)
+                self.handle = None
+        except Exception:
+            pass
+
+    def _stream(self, stream):
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        return s.cuda_stream
+
+    def layout(self, A, Bm, C, a_major, b_major):
+        return B.layout(a_major, b_major, _DT[A.dtype], _DT[C.dtype])
+
+    def run(self, A, Bm, C, bias=None, a_major=ROW, b_major=ROW, stream=None) -> None:
+        """Enqueues C = A·B (+bias) into the preallocated row-major C."""
+        M, N, K = problem_dims(A, Bm, a_major, b_major)
+        for t in (A, Bm, C) + ((bias,) if bias is not None else ()):
+            if t.device != self.device:
+                raise ValueError("tensor on %s, handle on %s" % (t.device, self.device))
+            if not t.is_contiguous():
+                raise ValueError("tensors must be contiguous")
+        if A.dtype != Bm.dtype or A.dtype not in _DT or C.dtype not in _DT:
+            raise TypeError("A, B: both float16 or both float32; C: float16 or float32")
+        if tuple(C.shape) != (M, N):
+            raise ValueError("C has shape %s, expected (%d, %d)" % (tuple(C.shape), M, N))
+        if bias is not None and (bias.dtype != torch.float32 or tuple(bias.shape) != (N,)):
+            raise ValueError("bias must be float32 of shape (N,)")
+        rc = B.gemm_run(self.handle, M, N, K, A.data_ptr(), Bm.data_ptr(),
+                        bias.data_ptr() if bias is not None else None, C.data_ptr(),
+                        self.layout(A, Bm, C, a_major, b_major), self._stream(stream))
+        if rc != B.GEMM_OK:
+            raise B.GemmError(rc, "gemm_run")
+
+    def __call__(self, A, Bm, bias=None, a_major=ROW, b_major=ROW, out_dtype=torch.float32,
+                 stream=None) -> torch.Tensor:
+        M, N, _ = problem_dims(A, Bm, a_major, b_major)
+        C = torch.empty((M, N), dtype=out_dtype, device=self.device)
+        self.run(A, Bm, C, bias, a_major, b_major, stream)
+        return C
+
+    def status(self, stream=None) -> None:
+        """Synchronises the stream and raises if a device-side wait expired."""
+        rc = B.gemm_status(self.handle, self._stream(stream))
+        if rc != B.GEMM_OK:
+            raise B.GemmError(rc, "gemm_status (detail %d)" % B.gemm_status_detail(self.handle))
+
+    def set_option(self, option: int, value: int) -> None:
+        rc = B.gemm_set_option(self.handle, option, value)
+        if rc != B.GEMM_OK:
+            raise B.GemmError(rc, "gemm_set_option")
+
+    def plan(self, M, N, K, a_major=ROW, b_major=ROW, in_dtype=B.GEMM_F16,
+             out_dtype=B.GEMM_F32) -> dict:
+        rc, p = B.gemm_query_plan(self.handle, M, N, K,
+                                  B.layout(a_major, b_major, in_dtype, out_dtype))
+        if rc != B.GEMM_OK:
+            raise B.GemmError(rc, "gemm_query_plan")
+        return p.as_dict()

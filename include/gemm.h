@@ -1,0 +1,185 @@
+/*
+ * gemm.h: C-ABI of the GB300 (sm_103a) dense GEMM library.
+ *
+ *     C = A · B (+ bias)
+ *
+ * The operation is the matrix product with an added bias row, "Output =
+ * Input * Weight + Bias", which the FuseReductionEpilogue series
+ * (kimm240.github.io/tvm, "[TIR][Schedule] Add FuseReductionEpilogue
+ * primitive to fuse epilogue into reduction init", parts 1 and 2) fuses into the
+ * reduction by starting it from the bias.  fp16 inputs are multiplied and summed
+ * in fp32, the mixed-precision multiply-accumulate of the Tensor Core notes
+ * (je-d.tistory.com, "tvm").  fp32 inputs run the CUDA-core path of the
+ * "TVM Matrix Multiplication Optimization" ladder (kimm240.github.io/tvm,
+ * Steps 1-7).  Small and skinny shapes use the Stream-K decomposition of the
+ * leiblog.wang Stream-K post (Technical index).
+ *
+ * Conventions for every call:
+ *   - A is M x K, B is K x N, C is M x N; sizes are element counts (>= 0).
+ *   - Leading dimensions are packed: A row-major has lda = K, column-major lda = M;
+ *     B row-major has ldb = N, column-major ldb = K; C is row-major, ldc = N.
+ *   - A, B, bias, C are DEVICE pointers on the handle's device, owned by the
+ *     caller; the library never frees or retains them past the call.
+ *   - bias is NULL or N fp32 values, added to every row in fp32 before the
+ *     single rounding to the output type.
+ *   - stream is a cudaStream_t (NULL = the legacy default stream).
+ *   - Every function returns a gemm_status_t; nothing aborts, traps or prints
+ *     (set GEMM_LOG=1 in the environment to print each plan to stderr).
+ */
+#ifndef DGEMM_GB300_GEMM_H_
+#define DGEMM_GB300_GEMM_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gemm_ctx *gemm_handle_t;
+
+typedef enum {
+  GEMM_OK = 0,
+  GEMM_ERR_INVALID_ARG = -1,    /* bad size, null pointer, unknown enum */
+  GEMM_ERR_UNSUPPORTED = -2,    /* valid request this library does not run */
+  GEMM_ERR_ALLOC = -3,          /* device or host allocation failed */
+  GEMM_ERR_CUDA = -4,           /* a CUDA runtime/driver call failed */
+  GEMM_ERR_DEVICE_TIMEOUT = -5  /* a bounded device-side wait expired */
+} gemm_status_t;
+
+enum { GEMM_F16 = 0, GEMM_F32 = 1 };
+enum { GEMM_ROW_MAJOR = 0, GEMM_COL_MAJOR = 1 };
+
+/* Storage and types.  a_major/b_major: GEMM_ROW_MAJOR or GEMM_COL_MAJOR.
+ * in_dtype applies to both A and B.  Supported pairs: f16 -> f16, f16 -> f32,
+ * f32 -> f32.  f32 -> f16 returns GEMM_ERR_UNSUPPORTED. */
+typedef struct {
+  uint8_t a_major;
+  uint8_t b_major;
+  uint8_t in_dtype;
+  uint8_t out_dtype;
+} gemm_layout_t;
+
+/* Kernels the picker chooses among. */
+enum {
+  GEMM_KERNEL_TC = 0,       /* tcgen05/TMEM tensor-core GEMM, whole output tiles */
+  GEMM_KERNEL_STREAMK = 1,  /* the same kernel with Stream-K (or hybrid) k-splitting */
+  GEMM_KERNEL_SIMT = 2,     /* CUDA-core fp32 GEMM */
+  GEMM_KERNEL_FILL = 3,     /* K == 0: C = bias (or 0) */
+  GEMM_KERNEL_NONE = 4      /* M == 0 or N == 0: nothing to do */
+};
+
+/* What gemm_run will launch for a shape.  "MMA view": with swap_ab = 1 the
+ * kernel computes Cᵀ = Bᵀ·Aᵀ, so its M side is the problem's N and vice versa. */
+typedef struct {
+  int32_t kernel;      /* GEMM_KERNEL_* */
+  int32_t swap_ab;     /* 1: operands swapped (skinny M), C written transposed */
+  int32_t tile_m;      /* CTA tile rows (MMA view) */
+  int32_t tile_n;      /* CTA tile columns (MMA view) */
+  int32_t tile_k;      /* k-block depth per pipeline stage */
+  int32_t stages;      /* shared-memory pipeline stages */
+  int32_t grid;        /* CTAs launched */
+  int32_t tiles_m;     /* output tiles along the MMA M side */
+  int32_t tiles_n;     /* output tiles along the MMA N side */
+  int32_t k_iters;     /* k-blocks per output tile = ceil(K / tile_k) */
+  int32_t dp_tiles;    /* tiles computed whole, tile c + u*grid by CTA c */
+  int32_t sk_tiles;    /* tiles whose k-blocks are split evenly over all CTAs */
+  int32_t a_mn_major;  /* MMA-view A operand is M-contiguous (else K-contiguous) */
+  int32_t b_mn_major;  /* MMA-view B operand is N-contiguous (else K-contiguous) */
+  int32_t group_m;     /* tile raster: groups of group_m tile rows */
+  int32_t reserved;
+  int64_t workspace_bytes; /* fp32 partial-tile bytes the split needs */
+} gemm_plan_t;
+
+/* Options for tests and tuning (gemm_set_option).  Values < 0 restore the default. */
+enum {
+  GEMM_OPT_FORCE_KERNEL = 0,     /* GEMM_KERNEL_TC / _STREAMK / _SIMT, or -1 */
+  GEMM_OPT_FORCE_TILE_N = 1,     /* 16, 32, 64, 128, 256 (tensor-core path), or -1 */
+  GEMM_OPT_FORCE_GRID = 2,       /* CTA count for the split path, or -1 */
+  GEMM_OPT_WAIT_LIMIT_NS = 3,    /* bound on each device-side wait (default 2e9 ns) */
+  GEMM_OPT_MIN_SPLIT_ITERS = 4,  /* fewest k-blocks per CTA when splitting (default 2) */
+  GEMM_OPT_FORCE_SWAP_AB = 5,    /* 0 or 1, or -1 for the picker's choice */
+  GEMM_OPT_GROUP_M = 6           /* tile raster group height (default 16) */
+};
+
+/* Creates a handle on CUDA device `device`.  Allocates, on that device, the
+ * Stream-K workspace (fp32 partial tiles, bounded by 2 x SM count tiles of
+ * 128 x 256), the per-tile arrival counters and the device status word.
+ * The caller's current device is restored before returning.
+ * Errors: INVALID_ARG (h NULL, no such device), UNSUPPORTED (device is not
+ * compute capability 10.3), ALLOC, CUDA. */
+int gemm_create(gemm_handle_t *h, int device);
+
+/* Frees everything gemm_create allocated.  The caller must have synchronised
+ * every stream the handle was used on.  NULL is accepted (no-op). */
+int gemm_destroy(gemm_handle_t h);
+
+/* Enqueues C = A·B (+bias) on `stream` and returns without waiting.
+ * Picks the kernel with the rules gemm_query_plan reports.
+ * Requirements for fp16 inputs (tensor-core path, operands read by TMA):
+ *   A and B 16-byte aligned and each leading dimension a multiple of 8
+ *   elements; otherwise GEMM_ERR_UNSUPPORTED.  C and bias have no alignment
+ *   requirement.  fp32 inputs have no alignment requirement.
+ * M == 0 or N == 0: nothing is launched.  K == 0: C = bias (or 0).
+ * One handle must not run on two streams at once: its workspace is shared.
+ * Device-side wait timeouts are not seen here; call gemm_status.
+ * Errors: INVALID_ARG (negative size, NULL pointer with non-empty operand,
+ * unknown enum), UNSUPPORTED, CUDA (launch failed). */
+int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A,
+             const void *B, const float *bias, void *C, gemm_layout_t layout,
+             void *stream);
+
+/* Synchronises `stream`, then reads and clears the device status word.
+ * Returns GEMM_OK, GEMM_ERR_DEVICE_TIMEOUT (a bounded wait inside a kernel
+ * expired; the kernel stopped early and C is unspecified; the handle's
+ * counters are reset so the handle stays usable), or GEMM_ERR_CUDA (the
+ * stream reported an error). */
+int gemm_status(gemm_handle_t h, void *stream);
+
+/* Raw device status word read by the last gemm_status call (0 = none;
+ * otherwise 1 + the role whose wait expired: 1 TMA producer, 2 MMA issuer
+ * waiting for data, 3 MMA issuer waiting for an accumulator, 4 epilogue,
+ * 5 drain, 6 the self-test below). */
+int gemm_status_detail(gemm_handle_t h);
+
+/* Failure-path self-test: enqueues one CTA whose wait on an mbarrier that
+ * nothing completes gives up after limit_ns nanoseconds, records the expiry
+ * in the device status word and returns normally (no trap, no fault).  The
+ * next gemm_status call on `stream` must report GEMM_ERR_DEVICE_TIMEOUT with
+ * detail 6; the handle stays usable.  Errors: INVALID_ARG, CUDA. */
+int gemm_selftest_wait_timeout(gemm_handle_t h, int64_t limit_ns, void *stream);
+
+/* Sets an option (GEMM_OPT_*) on the handle. Errors: INVALID_ARG. */
+int gemm_set_option(gemm_handle_t h, int option, int64_t value);
+
+/* Fills *out with the plan gemm_run would launch for this shape on the
+ * handle's device with its current options.  Errors as gemm_run's checks. */
+int gemm_query_plan(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                    gemm_layout_t layout, gemm_plan_t *out);
+
+/* Human-readable name of a gemm_status_t (static storage). */
+const char *gemm_strerror(int code);
+
+/* ---- Host-only functions: need no GPU, no handle. ---------------------- */
+
+/* The tile picker for a device with `num_sms` SMs and default options. */
+int gemm_plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t layout,
+                  int num_sms, gemm_plan_t *out);
+
+/* The work units CTA `cta` of `plan` processes, in order: writes up to
+ * `max_units` triples (tile, k_begin, k_end) to out (3 int32 each) and returns
+ * the count (which may exceed max_units), or a negative gemm_status_t. */
+int gemm_work_units(const gemm_plan_t *plan, int cta, int32_t *out, int max_units);
+
+/* For split tile `sk_tile` (0-based within the split region): the first and
+ * last contributing CTA, in ascending k order.  Returns 0 or INVALID_ARG. */
+int gemm_split_contributors(const gemm_plan_t *plan, int sk_tile, int32_t *first,
+                            int32_t *last);
+
+/* Shared-memory row strides (in floats) of the fp32 CUDA-core kernel's A and B
+ * staging tiles, padded as storage_align(factor 32, offset 4) pads them. */
+int gemm_simt_smem_strides(int32_t *a_stride, int32_t *b_stride);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DGEMM_GB300_GEMM_H_ */

@@ -1,0 +1,332 @@
+"""GPU parity: every kernel family against the CPU oracle, element by element,
+on seeded inputs that span several tiles with ragged tails; closed-form inputs
+(permutations, integers) that must come out exact; edge cases; determinism;
+and the full-size workloads on sampled rows."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dense_gemm_tmem_gb300 import binding as B
+from dense_gemm_tmem_gb300 import inputs
+from dense_gemm_tmem_gb300.gemm import Gemm
+
+from gpu_helpers import (as_f64, check, reset_opts, run, sample_rows, set_opts, to_dev, TDT)
+
+pytestmark = pytest.mark.gpu
+F16, F32 = inputs.F16, inputs.F32
+TC, SK, SIMT = B.GEMM_KERNEL_TC, B.GEMM_KERNEL_STREAMK, B.GEMM_KERNEL_SIMT
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda", 0)
+
+
+@pytest.fixture(scope="module")
+def g(dev):
+    h = Gemm(dev)
+    yield h
+    h.close()
+
+
+@pytest.fixture(autouse=True)
+def _clean_options(request):
+    yield
+    if "g" in request.fixturenames:
+        reset_opts(request.getfixturevalue("g"))
+
+
+def problem(M, N, K, am, bm, idt, odt, bias, seed, kind="uniform"):
+    return inputs.make_problem("t", M, N, K, am, bm, idt, odt, kind, bias, seed)
+
+
+def full_check(g, dev, p):
+    C = run(g, p, dev)
+    ref = oracle.gemm(p.A, p.B, p.bias, a_major=p.a_major, b_major=p.b_major)
+    return check(as_f64(C), ref, p)
+
+
+# ---------------------------------------------------------------- layouts --
+@pytest.mark.parametrize("kernel", [-1, TC, SK])
+@pytest.mark.parametrize("am,bm", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("odt", [F16, F32])
+@pytest.mark.parametrize("bias", [False, True])
+def test_tc_layouts_ragged(g, dev, kernel, am, bm, odt, bias):
+    """296 x 520 x 200: 3 tile rows (the last 40 high), 3 tile columns of 256
+    (the last 8 wide), 4 k-blocks (the last 8 deep), all four storage pairs."""
+    set_opts(g, kernel=kernel)
+    p = problem(296, 520, 200, am, bm, F16, odt, bias, 10 + am + 2 * bm)
+    full_check(g, dev, p)
+
+
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("kernel", [TC, SK])
+def test_tc_tile_widths(g, dev, tile_n, kernel):
+    set_opts(g, kernel=kernel, tile_n=tile_n)
+    p = problem(400, 776, 328, 0, 0, F16, F32, True, 21)
+    full_check(g, dev, p)
+
+
+@pytest.mark.parametrize("M", [1, 3, 16, 40, 64, 100, 128])
+@pytest.mark.parametrize("bm", [0, 1])
+@pytest.mark.parametrize("odt", [F16, F32])
+def test_swapped_skinny(g, dev, M, bm, odt):
+    """Skinny M runs with swapped operands (Cᵀ = Bᵀ·Aᵀ) and a transposed store."""
+    p = problem(M, 1000, 520, 0, bm, F16, odt, True, 30 + M)
+    pl = g.plan(M, 1000, 520, 0, bm, B.GEMM_F16, B.GEMM_F16 if odt == F16 else B.GEMM_F32)
+    assert pl["swap_ab"] == 1
+    full_check(g, dev, p)
+
+
+@pytest.mark.parametrize("tile_n", [16, 32, 64, 128])
+@pytest.mark.parametrize("kernel", [TC, SK])
+def test_swapped_tile_widths(g, dev, tile_n, kernel):
+    set_opts(g, kernel=kernel, tile_n=tile_n, swap=1)
+    p = problem(72, 640, 1032, 0, 0, F16, F32, True, 41)
+    full_check(g, dev, p)
+
+
+@pytest.mark.parametrize("grid", [1, 5, 37, 152])
+def test_split_grid_sizes(g, dev, grid):
+    """Stream-K with awkward CTA counts: ranges start and end mid-tile."""
+    set_opts(g, kernel=SK, grid=grid)
+    p = problem(392, 600, 1480, 0, 1, F16, F32, True, 50 + grid)
+    full_check(g, dev, p)
+
+
+def test_split_many_contributors(g, dev):
+    """One output tile whose 256 k-blocks are split over up to 128 CTAs."""
+    p = problem(128, 128, 16384, 0, 0, F16, F32, True, 61)
+    pl = g.plan(128, 128, 16384)
+    assert pl["kernel"] == SK and pl["grid"] >= 64
+    full_check(g, dev, p)
+
+
+# ---------------------------------------------------------- closed forms --
+@pytest.mark.parametrize("kernel", [TC, SK])
+@pytest.mark.parametrize("bm", [0, 1])
+def test_permutation_rows_exact(g, dev, kernel, bm):
+    """A = P: C must be B's rows permuted, exactly (catches swizzle, descriptor
+    and lane-mapping mistakes, which permute or mix elements)."""
+    set_opts(g, kernel=kernel)
+    n = 512
+    perm = np.random.default_rng(7).permutation(n)
+    P = np.zeros((n, n), np.float16)
+    P[np.arange(n), perm] = 1
+    Bs = inputs.draw(inputs.storage_shape_b(n, 384, bm), 71, "uniform", F16)
+    Bl = Bs if bm == 0 else Bs.T
+    p = inputs.Problem("perm", n, 384, n, P, Bs, None, 0, bm, F16, F32)
+    got = as_f64(run(g, p, dev))
+    assert np.array_equal(got, Bl[perm].astype(np.float64))
+
+
+@pytest.mark.parametrize("kernel", [TC, SK])
+def test_permutation_columns_exact(g, dev, kernel):
+    set_opts(g, kernel=kernel)
+    n = 512
+    perm = np.random.default_rng(8).permutation(n)
+    P = np.zeros((n, n), np.float16)
+    P[np.arange(n), perm] = 1
+    A = inputs.draw((264, n), 72, "uniform", F16)
+    p = inputs.Problem("permc", 264, n, n, A, P, None, 0, 0, F16, F16)
+    got = as_f64(run(g, p, dev))
+    assert np.array_equal(got, A[:, np.argsort(perm)].astype(np.float64))
+
+
+@pytest.mark.parametrize("case", [
+    ("tc", 384, 512, 1024, 0, 1, F16, F32, {"kernel": TC}),
+    ("tc16", 384, 512, 1024, 0, 0, F16, F16, {"kernel": TC}),
+    ("sk", 384, 512, 1024, 1, 0, F16, F32, {"kernel": SK, "grid": 23}),
+    ("sk16", 256, 768, 2048, 0, 1, F16, F16, {"kernel": SK}),
+    ("swap", 16, 2048, 4096, 0, 0, F16, F32, {}),
+    ("simt", 200, 300, 500, 0, 0, F32, F32, {}),
+    ("simt_col", 200, 300, 500, 1, 1, F32, F32, {}),
+])
+def test_integer_inputs_exact(g, dev, case):
+    """Integer-valued inputs: every partial sum is an integer below 2^24, so
+    any summation order gives the exact result: values must match exactly
+    (+0 and -0 count as equal)."""
+    name, M, N, K, am, bm, idt, odt, opts = case
+    set_opts(g, **opts)
+    p = problem(M, N, K, am, bm, idt, odt, True, 80, kind="int")
+    ref = oracle.gemm(p.A, p.B, p.bias, a_major=am, b_major=bm)
+    assert np.abs(ref).max() <= 2048
+    assert np.array_equal(as_f64(run(g, p, dev)), ref)
+
+
+def test_all_ones_gives_k(g, dev):
+    M, N, K = 300, 264, 1000
+    p = inputs.Problem("ones", M, N, K, np.ones((M, K), np.float16), np.ones((K, N), np.float16),
+                       None, 0, 0, F16, F32)
+    assert np.array_equal(as_f64(run(g, p, dev)), np.full((M, N), float(K)))
+
+
+# ------------------------------------------------------------ edge cases --
+@pytest.mark.parametrize("odt", [F16, F32])
+def test_k_zero_gives_bias(g, dev, odt):
+    bias = torch.arange(40, dtype=torch.float32, device=dev) - 7.5
+    A = torch.empty((33, 0), dtype=torch.float16, device=dev)
+    Bt = torch.empty((0, 40), dtype=torch.float16, device=dev)
+    C = g(A, Bt, bias, out_dtype=TDT[odt])
+    g.status()
+    assert torch.equal(C.float(), bias.expand(33, 40).to(TDT[odt]).float())
+    C = g(A, Bt, None, out_dtype=TDT[odt])
+    g.status()
+    assert torch.count_nonzero(C) == 0
+
+
+def test_empty_outputs_are_noops(g, dev):
+    for M, N in ((0, 16), (16, 0)):
+        A = torch.zeros((M, 8), dtype=torch.float16, device=dev)
+        Bt = torch.zeros((8, N), dtype=torch.float16, device=dev)
+        C = g(A, Bt)
+        g.status()
+        assert C.shape == (M, N)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 8, 8), (300, 8, 64), (8, 8, 4096), (129, 257, 8)])
+def test_tiny_and_thin(g, dev, M, N, K):
+    p = problem(M, N, K, 0, 0, F16, F32, True, 90 + M)
+    full_check(g, dev, p)
+
+
+def test_fp16_alignment_rules(g, dev):
+    A = torch.zeros((64, 104), dtype=torch.float16, device=dev)
+    Bt = torch.zeros((100, 64), dtype=torch.float16, device=dev)
+    C = torch.empty((64, 64), dtype=torch.float32, device=dev)
+    with pytest.raises(ValueError):
+        g.run(A[:, :100], Bt, C)  # not contiguous -> rejected before the C-ABI
+    A2 = torch.zeros((64, 100), dtype=torch.float16, device=dev)  # lda = 100: not % 8
+    with pytest.raises(B.GemmError) as e:
+        g.run(A2, Bt, C)
+    assert e.value.code == B.GEMM_ERR_UNSUPPORTED
+    # a base that is not 16-byte aligned
+    flat = torch.zeros(64 * 64 + 1, dtype=torch.float16, device=dev)
+    A3 = flat[1:].view(64, 64)
+    B3 = torch.zeros((64, 64), dtype=torch.float16, device=dev)
+    rc = B.gemm_run(g.handle, 64, 64, 64, A3.data_ptr(), B3.data_ptr(), None, C.data_ptr(),
+                    B.layout(0, 0, B.GEMM_F16, B.GEMM_F32), 0)
+    assert rc == B.GEMM_ERR_UNSUPPORTED
+
+
+def test_unaligned_outputs_and_bias(g, dev):
+    """C and bias have no alignment rule: offset both by one element."""
+    p = problem(130, 264, 72, 0, 0, F16, F16, True, 95)
+    A, Bt, bias = to_dev(p, dev)
+    cflat = torch.zeros(130 * 264 + 1, dtype=torch.float16, device=dev)
+    bflat = torch.zeros(265, dtype=torch.float32, device=dev)
+    bflat[1:] = bias
+    rc = B.gemm_run(g.handle, 130, 264, 72, A.data_ptr(), Bt.data_ptr(), bflat[1:].data_ptr(),
+                    cflat[1:].data_ptr(), B.layout(0, 0, B.GEMM_F16, B.GEMM_F16),
+                    torch.cuda.current_stream(dev).cuda_stream)
+    assert rc == 0
+    g.status()
+    ref = oracle.gemm(p.A, p.B, p.bias)
+    check(cflat[1:].view(130, 264).double().cpu().numpy(), ref, p)
+
+
+@pytest.mark.parametrize("am,bm", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("M,N,K", [(130, 70, 33), (257, 129, 128), (5, 3, 2)])
+def test_simt_layouts_ragged(g, dev, am, bm, M, N, K):
+    p = problem(M, N, K, am, bm, F32, F32, True, 100 + M)
+    full_check(g, dev, p)
+
+
+def test_simt_unaligned_pointers(g, dev):
+    p = problem(100, 68, 36, 0, 0, F32, F32, False, 111)
+    A, Bt, _ = to_dev(p, dev)
+    af = torch.zeros(A.numel() + 1, dtype=torch.float32, device=dev)
+    af[1:] = A.flatten()
+    C = torch.empty((100, 68), dtype=torch.float32, device=dev)
+    rc = B.gemm_run(g.handle, 100, 68, 36, af[1:].data_ptr(), Bt.data_ptr(), None, C.data_ptr(),
+                    B.layout(0, 0, B.GEMM_F32, B.GEMM_F32),
+                    torch.cuda.current_stream(dev).cuda_stream)
+    assert rc == 0
+    g.status()
+    check(as_f64(C), oracle.gemm(p.A, p.B), p)
+
+
+def test_fp32_to_fp16_unsupported(g, dev):
+    A = torch.zeros((8, 8), dtype=torch.float32, device=dev)
+    with pytest.raises(B.GemmError) as e:
+        g(A, A, out_dtype=torch.float16)
+    assert e.value.code == B.GEMM_ERR_UNSUPPORTED
+
+
+def test_side_stream(g, dev):
+    p = problem(256, 512, 256, 0, 1, F16, F32, True, 120)
+    A, Bt, bias = to_dev(p, dev)
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        C = g(A, Bt, bias, 0, 1, stream=s)
+    g.status(s)
+    check(as_f64(C), oracle.gemm(p.A, p.B, p.bias, b_major=1), p)
+
+
+# ----------------------------------------------------------- determinism --
+@pytest.mark.parametrize("kernel,grid", [(SK, -1), (SK, 29), (TC, -1)])
+def test_bitwise_repeatable(g, dev, kernel, grid):
+    set_opts(g, kernel=kernel, grid=grid)
+    p = problem(520, 776, 2056, 0, 1, F16, F32, True, 130, kind="normal")
+    A, Bt, bias = to_dev(p, dev)
+    C1 = g(A, Bt, bias, 0, 1)
+    C2 = g(A, Bt, bias, 0, 1)
+    g.status()
+    assert torch.equal(C1, C2)
+
+
+# ------------------------------------------------------ failure detection --
+def test_wait_timeout_selftest(g, dev):
+    """A bounded device wait that nothing completes must expire, be reported
+    by gemm_status, and leave the handle and context usable."""
+    s = torch.cuda.current_stream(dev).cuda_stream
+    assert B.gemm_selftest_wait_timeout(g.handle, 5_000_000, s) == B.GEMM_OK
+    assert B.gemm_status(g.handle, s) == B.GEMM_ERR_DEVICE_TIMEOUT
+    assert B.gemm_status_detail(g.handle) == 6
+    assert B.gemm_status(g.handle, s) == B.GEMM_OK
+    p = problem(256, 256, 512, 0, 0, F16, F32, False, 140)
+    full_check(g, dev, p)
+
+
+# ------------------------------------------------- the named workloads --
+def test_workload_512_full(g, dev):
+    p = inputs.WORKLOADS["gemm512_f16_f32out"].make()
+    full_check(g, dev, p)
+
+
+def test_workload_sgemm2048_full(g, dev):
+    p = inputs.WORKLOADS["sgemm2048_f32"].make()
+    assert g.plan(2048, 2048, 2048, 0, 0, B.GEMM_F32, B.GEMM_F32)["kernel"] == SIMT
+    full_check(g, dev, p)
+
+
+@pytest.mark.parametrize("M", [1, 16, 64, 128])
+def test_workload_skinny_full(g, dev, M):
+    p = inputs.WORKLOADS["skinny_m%d_4096" % M].make()
+    full_check(g, dev, p)
+
+
+@pytest.mark.parametrize("name,kind", [("gemm8192_f16_bias_f16out", None),
+                                       ("gemm8192_f16_bias_f16out", "int"),
+                                       ("gemm16384_f16_f16out", None)])
+def test_workload_large_sampled_rows(g, dev, name, kind):
+    """Full-size launch (the configuration the benchmark times), checked on one
+    seeded row per 128-row tile plus edge rows, all N columns each."""
+    w = inputs.WORKLOADS[name]
+    p = w.make(kind=kind)
+    pl = g.plan(w.M, w.N, w.K, w.a_major, w.b_major, B.GEMM_F16, B.GEMM_F16)
+    assert pl["kernel"] == TC and pl["tile_n"] == 256
+    C = run(g, p, dev)
+    rows = sample_rows(w.M, 7)
+    got = as_f64(C, rows)
+    del C
+    ref = oracle.gemm_rows(p.A, p.B, p.bias, a_major=p.a_major, b_major=p.b_major, rows=rows)
+    if kind == "int":
+        assert np.abs(ref).max() <= 2048
+        assert np.array_equal(got, ref)
+    else:
+        check(got, ref, p, rows)

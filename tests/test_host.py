@@ -1,0 +1,155 @@
+"""Host-side checks that need no GPU: the library loads and exports every
+declared symbol, the tile picker, the Stream-K work partition against the
+oracle's reading, the padded staging strides, and source/binary lints."""
+import os
+import re
+import subprocess
+
+import pytest
+
+from dense_gemm_tmem_gb300 import binding as B
+from oracle import schedule
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SMS = 152
+F16, F32 = B.GEMM_F16, B.GEMM_F32
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return B.load()
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"^(?:int|const char \*)\s*(gemm_\w+)\(", txt, re.M)
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_no_library_gemm_or_cuda_driver_link(lib):
+    """The product links no cuBLAS/CUTLASS and does not link libcuda directly."""
+    out = subprocess.run(["nm", "-D", "--undefined-only", B.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    assert "cublas" not in out.lower() and "cutlass" not in out.lower()
+    deps = subprocess.run(["ldd", B.library_path()], capture_output=True, text=True).stdout
+    assert "libcuda.so" not in deps and "libcublas" not in deps
+
+
+def test_sources_use_no_multicast_or_wgmma():
+    csrc = os.path.join(ROOT, "dense_gemm_tmem_gb300", "csrc")
+    for fn in os.listdir(csrc):
+        txt = open(os.path.join(csrc, fn)).read()
+        assert ".multicast::cluster" not in txt, fn
+        assert "wgmma" not in txt, fn
+        assert "mma.sync" not in txt and "wmma::" not in txt, fn
+
+
+def test_strerror(lib):
+    assert B.gemm_strerror(0) == "GEMM_OK"
+    assert "UNSUPPORTED" in B.gemm_strerror(-2)
+    assert B.gemm_strerror(12345) == "unknown gemm status"
+
+
+def plan(M, N, K, am=0, bm=0, idt=F16, odt=F32, sms=SMS):
+    rc, p = B.gemm_plan_for(M, N, K, B.layout(am, bm, idt, odt), sms)
+    return rc, p
+
+
+def test_picker_large_square_whole_tiles():
+    rc, p = plan(8192, 8192, 8192, 0, 1, F16, F16)
+    assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC
+    assert (p.tile_m, p.tile_n, p.tile_k) == (128, 256, 64)
+    assert (p.tiles_m, p.tiles_n, p.k_iters) == (64, 32, 128)
+    assert (p.dp_tiles, p.sk_tiles, p.grid) == (2048, 0, SMS)
+    assert (p.swap_ab, p.a_mn_major, p.b_mn_major) == (0, 0, 0)
+    rc, p = plan(16384, 16384, 16384, 0, 0, F16, F16)
+    assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC and p.b_mn_major == 1
+    assert p.dp_tiles == 128 * 64 and p.workspace_bytes == 0
+
+
+def test_picker_small_shape_is_split():
+    rc, p = plan(512, 512, 512)
+    assert rc == 0 and p.kernel == B.GEMM_KERNEL_STREAMK
+    assert (p.tile_n, p.tiles_m, p.tiles_n, p.k_iters) == (256, 4, 2, 8)
+    assert p.sk_tiles == 8 and p.dp_tiles == 0
+    assert p.grid == 32  # 64 k-blocks, at least 2 per CTA
+    assert p.workspace_bytes == 2 * 32 * 128 * 256 * 4
+
+
+@pytest.mark.parametrize("M,bn", [(1, 16), (16, 16), (64, 64), (128, 128)])
+def test_picker_skinny_swaps_operands(M, bn):
+    rc, p = plan(M, 4096, 4096)
+    assert rc == 0 and p.swap_ab == 1 and p.tile_n == bn
+    assert p.kernel == B.GEMM_KERNEL_STREAMK
+    assert (p.tiles_m, p.tiles_n, p.k_iters) == (32, 1, 64)
+    assert p.grid == SMS
+    assert (p.a_mn_major, p.b_mn_major) == (1, 0)  # Bᵀ is N-contiguous, A is K-contiguous
+
+
+def test_picker_hybrid_tail():
+    # 314 tiles on 152 SMs: one whole wave, then 162 tiles split evenly
+    rc, p = plan(128 * 157, 256 * 2, 1024)
+    assert rc == 0 and p.kernel == B.GEMM_KERNEL_STREAMK
+    assert (p.dp_tiles, p.sk_tiles, p.grid) == (152, 162, SMS)
+    # 200 tiles (1 wave + 48): all split
+    rc, p = plan(128 * 10, 256 * 20, 1024)
+    assert (p.dp_tiles, p.sk_tiles) == (0, 200)
+
+
+def test_picker_fp32_and_degenerate():
+    rc, p = plan(2048, 2048, 2048, 0, 0, F32, F32)
+    assert rc == 0 and p.kernel == B.GEMM_KERNEL_SIMT and p.grid == 256
+    assert plan(64, 64, 64, 0, 0, F32, F16)[0] == B.GEMM_ERR_UNSUPPORTED
+    assert plan(10, 10, 0)[1].kernel == B.GEMM_KERNEL_FILL
+    assert plan(0, 10, 10)[1].kernel == B.GEMM_KERNEL_NONE
+    assert plan(10, 0, 10)[1].kernel == B.GEMM_KERNEL_NONE
+    assert plan(-1, 10, 10)[0] == B.GEMM_ERR_INVALID_ARG
+    rc, _ = B.gemm_plan_for(8, 8, 8, B.layout(2, 0, F16, F32), SMS)
+    assert rc == B.GEMM_ERR_INVALID_ARG
+
+
+def test_picker_fp16_tma_stride_rule():
+    assert plan(64, 64, 100)[0] == B.GEMM_ERR_UNSUPPORTED       # A row-major, K % 8
+    assert plan(64, 100, 64)[0] == B.GEMM_ERR_UNSUPPORTED       # B row-major, N % 8
+    assert plan(64, 100, 64, 0, 1)[0] == 0                      # B col-major: ldb = K
+    assert plan(100, 64, 64, 1, 0)[0] == B.GEMM_ERR_UNSUPPORTED  # A col-major, M % 8
+
+
+PLANS = [(512, 512, 512, 0, 0), (1, 4096, 4096, 0, 0), (16, 4096, 4096, 0, 0),
+         (128, 4096, 4096, 0, 0), (128 * 157, 512, 1024, 0, 0), (1280, 5120, 1024, 0, 0),
+         (296, 520, 200, 0, 1), (1000, 1000, 4000, 1, 1), (8192, 8192, 8192, 0, 1)]
+
+
+@pytest.mark.parametrize("M,N,K,am,bm", PLANS)
+def test_work_units_match_oracle_reading(M, N, K, am, bm):
+    rc, p = plan(M, N, K, am, bm)
+    assert rc == 0
+    ref = schedule.streamk_units(p.dp_tiles, p.sk_tiles, p.k_iters, p.grid)
+    for c in range(p.grid):
+        assert B.gemm_work_units(p, c) == ref[c]
+    # contributors of each split tile: the CTAs touching it, in k order
+    owners = {}
+    for c, units in enumerate(ref):
+        for tile, k0, _ in units:
+            if tile >= p.dp_tiles:
+                owners.setdefault(tile - p.dp_tiles, []).append((k0, c))
+    for s in range(p.sk_tiles):
+        cs = [c for _, c in sorted(owners[s])]
+        assert B.gemm_split_contributors(p, s) == (cs[0], cs[-1])
+        assert cs == list(range(cs[0], cs[-1] + 1))
+
+
+def test_simt_staging_strides_follow_storage_align():
+    a, b = B.gemm_simt_smem_strides()
+    assert a == schedule.storage_align_strides([8, 128], [(32, 4), None])[0]
+    assert b == schedule.storage_align_strides([8, 128], [(32, 4), None])[0]
