@@ -84,6 +84,8 @@ def load(build_if_missing: bool = True):
         "gemm_split_contributors": (c_int, [P(gemm_plan_t), c_int, P(c_int32), P(c_int32)]),
         "gemm_simt_smem_strides": (c_int, [P(c_int32), P(c_int32)]),
         "gemm_selftest_wait_timeout": (c_int, [c_void_p, c_int64, c_void_p]),
+        "gemm_run_noalloc": (c_int, [c_int64, c_int64, c_int64, c_void_p, c_void_p, c_void_p,
+                                     c_void_p, gemm_layout_t, c_void_p, c_void_p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -173,3 +175,12 @@ def gemm_simt_smem_strides():
 
 def gemm_selftest_wait_timeout(h, limit_ns: int, stream_ptr) -> int:
     return load().gemm_selftest_wait_timeout(c_void_p(h), int(limit_ns), c_void_p(stream_ptr))
+
+
+def gemm_run_noalloc(M, N, K, A_ptr, B_ptr, bias_ptr, C_ptr, lay: gemm_layout_t, stream_ptr,
+                     status_ptr=None) -> int:
+    """The allocation-free entry point (no handle; scratch compiled into the
+    library).  Pointers are device addresses on the current device."""
+    return load().gemm_run_noalloc(int(M), int(N), int(K), c_void_p(A_ptr), c_void_p(B_ptr),
+                                   c_void_p(bias_ptr), c_void_p(C_ptr), lay,
+                                   c_void_p(stream_ptr), c_void_p(status_ptr))

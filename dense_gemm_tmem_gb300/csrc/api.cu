@@ -20,16 +20,6 @@ constexpr int kTicketCap = 16384;     // split tiles one launch may have
 constexpr int kTmapCacheSize = 32;
 constexpr int64_t kMaxCoord = (int64_t(1) << 31) - 1024;  // TMA coordinates are int32
 
-struct Options {
-  int force_kernel = -1;
-  int force_tile_n = -1;
-  int force_grid = -1;
-  int min_split_iters = 2;
-  int force_swap = -1;
-  int group_m = 16;
-  uint64_t wait_limit_ns = 2000000000ull;
-};
-
 struct TmapKey {
   const void* ptr;
   int64_t rows, k;
@@ -57,6 +47,8 @@ bool log_enabled() {
 }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
 
 // ------------------------------------------------------------ tile picker --
 // Chooses kernel, tile, split and grid for a shape.  Rules:
@@ -205,12 +197,6 @@ WorkSpec spec_of(const gemm_plan_t& p) {
 }
 
 // ------------------------------------------------------------- TMA maps --
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                   CUtensorMapFloatOOBfill);
-
 EncodeTiledFn encode_fn() {
   static EncodeTiledFn fn = nullptr;
   static std::once_flag once;
@@ -225,7 +211,6 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-}  // namespace
 }  // namespace dg
 
 struct gemm_ctx {

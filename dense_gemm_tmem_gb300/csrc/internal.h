@@ -7,9 +7,35 @@
 
 #include <cstdint>
 
+#include "../../include/gemm.h"
 #include "tc_kernel.cuh"
 
 namespace dg {
+
+// Picker options (gemm_set_option; defaults below).
+struct Options {
+  int force_kernel = -1;
+  int force_tile_n = -1;
+  int force_grid = -1;
+  int min_split_iters = 2;
+  int force_swap = -1;
+  int group_m = 16;
+  uint64_t wait_limit_ns = 2000000000ull;
+};
+
+// The tile picker (api.cu).
+int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
+             const Options& o, gemm_plan_t* p);
+WorkSpec spec_of(const gemm_plan_t& p);
+
+// cuTensorMapEncodeTiled, reached through the runtime's entry-point query
+// (NULL if the driver does not provide it).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn();
 
 // One tensor-core launch, fully described.
 struct TcLaunch {

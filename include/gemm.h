@@ -148,6 +148,45 @@ int gemm_status_detail(gemm_handle_t h);
  * detail 6; the handle stays usable.  Errors: INVALID_ARG, CUDA. */
 int gemm_selftest_wait_timeout(gemm_handle_t h, int64_t limit_ns, void *stream);
 
+/* C = A·B (+bias) for callers that cannot allocate device memory.
+ * (The pages have no counterpart to this entry point.)
+ *
+ * Some callers cannot call cudaMalloc: a plugin inside a host application whose
+ * own caching allocator has reserved the device memory (an outside cudaMalloc
+ * may fail, or bypasses that allocator's accounting), or a latency-critical
+ * path where cudaMalloc/cudaFree would synchronise the device.  gemm_create
+ * allocates; this call does not, and needs no handle.  It runs the same
+ * tensor-core kernel and picker as gemm_run, with the split path's scratch in
+ * a fixed array compiled into the library: 16 MiB of fp32 partial tiles, 4096
+ * split-tile counters and one status word.  Every GPU that loads the library
+ * holds that array until the process exits.
+ *
+ * Arguments are gemm_run's, minus the handle: A, B, bias, C are device pointers
+ * on the CURRENT device, owned by the caller; stream belongs to that device.
+ * dev_status: NULL, or a device int the caller owns that the kernel sets to a
+ * nonzero site code (as gemm_status_detail reports) if a bounded device-side
+ * wait expires; with NULL such an expiry is recorded only in the array.
+ *
+ * The first call on a device looks up the array's device address with that
+ * device current (cudaGetSymbolAddress) and caches it; make that first call
+ * before any stream capture.  Calls never call cudaMalloc, cudaFree or any
+ * allocating routine.
+ *
+ * All calls share the one array, which keeps the last call's contents; each
+ * call clears the counters it uses (cudaMemsetAsync on `stream`) before its
+ * kernel.  Calls whose kernels overlap on the GPU (different streams, no
+ * ordering between them) race on the array and give wrong results: order them.
+ *
+ * Limits: fp16 inputs only (fp32 inputs return GEMM_ERR_UNSUPPORTED; use
+ * gemm_run).  A split whose partial tiles exceed 16 MiB runs on fewer CTAs
+ * so that they fit; a split over more than 4096 output tiles is refused with
+ * GEMM_ERR_UNSUPPORTED (the counters would not fit).  Other errors as gemm_run:
+ * INVALID_ARG, UNSUPPORTED (alignment, device not compute capability 10.3),
+ * CUDA. */
+int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, const void *B,
+                     const float *bias, void *C, gemm_layout_t layout, void *stream,
+                     int *dev_status);
+
 /* Sets an option (GEMM_OPT_*) on the handle. Errors: INVALID_ARG. */
 int gemm_set_option(gemm_handle_t h, int option, int64_t value);
 
