@@ -22,9 +22,10 @@ GEMM_ERR_DEVICE_TIMEOUT = -5
 
 GEMM_F16, GEMM_F32 = 0, 1
 GEMM_ROW_MAJOR, GEMM_COL_MAJOR = 0, 1
-GEMM_KERNEL_TC, GEMM_KERNEL_STREAMK, GEMM_KERNEL_SIMT, GEMM_KERNEL_FILL, GEMM_KERNEL_NONE = range(5)
+(GEMM_KERNEL_TC, GEMM_KERNEL_STREAMK, GEMM_KERNEL_SIMT, GEMM_KERNEL_FILL, GEMM_KERNEL_NONE,
+ GEMM_KERNEL_TC2) = range(6)
 (GEMM_OPT_FORCE_KERNEL, GEMM_OPT_FORCE_TILE_N, GEMM_OPT_FORCE_GRID, GEMM_OPT_WAIT_LIMIT_NS,
- GEMM_OPT_MIN_SPLIT_ITERS, GEMM_OPT_FORCE_SWAP_AB, GEMM_OPT_GROUP_M) = range(7)
+ GEMM_OPT_MIN_SPLIT_ITERS, GEMM_OPT_FORCE_SWAP_AB, GEMM_OPT_GROUP_M, GEMM_OPT_PAIR) = range(8)
 
 
 class gemm_layout_t(ctypes.Structure):

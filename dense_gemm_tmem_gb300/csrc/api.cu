@@ -12,6 +12,7 @@
 
 #include "../../include/gemm.h"
 #include "internal.h"
+#include "tc2_kernel.cuh"
 
 namespace dg {
 
@@ -103,12 +104,52 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
   const int64_t ldb = L.b_major == GEMM_ROW_MAJOR ? N : K;
   if (lda % 8 != 0 || ldb % 8 != 0) return GEMM_ERR_UNSUPPORTED;  // TMA stride rule
 
+  const bool forced_pair = o.force_kernel == GEMM_KERNEL_TC2;
   const bool swap = o.force_swap >= 0 ? (o.force_swap != 0)
+                    : forced_pair     ? false
                                       : (L.a_major == GEMM_ROW_MAJOR && M <= 128 && N >= 2 * M);
   const int64_t Mm = swap ? N : M;
   const int64_t Nm = swap ? M : N;
   const int a_mn = swap ? (L.b_major == GEMM_ROW_MAJOR) : (L.a_major == GEMM_COL_MAJOR);
   const int b_mn = swap ? (L.a_major == GEMM_COL_MAJOR) : (L.b_major == GEMM_ROW_MAJOR);
+
+  // Two-SM kernel (CTA pairs, 256 x 256 tiles, whole tiles only): when asked
+  // for, or when the pair tiles fill whole waves of pairs (a multiple of the
+  // resident pairs, or at least four waves) the same way the one-SM rule below
+  // decides for whole tiles.
+  const int64_t pairs = o.pair_clusters > 0 ? o.pair_clusters : num_sms / 2;
+  if (forced_pair && (swap || pairs < 1 || o.force_tile_n > 0)) return GEMM_ERR_UNSUPPORTED;
+  if (!swap && pairs >= 1 && o.force_tile_n <= 0 &&
+      (forced_pair || (o.force_kernel < 0 && o.pair != 0))) {
+    const int64_t t2m = ceil_div(Mm, kPairBM), t2n = ceil_div(Nm, kPairBN);
+    const int64_t T2 = t2m * t2n;
+    const int64_t I2 = ceil_div(K, kBK);
+    bool use = forced_pair || o.pair == 1;
+    if (!use && o.force_grid <= 0 && T2 >= pairs)
+      use = (T2 % pairs == 0) || (T2 / pairs >= 4);
+    if (use) {
+      if (T2 > INT32_MAX / 2 || I2 > INT32_MAX / 2) return GEMM_ERR_UNSUPPORTED;
+      int64_t np = std::min(pairs, T2);
+      if (o.force_grid > 0) np = std::max<int64_t>(1, std::min<int64_t>(np, o.force_grid / 2));
+      p->kernel = GEMM_KERNEL_TC2;
+      p->swap_ab = 0;
+      p->tile_m = kPairBM;
+      p->tile_n = kPairBN;
+      p->tile_k = kBK;
+      p->stages = Tc2Config::kStages;
+      p->grid = int32_t(2 * np);
+      p->tiles_m = int32_t(t2m);
+      p->tiles_n = int32_t(t2n);
+      p->k_iters = int32_t(I2);
+      p->dp_tiles = int32_t(T2);
+      p->sk_tiles = 0;
+      p->a_mn_major = a_mn;
+      p->b_mn_major = b_mn;
+      p->group_m = std::max(1, o.group_m);
+      p->workspace_bytes = 0;
+      return GEMM_OK;
+    }
+  }
 
   int bn;
   if (o.force_tile_n > 0) {
@@ -191,7 +232,7 @@ WorkSpec spec_of(const gemm_plan_t& p) {
   w.k_iters = p.k_iters;
   w.dp_tiles = p.dp_tiles;
   w.sk_tiles = p.sk_tiles;
-  w.grid = p.grid;
+  w.grid = p.kernel == GEMM_KERNEL_TC2 ? p.grid / 2 : p.grid;  // pairs work as one unit
   w.group_m = p.group_m;
   return w;
 }
@@ -301,6 +342,7 @@ void log_plan(const gemm_plan_t& p, int64_t M, int64_t N, int64_t K) {
 }  // namespace
 
 cudaError_t launch_tc(const TcLaunch& L) {
+  if (L.pair) return launch_tc2(L);
   if (L.bn == 256) return launch_tc_n256(L);
   if (L.bn == 128) return launch_tc_n128(L);
   return launch_tc_small(L);
@@ -349,10 +391,13 @@ int gemm_plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t layout, int num
 }
 
 int gemm_work_units(const gemm_plan_t* plan, int cta, int32_t* out, int max_units) {
-  if (!plan || cta < 0 || cta >= plan->grid || max_units < 0 || (max_units > 0 && !out))
+  if (!plan || max_units < 0 || (max_units > 0 && !out)) return GEMM_ERR_INVALID_ARG;
+  if (plan->kernel != GEMM_KERNEL_TC && plan->kernel != GEMM_KERNEL_STREAMK &&
+      plan->kernel != GEMM_KERNEL_TC2)
     return GEMM_ERR_INVALID_ARG;
-  if (plan->kernel != GEMM_KERNEL_TC && plan->kernel != GEMM_KERNEL_STREAMK)
-    return GEMM_ERR_INVALID_ARG;
+  // for the two-SM kernel `cta` numbers CTA pairs
+  const int units = plan->kernel == GEMM_KERNEL_TC2 ? plan->grid / 2 : plan->grid;
+  if (cta < 0 || cta >= units) return GEMM_ERR_INVALID_ARG;
   const dg::WorkSpec w = dg::spec_of(*plan);
   dg::WorkIter it;
   it.init(w, cta);
@@ -399,6 +444,8 @@ int gemm_create(gemm_handle_t* out, int device) {
     if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return GEMM_ERR_CUDA;
     if (prop.major != 10 || prop.minor != 3) return GEMM_ERR_UNSUPPORTED;
     h->num_sms = prop.multiProcessorCount;
+    const int pairs = dg::tc2_max_active_clusters(true);
+    h->opt.pair_clusters = pairs > 0 ? std::min(pairs, h->num_sms / 2) : h->num_sms / 2;
     h->workspace_bytes = size_t(2) * h->num_sms * dg::kBM * dg::kMaxTileN * sizeof(float);
     if (cudaMalloc(&h->workspace, h->workspace_bytes) != cudaSuccess) return GEMM_ERR_ALLOC;
     if (cudaMalloc(&h->tickets, sizeof(int) * dg::kTicketCap) != cudaSuccess)
@@ -437,7 +484,7 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value) {
   switch (option) {
     case GEMM_OPT_FORCE_KERNEL:
       if (value >= 0 && value != GEMM_KERNEL_TC && value != GEMM_KERNEL_STREAMK &&
-          value != GEMM_KERNEL_SIMT)
+          value != GEMM_KERNEL_SIMT && value != GEMM_KERNEL_TC2)
         return GEMM_ERR_INVALID_ARG;
       o.force_kernel = value < 0 ? d.force_kernel : int(value);
       return GEMM_OK;
@@ -462,6 +509,10 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value) {
       return GEMM_OK;
     case GEMM_OPT_GROUP_M:
       o.group_m = value <= 0 ? d.group_m : int(std::min<int64_t>(value, 1 << 16));
+      return GEMM_OK;
+    case GEMM_OPT_PAIR:
+      if (value > 1) return GEMM_ERR_INVALID_ARG;
+      o.pair = value < 0 ? d.pair : int(value);
       return GEMM_OK;
     default:
       return GEMM_ERR_INVALID_ARG;
@@ -517,15 +568,19 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, co
   const int64_t Mm = swap ? N : M;
   const int64_t Nm = swap ? M : N;
 
+  const bool pair = plan.kernel == GEMM_KERNEL_TC2;
   dg::TcLaunch L;
   L.bn = plan.tile_n;
   L.out_f16 = layout.out_dtype == GEMM_F16;
   L.trans = swap;
+  L.pair = pair;
   L.grid = plan.grid;
   L.stream = stream;
+  // each CTA loads 128 rows of A; a pair CTA loads half of the 256-column B tile
   rc = dg::encode_operand(h, &L.tmA, opA, Mm, K, plan.a_mn_major, dg::kBM);
   if (rc != GEMM_OK) return rc;
-  rc = dg::encode_operand(h, &L.tmB, opB, Nm, K, plan.b_mn_major, plan.tile_n);
+  rc = dg::encode_operand(h, &L.tmB, opB, Nm, K, plan.b_mn_major,
+                          pair ? dg::kHalfBN : plan.tile_n);
   if (rc != GEMM_OK) return rc;
   dg::TcArgs& a = L.args;
   a.work = dg::spec_of(plan);
@@ -540,7 +595,8 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, co
   a.wait_limit_ns = h->opt.wait_limit_ns;
   a.a_mn = plan.a_mn_major;
   a.b_mn = plan.b_mn_major;
-  a.idesc = dg::make_idesc_f16(dg::kBM, plan.tile_n, plan.a_mn_major, plan.b_mn_major);
+  a.idesc = dg::make_idesc_f16(pair ? dg::kPairBM : dg::kBM, plan.tile_n, plan.a_mn_major,
+                               plan.b_mn_major);
   return dg::on_device(h->device, [&]() -> int {
     return dg::launch_tc(L) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
   });

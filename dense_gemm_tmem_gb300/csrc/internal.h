@@ -20,6 +20,8 @@ struct Options {
   int min_split_iters = 2;
   int force_swap = -1;
   int group_m = 16;
+  int pair = -1;           // two-SM kernel: 0 never, 1 whenever possible, -1 picker's rule
+  int pair_clusters = 0;   // CTA pairs resident at once (0: SMs / 2); set per device
   uint64_t wait_limit_ns = 2000000000ull;
 };
 
@@ -42,6 +44,7 @@ struct TcLaunch {
   int bn;             // MMA N tile: 16, 32, 64, 128 or 256
   bool out_f16;
   bool trans;         // swapped operands, transposed store
+  bool pair = false;  // two-SM kernel (cluster pairs, 256 x 256 tiles)
   int grid;
   CUtensorMap tmA;
   CUtensorMap tmB;
@@ -56,6 +59,10 @@ cudaError_t launch_tc(const TcLaunch& L);
 cudaError_t launch_tc_n256(const TcLaunch& L);
 cudaError_t launch_tc_n128(const TcLaunch& L);
 cudaError_t launch_tc_small(const TcLaunch& L);
+// Two-SM kernel (tc2.cu): even grid, not swapped, whole 256 x 256 tiles.
+cudaError_t launch_tc2(const TcLaunch& L);
+// Clusters of two that fit on the device at once (-1 if the query fails).
+int tc2_max_active_clusters(bool out_f16);
 int tc_stages_for(int bn);
 int tc_smem_bytes_for(int bn);
 

@@ -19,6 +19,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "tc2_kernel.cuh"
 
 namespace dg {
 namespace {
@@ -41,6 +42,7 @@ struct DeviceScratch {
   bool ready = false;
   unsigned char* base = nullptr;  // device address of g_noalloc_scratch
   int num_sms = 0;
+  int pairs = 0;                  // CTA pairs of the two-SM kernel resident at once
 };
 
 std::mutex g_na_mu;
@@ -66,6 +68,8 @@ int scratch_for_device(int device, DeviceScratch* out) {
       return GEMM_ERR_CUDA;
     d.base = static_cast<unsigned char*>(ptr);
     d.num_sms = sms;
+    const int pairs = tc2_max_active_clusters(true);
+    d.pairs = pairs > 0 ? (pairs < sms / 2 ? pairs : sms / 2) : sms / 2;
     d.ready = true;
   }
   *out = d;
@@ -115,6 +119,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
   if (rc != GEMM_OK) return rc;
 
   Options opt;
+  opt.pair_clusters = sc.pairs;
   gemm_plan_t plan;
   rc = plan_for(M, N, K, layout, sc.num_sms, opt, &plan);
   if (rc != GEMM_OK) return rc;
@@ -154,15 +159,18 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
   const bool swap = plan.swap_ab != 0;
   const int64_t Mm = swap ? N : M;
   const int64_t Nm = swap ? M : N;
+  const bool pair = plan.kernel == GEMM_KERNEL_TC2;  // whole tiles: no scratch but status
   TcLaunch L;
   L.bn = plan.tile_n;
   L.out_f16 = layout.out_dtype == GEMM_F16;
   L.trans = swap;
+  L.pair = pair;
   L.grid = plan.grid;
   L.stream = stream;
   rc = encode_operand_na(&L.tmA, swap ? B : A, Mm, K, plan.a_mn_major, kBM);
   if (rc != GEMM_OK) return rc;
-  rc = encode_operand_na(&L.tmB, swap ? A : B, Nm, K, plan.b_mn_major, plan.tile_n);
+  rc = encode_operand_na(&L.tmB, swap ? A : B, Nm, K, plan.b_mn_major,
+                         pair ? kHalfBN : plan.tile_n);
   if (rc != GEMM_OK) return rc;
   TcArgs& a = L.args;
   a.work = spec_of(plan);
@@ -177,6 +185,6 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
   a.wait_limit_ns = opt.wait_limit_ns;
   a.a_mn = plan.a_mn_major;
   a.b_mn = plan.b_mn_major;
-  a.idesc = make_idesc_f16(kBM, plan.tile_n, plan.a_mn_major, plan.b_mn_major);
+  a.idesc = make_idesc_f16(pair ? kPairBM : kBM, plan.tile_n, plan.a_mn_major, plan.b_mn_major);
   return launch_tc(L) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }

@@ -1,0 +1,51 @@
+// Instantiations of the two-SM (cta_group::2) kernel: fp16 or fp32 output.
+#include "internal.h"
+#include "tc2_kernel.cuh"
+
+namespace dg {
+
+namespace {
+template <bool OUT_F16>
+cudaError_t launch_tc2_inst(const TcLaunch& L) {
+  auto kern = tc2_gemm_kernel<OUT_F16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Tc2Config::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  // the cluster shape (2, 1, 1) is compiled into the kernel; grid is even
+  kern<<<L.grid, kTcThreads, Tc2Config::kSmemBytes, L.stream>>>(L.tmA, L.tmB, L.args);
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_tc2(const TcLaunch& L) {
+  if (L.trans || L.grid <= 0 || (L.grid & 1)) return cudaErrorInvalidValue;
+  return L.out_f16 ? launch_tc2_inst<true>(L) : launch_tc2_inst<false>(L);
+}
+
+int tc2_max_active_clusters(bool out_f16) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = Tc2Config::kSmemBytes;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  cudaError_t e;
+  if (out_f16) {
+    e = cudaFuncSetAttribute(tc2_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Tc2Config::kSmemBytes);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, tc2_gemm_kernel<true>, &cfg);
+  } else {
+    e = cudaFuncSetAttribute(tc2_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Tc2Config::kSmemBytes);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, tc2_gemm_kernel<false>, &cfg);
+  }
+  return e == cudaSuccess ? n : -1;
+}
+
+}  // namespace dg

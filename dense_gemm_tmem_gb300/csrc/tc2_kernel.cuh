@@ -1,0 +1,364 @@
+// tc2_kernel.cuh: the two-SM tcgen05 GEMM (cta_group::2) for large shapes.
+//
+// The last rung of the native GEMM ladder in the TIRx "Compiling and inspecting"
+// page ("sync -> TMA -> warp specialization -> 2-CTA cluster") on sm_103a:
+// a cluster of two CTAs on two SMs owns one 256 x 256 output tile.
+//   - Each CTA TMA-loads its own 128 rows of A and its own 128-column half of B
+//     into its S-stage ring (32 KiB per stage instead of 48 KiB per SM for the
+//     one-SM 128 x 256 tile: each SM fetches half of B).  Both CTAs' bytes
+//     complete on the leader CTA's `full` barrier.
+//   - One thread of the leader (cluster rank 0) issues
+//     tcgen05.mma.cta_group::2 with M = 256, N = 256: the hardware reads A rows
+//     0-127 and B columns 0-127 from the leader's shared memory and the other
+//     halves from the peer's, at the same offsets, and accumulates rows 0-127 in
+//     the leader's TMEM and rows 128-255 in the peer's.
+//   - tcgen05.commit with a two-CTA multicast frees the stage in both CTAs and
+//     hands both accumulators to their epilogues; each epilogue warp reports a
+//     drained accumulator to the leader with a remote mbarrier arrive.
+// Whole tiles only (persistent over clusters, grouped raster); the Stream-K
+// split stays on the one-SM kernel, which the picker uses for small shapes.
+// Every wait is bounded as in the one-SM kernel.
+#pragma once
+
+#include "tc_kernel.cuh"
+
+namespace dg {
+
+constexpr int kPairBM = 256;  // rows per cluster tile
+constexpr int kPairBN = 256;  // columns per cluster tile
+constexpr int kHalfBN = 128;  // B columns each CTA loads
+
+struct Tc2Config {
+  static constexpr int kStages = 6;
+  static constexpr int kABytes = kBM * kBK * 2;      // 16 KiB: this CTA's 128 rows
+  static constexpr int kBBytes = kHalfBN * kBK * 2;  // 16 KiB: this CTA's 128 columns
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 512;  // two 256-column accumulators
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+  static_assert((2 * kStages + 5) * 8 + 16 <= kBarBytes, "barrier area");
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// shared::cluster address of the same shared-memory offset in CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives on the barrier at this shared-memory offset in both CTAs of the pair
+// once every tcgen05 op this thread issued so far has completed.
+__device__ __forceinline__ void tc_commit_pair_both(uint32_t bar) {
+  const uint16_t mask = 0x3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
+// Same, on this CTA's barrier only.
+__device__ __forceinline__ void tc_commit_pair_self(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion is counted on a
+// barrier that may live in the peer CTA (shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+
+// Busy-waits about `ns` nanoseconds (only on the abort path, to let this CTA's
+// copies that signal the leader's barrier land before the CTA exits).
+__device__ __forceinline__ void spin_ns(uint64_t ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < ns) {
+  }
+}
+
+// TMA producer (one thread in each CTA): this CTA's A rows and B half per
+// k-block; the leader's arrive.expect_tx covers both CTAs' bytes.
+template <int S>
+__device__ __forceinline__ void tc2_producer(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                             const TcArgs& args, uint8_t* sA, uint8_t* sB,
+                                             uint64_t* full, uint64_t* empty, const WaitCtl& wc,
+                                             uint32_t rank, int32_t cluster_id) {
+  using Cfg = Tc2Config;
+  const WorkSpec& W = args.work;
+  WorkIter it;
+  it.init(W, cluster_id);
+  Unit u;
+  int s = 0;
+  uint32_t ph = 0, issued = 0, issued_par = 0;
+  bool ok = true;
+  const int32_t row_off = int32_t(rank) * kBM;      // this CTA's rows of the A tile
+  const int32_t col_off = int32_t(rank) * kHalfBN;  // this CTA's columns of the B tile
+  while (ok && it.next(W, u)) {
+    int32_t tm, tn;
+    tile_coords(W, u.tile, tm, tn);
+    const int32_t a_row = tm * kPairBM + row_off;
+    const int32_t b_row = tn * kPairBN + col_off;
+    for (int32_t kb = u.kb0; kb < u.kb1; ++kb) {
+      if (!wait_bounded(smem_u32(&empty[s]), ph ^ 1, wc, kSiteProducer)) {
+        ok = false;
+        break;
+      }
+      const uint32_t fb_local = smem_u32(&full[s]);
+      if (rank == 0) mbar_arrive_expect_tx(fb_local, 2 * Cfg::kStageBytes);
+      const uint32_t fb = map_to_rank(fb_local, 0);
+      const uint32_t a_dst = smem_u32(sA + s * Cfg::kABytes);
+      const uint32_t b_dst = smem_u32(sB + s * Cfg::kBBytes);
+      const int32_t k0 = kb * kBK;
+      if (!args.a_mn) {
+        tma_load_2d_pair(a_dst, &tmA, fb, k0, a_row);
+      } else {
+        tma_load_2d_pair(a_dst, &tmA, fb, a_row, k0);
+        tma_load_2d_pair(a_dst + 8192, &tmA, fb, a_row + 64, k0);
+      }
+      if (!args.b_mn) {
+        tma_load_2d_pair(b_dst, &tmB, fb, k0, b_row);
+      } else {
+        tma_load_2d_pair(b_dst, &tmB, fb, b_row, k0);
+        tma_load_2d_pair(b_dst + 8192, &tmB, fb, b_row + 64, k0);
+      }
+      issued |= 1u << s;
+      issued_par = (issued_par & ~(1u << s)) | (ph << s);
+      if (++s == S) {
+        s = 0;
+        ph ^= 1;
+      }
+    }
+  }
+  if (!ok) {
+    if (rank == 0) {
+      for (int t = 0; t < S; ++t)
+        if ((issued >> t) & 1) wait_drain(smem_u32(&full[t]), (issued_par >> t) & 1, wc);
+    } else if (issued) {
+      spin_ns(200000);  // the peer's copies complete on the leader's barrier
+    }
+  }
+}
+
+// MMA issuer (one thread of the leader CTA).
+template <int S>
+__device__ __forceinline__ void tc2_mma(const TcArgs& args, uint8_t* sA, uint8_t* sB,
+                                        uint64_t* full, uint64_t* empty, uint64_t* acc_full,
+                                        uint64_t* acc_empty, uint64_t* drain, const WaitCtl& wc,
+                                        uint32_t tmem_base, int32_t cluster_id) {
+  using Cfg = Tc2Config;
+  const WorkSpec& W = args.work;
+  WorkIter it;
+  it.init(W, cluster_id);
+  Unit u;
+  int s = 0, b = 0;
+  uint32_t ph = 0, aph = 0;
+  bool ok = true, any = false;
+  const uint32_t a_lbo = args.a_mn ? 8192u : 16u;
+  const uint32_t b_lbo = args.b_mn ? 8192u : 16u;
+  const uint32_t a_step = args.a_mn ? (2048u >> 4) : (32u >> 4);
+  const uint32_t b_step = args.b_mn ? (2048u >> 4) : (32u >> 4);
+  while (ok && it.next(W, u)) {
+    if (!wait_bounded(smem_u32(&acc_empty[b]), aph ^ 1, wc, kSiteMmaAccum)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    const uint32_t d_tmem = tmem_base + uint32_t(b * kPairBN);
+    for (int32_t kb = u.kb0; kb < u.kb1; ++kb) {
+      if (!wait_bounded(smem_u32(&full[s]), ph, wc, kSiteMmaFull)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint64_t adesc = make_sdesc_sw128(smem_u32(sA + s * Cfg::kABytes), a_lbo, 1024);
+      const uint64_t bdesc = make_sdesc_sw128(smem_u32(sB + s * Cfg::kBBytes), b_lbo, 1024);
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk)
+        tc_mma_f16_pair(d_tmem, adesc + uint64_t(kk * a_step), bdesc + uint64_t(kk * b_step),
+                        args.idesc, (kb > u.kb0 || kk > 0) ? 1u : 0u);
+      any = true;
+      tc_commit_pair_both(smem_u32(&empty[s]));
+      if (++s == S) {
+        s = 0;
+        ph ^= 1;
+      }
+    }
+    if (!ok) break;
+    tc_commit_pair_both(smem_u32(&acc_full[b]));
+    if (++b == 2) {
+      b = 0;
+      aph ^= 1;
+    }
+  }
+  if (!ok && any) {  // every MMA issued so far must finish before TMEM is freed
+    tc_commit_pair_self(smem_u32(drain));
+    wait_drain(smem_u32(drain), 0, wc);
+  }
+}
+
+// Epilogue (warps 2-5 of each CTA): this CTA's 128 rows of the 256 x 256 tile.
+template <bool OUT_F16>
+__device__ __forceinline__ void tc2_epilogue(const TcArgs& args, uint64_t* acc_full,
+                                             uint64_t* acc_empty, const WaitCtl& wc,
+                                             uint32_t tmem_base, uint32_t rank,
+                                             int32_t cluster_id) {
+  const WorkSpec& W = args.work;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int q = warp & 3;  // TMEM lane quarter this warp may access
+  const int row = q * 32 + lane;
+  const uint32_t leader_empty0 = map_to_rank(smem_u32(&acc_empty[0]), 0);
+  const uint32_t leader_empty1 = map_to_rank(smem_u32(&acc_empty[1]), 0);
+  WorkIter it;
+  it.init(W, cluster_id);
+  Unit u;
+  int b = 0;
+  uint32_t aph = 0;
+  while (it.next(W, u)) {
+    const bool got = wait_bounded(smem_u32(&acc_full[b]), aph, wc, kSiteEpilogue);
+    if (!epi_all(got)) break;
+    tc_fence_after();
+    int32_t tm, tn;
+    tile_coords(W, u.tile, tm, tn);
+    const int32_t mm = tm * kPairBM + int32_t(rank) * kBM + row;
+    const int32_t nbase = tn * kPairBN;
+    const uint32_t taddr = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(b * kPairBN);
+#pragma unroll 1
+    for (int c = 0; c < kPairBN / 32; ++c) {
+      float v[32];
+      __syncwarp();
+      tmem_load_chunk<32>(taddr + c * 32, v);
+      store_chunk<32, OUT_F16, false>(args, mm, nbase + c * 32, v);
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cluster(b == 0 ? leader_empty0 : leader_empty1);
+    if (++b == 2) {
+      b = 0;
+      aph ^= 1;
+    }
+  }
+}
+
+// args.work counts cluster tiles (256 x 256) and clusters (work.grid = CTAs / 2).
+template <bool OUT_F16>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
+    tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB, const TcArgs args) {
+  using Cfg = Tc2Config;
+  constexpr int S = Cfg::kStages;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + S * Cfg::kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * Cfg::kBBytes);
+  uint64_t* full = bars;               // leader's counts both CTAs' bytes
+  uint64_t* empty = bars + S;          // one multicast commit per phase, in both CTAs
+  uint64_t* acc_full = bars + 2 * S;   // one multicast commit per unit, in both CTAs
+  uint64_t* acc_empty = acc_full + 2;  // leader's: 4 epilogue warps x 2 CTAs
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int32_t cluster_id = int32_t(blockIdx.x >> 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&acc_full[b]), 1);
+      mbar_init(smem_u32(&acc_empty[b]), 2 * (kEpiThreads / 32));
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), Cfg::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs' barriers initialised and TMEM allocated
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtl wc{args.wait_limit_ns, args.status, abort_flag};
+
+  if (warp == 0) {
+    if (lane == 0) tc2_producer<S>(tmA, tmB, args, sA, sB, full, empty, wc, rank, cluster_id);
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0)
+      tc2_mma<S>(args, sA, sB, full, empty, acc_full, acc_empty, drain, wc, tmem_base,
+                 cluster_id);
+  } else {
+    tc2_epilogue<OUT_F16>(args, acc_full, acc_empty, wc, tmem_base, rank, cluster_id);
+  }
+
+  __syncthreads();
+  tc_fence_before();
+  cluster_sync_all();  // no MMA or remote arrive is still aimed at either CTA
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+}  // namespace dg

@@ -65,7 +65,9 @@ enum {
   GEMM_KERNEL_STREAMK = 1,  /* the same kernel with Stream-K (or hybrid) k-splitting */
   GEMM_KERNEL_SIMT = 2,     /* CUDA-core fp32 GEMM */
   GEMM_KERNEL_FILL = 3,     /* K == 0: C = bias (or 0) */
-  GEMM_KERNEL_NONE = 4      /* M == 0 or N == 0: nothing to do */
+  GEMM_KERNEL_NONE = 4,     /* M == 0 or N == 0: nothing to do */
+  GEMM_KERNEL_TC2 = 5       /* two-SM tcgen05 GEMM (CTA pairs, cta_group::2), whole
+                               256 x 256 tiles; tile_m = tile_n = 256, grid = 2 x pairs */
 };
 
 /* What gemm_run will launch for a shape.  "MMA view": with swap_ab = 1 the
@@ -92,13 +94,15 @@ typedef struct {
 
 /* Options for tests and tuning (gemm_set_option).  Values < 0 restore the default. */
 enum {
-  GEMM_OPT_FORCE_KERNEL = 0,     /* GEMM_KERNEL_TC / _STREAMK / _SIMT, or -1 */
+  GEMM_OPT_FORCE_KERNEL = 0,     /* GEMM_KERNEL_TC / _STREAMK / _SIMT / _TC2, or -1 */
   GEMM_OPT_FORCE_TILE_N = 1,     /* 16, 32, 64, 128, 256 (tensor-core path), or -1 */
   GEMM_OPT_FORCE_GRID = 2,       /* CTA count for the split path, or -1 */
   GEMM_OPT_WAIT_LIMIT_NS = 3,    /* bound on each device-side wait (default 2e9 ns) */
   GEMM_OPT_MIN_SPLIT_ITERS = 4,  /* fewest k-blocks per CTA when splitting (default 2) */
   GEMM_OPT_FORCE_SWAP_AB = 5,    /* 0 or 1, or -1 for the picker's choice */
-  GEMM_OPT_GROUP_M = 6           /* tile raster group height (default 16) */
+  GEMM_OPT_GROUP_M = 6,          /* tile raster group height (default 16) */
+  GEMM_OPT_PAIR = 7              /* two-SM kernel: 0 never, 1 whenever the shape allows
+                                    (not swapped), -1 the picker's rule */
 };
 
 /* Creates a handle on CUDA device `device`.  Allocates, on that device, the

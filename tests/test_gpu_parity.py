@@ -15,7 +15,8 @@ from gpu_helpers import (as_f64, check, reset_opts, run, sample_rows, set_opts, 
 
 pytestmark = pytest.mark.gpu
 F16, F32 = inputs.F16, inputs.F32
-TC, SK, SIMT = B.GEMM_KERNEL_TC, B.GEMM_KERNEL_STREAMK, B.GEMM_KERNEL_SIMT
+TC, SK, SIMT, TC2 = (B.GEMM_KERNEL_TC, B.GEMM_KERNEL_STREAMK, B.GEMM_KERNEL_SIMT,
+                      B.GEMM_KERNEL_TC2)
 
 
 @pytest.fixture(scope="module")
@@ -97,6 +98,29 @@ def test_split_grid_sizes(g, dev, grid):
     full_check(g, dev, p)
 
 
+@pytest.mark.parametrize("am,bm", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("odt", [F16, F32])
+@pytest.mark.parametrize("bias", [False, True])
+def test_pair_layouts_ragged(g, dev, am, bm, odt, bias):
+    """Two-SM kernel on 296 x 520 x 200: the second pair tile has 40 valid rows,
+    all in the leader CTA, so the peer CTA computes only zero-filled rows."""
+    set_opts(g, kernel=TC2)
+    p = problem(296, 520, 200, am, bm, F16, odt, bias, 110 + am + 2 * bm)
+    pl = g.plan(296, 520, 200, am, bm, B.GEMM_F16, B.GEMM_F16 if odt == F16 else B.GEMM_F32)
+    assert pl["kernel"] == TC2 and pl["tile_m"] == 256
+    full_check(g, dev, p)
+
+
+@pytest.mark.parametrize("grid", [2, 6, 150])
+def test_pair_grid_sizes(g, dev, grid):
+    """16 pair tiles on 1, 3 or 75 CTA pairs: each pair walks many tiles, both
+    accumulators and every pipeline phase wrap around."""
+    set_opts(g, kernel=TC2, grid=grid)
+    p = problem(1000, 1000, 1480, 0, 1, F16, F32, True, 120 + grid)
+    assert g.plan(1000, 1000, 1480, 0, 1)["grid"] == min(grid, 32)
+    full_check(g, dev, p)
+
+
 def test_split_many_contributors(g, dev):
     """One output tile whose 256 k-blocks are split over up to 128 CTAs."""
     p = problem(128, 128, 16384, 0, 0, F16, F32, True, 61)
@@ -106,7 +130,7 @@ def test_split_many_contributors(g, dev):
 
 
 # ---------------------------------------------------------- closed forms --
-@pytest.mark.parametrize("kernel", [TC, SK])
+@pytest.mark.parametrize("kernel", [TC, SK, TC2])
 @pytest.mark.parametrize("bm", [0, 1])
 def test_permutation_rows_exact(g, dev, kernel, bm):
     """A = P: C must be B's rows permuted, exactly (catches swizzle, descriptor
@@ -123,7 +147,7 @@ def test_permutation_rows_exact(g, dev, kernel, bm):
     assert np.array_equal(got, Bl[perm].astype(np.float64))
 
 
-@pytest.mark.parametrize("kernel", [TC, SK])
+@pytest.mark.parametrize("kernel", [TC, SK, TC2])
 def test_permutation_columns_exact(g, dev, kernel):
     set_opts(g, kernel=kernel)
     n = 512
@@ -144,6 +168,8 @@ def test_permutation_columns_exact(g, dev, kernel):
     ("swap", 16, 2048, 4096, 0, 0, F16, F32, {}),
     ("simt", 200, 300, 500, 0, 0, F32, F32, {}),
     ("simt_col", 200, 300, 500, 1, 1, F32, F32, {}),
+    ("pair", 520, 776, 1032, 0, 1, F16, F32, {"kernel": TC2}),
+    ("pair16", 296, 520, 2048, 1, 0, F16, F16, {"kernel": TC2, "grid": 4}),
 ])
 def test_integer_inputs_exact(g, dev, case):
     """Integer-valued inputs: every partial sum is an integer below 2^24, so
@@ -268,7 +294,7 @@ def test_side_stream(g, dev):
 
 
 # ----------------------------------------------------------- determinism --
-@pytest.mark.parametrize("kernel,grid", [(SK, -1), (SK, 29), (TC, -1)])
+@pytest.mark.parametrize("kernel,grid", [(SK, -1), (SK, 29), (TC, -1), (TC2, -1)])
 def test_bitwise_repeatable(g, dev, kernel, grid):
     set_opts(g, kernel=kernel, grid=grid)
     p = problem(520, 776, 2056, 0, 1, F16, F32, True, 130, kind="normal")
@@ -319,7 +345,7 @@ def test_workload_large_sampled_rows(g, dev, name, kind):
     w = inputs.WORKLOADS[name]
     p = w.make(kind=kind)
     pl = g.plan(w.M, w.N, w.K, w.a_major, w.b_major, B.GEMM_F16, B.GEMM_F16)
-    assert pl["kernel"] == TC and pl["tile_n"] == 256
+    assert pl["kernel"] == TC2 and pl["tile_n"] == 256
     C = run(g, p, dev)
     rows = sample_rows(w.M, 7)
     got = as_f64(C, rows)

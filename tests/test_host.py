@@ -45,11 +45,16 @@ def test_no_library_gemm_or_cuda_driver_link(lib):
     assert "libcuda.so" not in deps and "libcublas" not in deps
 
 
-def test_sources_use_no_multicast_or_wgmma():
+def test_sources_use_no_multicast_loads_or_wgmma():
+    """No TMA multicast loads (every CTA fetches its own operand tiles), and no
+    Hopper/legacy MMA forms.  A tcgen05.commit multicast (a completion signal to
+    both CTAs of a pair) is not a load and is allowed."""
     csrc = os.path.join(ROOT, "dense_gemm_tmem_gb300", "csrc")
     for fn in os.listdir(csrc):
         txt = open(os.path.join(csrc, fn)).read()
-        assert ".multicast::cluster" not in txt, fn
+        for line in txt.splitlines():
+            if "cp.async.bulk" in line:
+                assert "multicast" not in line, (fn, line)
         assert "wgmma" not in txt, fn
         assert "mma.sync" not in txt and "wmma::" not in txt, fn
 
@@ -65,16 +70,29 @@ def plan(M, N, K, am=0, bm=0, idt=F16, odt=F32, sms=SMS):
     return rc, p
 
 
-def test_picker_large_square_whole_tiles():
+def test_picker_large_square_two_sm_tiles():
+    """Large shapes run on CTA pairs: 256 x 256 tiles, whole waves of 76 pairs."""
     rc, p = plan(8192, 8192, 8192, 0, 1, F16, F16)
-    assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC
-    assert (p.tile_m, p.tile_n, p.tile_k) == (128, 256, 64)
-    assert (p.tiles_m, p.tiles_n, p.k_iters) == (64, 32, 128)
-    assert (p.dp_tiles, p.sk_tiles, p.grid) == (2048, 0, SMS)
+    assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC2
+    assert (p.tile_m, p.tile_n, p.tile_k, p.stages) == (256, 256, 64, 6)
+    assert (p.tiles_m, p.tiles_n, p.k_iters) == (32, 32, 128)
+    assert (p.dp_tiles, p.sk_tiles, p.grid) == (1024, 0, SMS)
     assert (p.swap_ab, p.a_mn_major, p.b_mn_major) == (0, 0, 0)
     rc, p = plan(16384, 16384, 16384, 0, 0, F16, F16)
-    assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC and p.b_mn_major == 1
-    assert p.dp_tiles == 128 * 64 and p.workspace_bytes == 0
+    assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC2 and p.b_mn_major == 1
+    assert p.dp_tiles == 64 * 64 and p.workspace_bytes == 0
+
+
+def test_picker_pair_rule_falls_back():
+    # 100 pair tiles on 76 pairs: 1.3 waves -> the one-SM rules decide
+    rc, p = plan(1280, 5120, 1024)
+    assert rc == 0 and p.kernel == B.GEMM_KERNEL_STREAMK and p.tile_m == 128
+    # exactly one wave of pairs: 76 = 4 x 19 tiles
+    rc, p = plan(1024, 19 * 256, 512)
+    assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC2 and p.grid == 152
+    # skinny shapes swap operands and never pair
+    rc, p = plan(64, 65536, 4096)
+    assert rc == 0 and p.swap_ab == 1 and p.kernel != B.GEMM_KERNEL_TC2
 
 
 def test_picker_small_shape_is_split():
@@ -134,9 +152,13 @@ PLANS = [(512, 512, 512, 0, 0), (1, 4096, 4096, 0, 0), (16, 4096, 4096, 0, 0),
 def test_work_units_match_oracle_reading(M, N, K, am, bm):
     rc, p = plan(M, N, K, am, bm)
     assert rc == 0
-    ref = schedule.streamk_units(p.dp_tiles, p.sk_tiles, p.k_iters, p.grid)
-    for c in range(p.grid):
+    # the two-SM kernel hands work to CTA pairs
+    units = p.grid // 2 if p.kernel == B.GEMM_KERNEL_TC2 else p.grid
+    ref = schedule.streamk_units(p.dp_tiles, p.sk_tiles, p.k_iters, units)
+    for c in range(units):
         assert B.gemm_work_units(p, c) == ref[c]
+    with pytest.raises(B.GemmError):
+        B.gemm_work_units(p, units)
     # contributors of each split tile: the CTAs touching it, in k order
     owners = {}
     for c, units in enumerate(ref):
