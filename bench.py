@@ -66,10 +66,11 @@ def load_peaks():
             "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(files):
+    """Hash of the listed kernel source files (in the listed order)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_gemm_tmem_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in files:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
@@ -77,13 +78,13 @@ def kernel_source_hash():
 
 def recorded_traffic(workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
+    on the current sources of the kernel it names; else None."""
     try:
         with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
             rec = json.load(f).get(workload)
-    except (OSError, ValueError):
-        return None
-    if not rec or rec.get("src_hash") != kernel_source_hash():
+        if not rec or rec.get("src_hash") != kernel_source_hash(rec["sources"]):
+            return None
+    except (OSError, ValueError, KeyError):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -324,10 +325,21 @@ def run_ours(args):
     if p.in_dtype == inputs.F16:
         sustained = region_s >= 1.0
         peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
-        roof = {"bound": "tensor", "achieved": step_flops / avg_launch_s / 1e12, "peak": peak,
-                "unit": "TFLOP/s",
-                "peak_source": "%s dense bf16 %s (fp16 dense rate is the same)"
-                               % (peak_src, "sustained" if sustained else "burst")}
+        ridge = peak * 1e12 / (peaks["hbm_gbs"] * 1e9)  # flop per byte
+        intensity = step_flops / step_bytes
+        if intensity >= ridge:
+            roof = {"bound": "tensor", "achieved": step_flops / avg_launch_s / 1e12,
+                    "peak": peak, "unit": "TFLOP/s",
+                    "peak_source": "%s dense bf16 %s (fp16 dense rate is the same)"
+                                   % (peak_src, "sustained" if sustained else "burst")}
+        else:
+            # below the ridge: the operands' bytes bound the kernel
+            roof = {"bound": "hbm", "achieved": step_bytes / avg_launch_s / 1e9,
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "peak_source": "%s copy bandwidth" % peak_src,
+                    "tflops": step_flops / avg_launch_s / 1e12}
+        roof["intensity_flop_per_byte"] = intensity
+        roof["ridge_flop_per_byte"] = ridge
     else:
         # fp32 CUDA-core path: SMs x 128 FMA lanes x 2 flop x max SM clock
         props = torch.cuda.get_device_properties(dev)

@@ -84,14 +84,27 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
   }
   if (L.in_dtype == GEMM_F32) {
     if (o.force_kernel >= 0 && o.force_kernel != GEMM_KERNEL_SIMT) return GEMM_ERR_UNSUPPORTED;
-    if (ceil_div(M, kSimtBM) > 65535) return GEMM_ERR_UNSUPPORTED;
+    // 128x128 tiles (2 CTAs per SM) when they make at least four waves or
+    // whole waves; otherwise 64x64 tiles (8 CTAs per SM) so the last wave
+    // leaves fewer SMs idle.
+    int tile;
+    if (o.force_tile_n > 0) {
+      if (o.force_tile_n != kSimtBM && o.force_tile_n != kSimtSmallTile)
+        return GEMM_ERR_UNSUPPORTED;
+      tile = o.force_tile_n;
+    } else {
+      const int64_t big = ceil_div(M, kSimtBM) * ceil_div(N, kSimtBN);
+      const int64_t slots = int64_t(2) * num_sms;
+      tile = (big >= 4 * slots || big % slots == 0) ? kSimtBM : kSimtSmallTile;
+    }
+    if (ceil_div(M, tile) > 65535) return GEMM_ERR_UNSUPPORTED;
     p->kernel = GEMM_KERNEL_SIMT;
-    p->tile_m = kSimtBM;
-    p->tile_n = kSimtBN;
+    p->tile_m = tile;
+    p->tile_n = tile;
     p->tile_k = kSimtBK;
     p->stages = 2;
-    p->tiles_m = int32_t(ceil_div(M, kSimtBM));
-    p->tiles_n = int32_t(ceil_div(N, kSimtBN));
+    p->tiles_m = int32_t(ceil_div(M, tile));
+    p->tiles_n = int32_t(ceil_div(N, tile));
     p->grid = p->tiles_m * p->tiles_n;
     p->k_iters = int32_t(std::min<int64_t>(ceil_div(K, kSimtBK), INT32_MAX));
     p->dp_tiles = p->grid;
@@ -553,6 +566,7 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, co
     L.C = static_cast<float*>(C);
     L.a_major = layout.a_major;
     L.b_major = layout.b_major;
+    L.tile = plan.tile_m;
     L.stream = stream;
     return dg::on_device(h->device, [&]() -> int {
       return dg::launch_simt(L) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;

@@ -74,10 +74,12 @@ struct SimtLaunch {
   const float* bias;
   float* C;
   int a_major, b_major;  // 0 row, 1 column
+  int tile = 128;        // square tile edge: kSimtBM (128) or kSimtSmallTile (64)
   cudaStream_t stream;
 };
 cudaError_t launch_simt(const SimtLaunch& L);
 constexpr int kSimtBM = 128, kSimtBN = 128, kSimtBK = 8, kSimtThreads = 256;
+constexpr int kSimtSmallTile = 64;  // 64 x 64 tiles, 64 threads
 int simt_a_stride();
 int simt_b_stride();
 

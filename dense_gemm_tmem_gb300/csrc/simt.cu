@@ -2,11 +2,11 @@
 //
 // Each technique of the "TVM Matrix Multiplication Optimization" ladder
 // (kimm240.github.io/tvm, Steps 1-6) has its place here:
-//   Step 1 data-parallel 2-D thread map    -> 2-D grid of 128x128 output tiles
+//   Step 1 data-parallel 2-D thread map    -> 2-D grid of BM x BN output tiles
 //   Step 2 tiling + loop reordering        -> each thread owns an 8x8 register tile
 //                                             and runs the k loop outermost
-//   Step 3 shared memory, cooperative fetch-> all 256 threads stage a 128x8 A block
-//                                             and an 8x128 B block per k-step
+//   Step 3 shared memory, cooperative fetch-> all threads stage a BM x 8 A block
+//                                             and an 8 x BN B block per k-step
 //   Step 4 vectorisation + register caching-> float4 global and shared loads;
 //                                             accumulators live in registers
 //   Step 5 software pipelining             -> two shared-memory buffers; the next
@@ -16,8 +16,12 @@
 //                                             fully unrolled
 // The staging rows are padded as storage_align(factor 32, offset 4) pads them
 // (leiblog.wang, the storage_align answer: the stride is raised to the next
-// value congruent to offset mod factor), 128 -> 132 floats, which makes the
-// transposed A stores free of bank conflicts.
+// value congruent to offset mod factor), 128 -> 132 and 64 -> 68 floats, which
+// makes the transposed A stores free of bank conflicts.
+//
+// Two tile shapes: 128 x 128 with 256 threads, and 64 x 64 with 64 threads for
+// grids too small to balance over the SMs (the 8x8 thread tile, and so the
+// ratio of shared loads to FMAs, is the same in both).
 #include "internal.h"
 
 namespace dg {
@@ -25,12 +29,11 @@ namespace dg {
 namespace {
 
 // storage_align(factor, offset) applied to a row of `extent` elements.
-constexpr int aligned_stride(int extent, int factor, int offset) {
+__host__ __device__ constexpr int aligned_stride(int extent, int factor, int offset) {
   return extent + (factor + offset - extent % factor) % factor;
 }
-constexpr int kAS = aligned_stride(kSimtBM, 32, 4);
-constexpr int kBS = aligned_stride(kSimtBN, 32, 4);
-static_assert(kAS == 132 && kBS == 132, "padded staging strides");
+static_assert(aligned_stride(128, 32, 4) == 132 && aligned_stride(64, 32, 4) == 68,
+              "padded staging strides");
 
 struct SimtArgs {
   int64_t M, N, K;
@@ -41,91 +44,104 @@ struct SimtArgs {
   bool vec_a, vec_b, vec_c;  // float4 access allowed (16-byte aligned rows)
 };
 
-template <bool A_COL, bool B_COL>
-__global__ void __launch_bounds__(kSimtThreads, 2) simt_sgemm_kernel(const SimtArgs a) {
-  constexpr int BM = kSimtBM, BN = kSimtBN, BK = kSimtBK;
-  __shared__ __align__(16) float As[2][BK][kAS];
-  __shared__ __align__(16) float Bs[2][BK][kBS];
+// One float4-wide piece of a k-block: `count` consecutive elements along the
+// storage row, starting at p; zero outside [0, limit) or when `inside` is false.
+__device__ __forceinline__ void load4(float (&r)[4], const float* p, bool vec, bool inside,
+                                      int64_t first, int64_t limit) {
+  if (vec && inside && first + 3 < limit) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(p));
+    r[0] = v.x; r[1] = v.y; r[2] = v.z; r[3] = v.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r[i] = (inside && first + i < limit) ? __ldg(p + i) : 0.f;
+  }
+}
+
+// BM x BN tile, NT = (BM/8) x (BN/8) threads, each an 8x8 register tile made
+// of two 4-row groups BM/2 apart and two 4-column groups BN/2 apart.
+template <int BM, int BN, bool A_COL, bool B_COL>
+__global__ void __launch_bounds__((BM / 8) * (BN / 8), 2 * 256 / ((BM / 8) * (BN / 8)))
+    simt_sgemm_kernel(const SimtArgs a) {
+  constexpr int BK = kSimtBK;
+  constexpr int NT = (BM / 8) * (BN / 8);
+  constexpr int AS = aligned_stride(BM, 32, 4);
+  constexpr int BS = aligned_stride(BN, 32, 4);
+  constexpr int AV = BM * BK / 4 / NT;  // float4 pieces of A per thread per k-block
+  constexpr int BV = BN * BK / 4 / NT;
+  static_assert(AV >= 1 && BV >= 1 && AV * NT * 4 == BM * BK && BV * NT * 4 == BN * BK, "");
+  __shared__ __align__(16) float As[2][BK][AS];
+  __shared__ __align__(16) float Bs[2][BK][BS];
 
   const int t = threadIdx.x;
-  const int tx = t & 15, ty = t >> 4;
+  const int tx = t % (BN / 8), ty = t / (BN / 8);
   const int64_t m0 = int64_t(blockIdx.y) * BM;
   const int64_t n0 = int64_t(blockIdx.x) * BN;
   const int64_t M = a.M, N = a.N, K = a.K;
 
-  float ra[4], rb[4];
+  float ra[AV][4], rb[BV][4];
   float acc[8][8];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
-  // Global -> registers for k-block k0 (zero outside the matrix).
+  // Global -> registers for the k-block starting at k0.  Piece f of A is, for
+  // row-major A, row f/2 and k-quarter f%2; for column-major A, k-row
+  // f/(BM/4) and m-quarter f%(BM/4).  B likewise.
   auto fetch = [&](int64_t k0) {
-    if (!A_COL) {  // A row-major: row m, 4 consecutive k
-      const int64_t m = m0 + (t >> 1), k = k0 + (t & 1) * 4;
-      const float* p = a.A + m * K + k;
-      if (a.vec_a && m < M && k + 3 < K) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(p));
-        ra[0] = v.x; ra[1] = v.y; ra[2] = v.z; ra[3] = v.w;
-      } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) ra[i] = (m < M && k + i < K) ? __ldg(p + i) : 0.f;
-      }
-    } else {       // A column-major (K x M storage): row k, 4 consecutive m
-      const int64_t k = k0 + (t >> 5), m = m0 + (t & 31) * 4;
-      const float* p = a.A + k * M + m;
-      if (a.vec_a && k < K && m + 3 < M) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(p));
-        ra[0] = v.x; ra[1] = v.y; ra[2] = v.z; ra[3] = v.w;
+    for (int v = 0; v < AV; ++v) {
+      const int f = t + v * NT;
+      if (!A_COL) {
+        const int64_t m = m0 + (f >> 1), k = k0 + (f & 1) * 4;
+        load4(ra[v], a.A + m * K + k, a.vec_a, m < M, k, K);
       } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) ra[i] = (k < K && m + i < M) ? __ldg(p + i) : 0.f;
+        const int64_t k = k0 + f / (BM / 4), m = m0 + (f % (BM / 4)) * 4;
+        load4(ra[v], a.A + k * M + m, a.vec_a, k < K, m, M);
       }
     }
-    if (!B_COL) {  // B row-major: row k, 4 consecutive n
-      const int64_t k = k0 + (t >> 5), n = n0 + (t & 31) * 4;
-      const float* p = a.B + k * N + n;
-      if (a.vec_b && k < K && n + 3 < N) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(p));
-        rb[0] = v.x; rb[1] = v.y; rb[2] = v.z; rb[3] = v.w;
-      } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) rb[i] = (k < K && n + i < N) ? __ldg(p + i) : 0.f;
-      }
-    } else {       // B column-major (N x K storage): column n, 4 consecutive k
-      const int64_t n = n0 + (t >> 1), k = k0 + (t & 1) * 4;
-      const float* p = a.B + n * K + k;
-      if (a.vec_b && n < N && k + 3 < K) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(p));
-        rb[0] = v.x; rb[1] = v.y; rb[2] = v.z; rb[3] = v.w;
+    for (int v = 0; v < BV; ++v) {
+      const int f = t + v * NT;
+      if (!B_COL) {
+        const int64_t k = k0 + f / (BN / 4), n = n0 + (f % (BN / 4)) * 4;
+        load4(rb[v], a.B + k * N + n, a.vec_b, k < K, n, N);
       } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) rb[i] = (n < N && k + i < K) ? __ldg(p + i) : 0.f;
+        const int64_t n = n0 + (f >> 1), k = k0 + (f & 1) * 4;
+        load4(rb[v], a.B + n * K + k, a.vec_b, n < N, k, K);
       }
     }
   };
 
   // Registers -> shared buffer `buf`, as As[k][m] and Bs[k][n].
   auto stage = [&](int buf) {
-    if (!A_COL) {
-      const int m = t >> 1, k = (t & 1) * 4;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) As[buf][k + i][m] = ra[i];
-    } else {
-      const int k = t >> 5, m = (t & 31) * 4;
-      *reinterpret_cast<float4*>(&As[buf][k][m]) = make_float4(ra[0], ra[1], ra[2], ra[3]);
+    for (int v = 0; v < AV; ++v) {
+      const int f = t + v * NT;
+      if (!A_COL) {
+        const int m = f >> 1, k = (f & 1) * 4;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) As[buf][k + i][m] = ra[v][i];
+      } else {
+        const int k = f / (BM / 4), m = (f % (BM / 4)) * 4;
+        *reinterpret_cast<float4*>(&As[buf][k][m]) =
+            make_float4(ra[v][0], ra[v][1], ra[v][2], ra[v][3]);
+      }
     }
-    if (!B_COL) {
-      const int k = t >> 5, n = (t & 31) * 4;
-      *reinterpret_cast<float4*>(&Bs[buf][k][n]) = make_float4(rb[0], rb[1], rb[2], rb[3]);
-    } else {
-      const int n = t >> 1, k = (t & 1) * 4;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) Bs[buf][k + i][n] = rb[i];
+    for (int v = 0; v < BV; ++v) {
+      const int f = t + v * NT;
+      if (!B_COL) {
+        const int k = f / (BN / 4), n = (f % (BN / 4)) * 4;
+        *reinterpret_cast<float4*>(&Bs[buf][k][n]) =
+            make_float4(rb[v][0], rb[v][1], rb[v][2], rb[v][3]);
+      } else {
+        const int n = f >> 1, k = (f & 1) * 4;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) Bs[buf][k + i][n] = rb[v][i];
+      }
     }
   };
-
   const int64_t nk = (K + BK - 1) / BK;
   fetch(0);
   stage(0);
@@ -136,9 +152,9 @@ __global__ void __launch_bounds__(kSimtThreads, 2) simt_sgemm_kernel(const SimtA
 #pragma unroll
     for (int kk = 0; kk < BK; ++kk) {
       const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
-      const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][64 + ty * 4]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][BM / 2 + ty * 4]);
       const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][64 + tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][BN / 2 + tx * 4]);
       const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
       const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
@@ -150,14 +166,14 @@ __global__ void __launch_bounds__(kSimtThreads, 2) simt_sgemm_kernel(const SimtA
     __syncthreads();
   }
 
-  // Epilogue: + bias[n], rows ty*4+i (+64), columns tx*4+j (+64).
+  // Epilogue: + bias[n]; rows ty*4+i (+BM/2), columns tx*4+j (+BN/2).
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int64_t m = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
+    const int64_t m = m0 + (i < 4 ? ty * 4 + i : BM / 2 + ty * 4 + (i - 4));
     if (m >= M) continue;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int64_t n = n0 + h * 64 + tx * 4;
+      const int64_t n = n0 + h * (BN / 2) + tx * 4;
       if (n >= N) continue;
       float o[4];
 #pragma unroll
@@ -177,10 +193,28 @@ __global__ void __launch_bounds__(kSimtThreads, 2) simt_sgemm_kernel(const SimtA
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+template <int BM, int BN>
+cudaError_t launch_simt_tile(const SimtArgs& a, int a_major, int b_major, cudaStream_t s) {
+  constexpr int NT = (BM / 8) * (BN / 8);
+  const int64_t gx = (a.N + BN - 1) / BN;
+  const int64_t gy = (a.M + BM - 1) / BM;
+  if (gx > 0x7fffffff || gy > 65535) return cudaErrorInvalidConfiguration;
+  const dim3 grid{unsigned(gx), unsigned(gy), 1u};
+  if (a_major == 0 && b_major == 0)
+    simt_sgemm_kernel<BM, BN, false, false><<<grid, NT, 0, s>>>(a);
+  else if (a_major == 0)
+    simt_sgemm_kernel<BM, BN, false, true><<<grid, NT, 0, s>>>(a);
+  else if (b_major == 0)
+    simt_sgemm_kernel<BM, BN, true, false><<<grid, NT, 0, s>>>(a);
+  else
+    simt_sgemm_kernel<BM, BN, true, true><<<grid, NT, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
-int simt_a_stride() { return kAS; }
-int simt_b_stride() { return kBS; }
+int simt_a_stride() { return aligned_stride(kSimtBM, 32, 4); }
+int simt_b_stride() { return aligned_stride(kSimtBN, 32, 4); }
 
 cudaError_t launch_simt(const SimtLaunch& L) {
   SimtArgs a;
@@ -189,19 +223,9 @@ cudaError_t launch_simt(const SimtLaunch& L) {
   a.vec_a = aligned16(L.A) && ((L.a_major == 0 ? L.K : L.M) % 4 == 0);
   a.vec_b = aligned16(L.B) && ((L.b_major == 0 ? L.N : L.K) % 4 == 0);
   a.vec_c = aligned16(L.C) && (L.N % 4 == 0);
-  const int64_t gx = (L.N + kSimtBN - 1) / kSimtBN;
-  const int64_t gy = (L.M + kSimtBM - 1) / kSimtBM;
-  if (gx > 0x7fffffff || gy > 65535) return cudaErrorInvalidConfiguration;
-  const dim3 grid{unsigned(gx), unsigned(gy), 1u};
-  if (L.a_major == 0 && L.b_major == 0)
-    simt_sgemm_kernel<false, false><<<grid, kSimtThreads, 0, L.stream>>>(a);
-  else if (L.a_major == 0)
-    simt_sgemm_kernel<false, true><<<grid, kSimtThreads, 0, L.stream>>>(a);
-  else if (L.b_major == 0)
-    simt_sgemm_kernel<true, false><<<grid, kSimtThreads, 0, L.stream>>>(a);
-  else
-    simt_sgemm_kernel<true, true><<<grid, kSimtThreads, 0, L.stream>>>(a);
-  return cudaGetLastError();
+  if (L.tile == kSimtSmallTile)
+    return launch_simt_tile<kSimtSmallTile, kSimtSmallTile>(a, L.a_major, L.b_major, L.stream);
+  return launch_simt_tile<kSimtBM, kSimtBN>(a, L.a_major, L.b_major, L.stream);
 }
 
 // ---------------------------------------------------------------- K == 0 --

@@ -254,9 +254,11 @@ def test_unaligned_outputs_and_bias(g, dev):
     check(cflat[1:].view(130, 264).double().cpu().numpy(), ref, p)
 
 
+@pytest.mark.parametrize("tile", [64, 128])
 @pytest.mark.parametrize("am,bm", [(0, 0), (0, 1), (1, 0), (1, 1)])
 @pytest.mark.parametrize("M,N,K", [(130, 70, 33), (257, 129, 128), (5, 3, 2)])
-def test_simt_layouts_ragged(g, dev, am, bm, M, N, K):
+def test_simt_layouts_ragged(g, dev, tile, am, bm, M, N, K):
+    set_opts(g, tile_n=tile)
     p = problem(M, N, K, am, bm, F32, F32, True, 100 + M)
     full_check(g, dev, p)
 

@@ -126,7 +126,11 @@ def test_picker_hybrid_tail():
 
 def test_picker_fp32_and_degenerate():
     rc, p = plan(2048, 2048, 2048, 0, 0, F32, F32)
-    assert rc == 0 and p.kernel == B.GEMM_KERNEL_SIMT and p.grid == 256
+    # 256 tiles of 128 would leave half the SMs with one CTA and half with two:
+    # 1024 tiles of 64 (8 resident per SM) balance to 6.7 per SM
+    assert rc == 0 and p.kernel == B.GEMM_KERNEL_SIMT and (p.tile_m, p.grid) == (64, 1024)
+    rc, p = plan(8192, 8192, 512, 0, 0, F32, F32)   # 4096 tiles of 128 >= 4 waves
+    assert rc == 0 and (p.tile_m, p.grid) == (128, 4096)
     assert plan(64, 64, 64, 0, 0, F32, F16)[0] == B.GEMM_ERR_UNSUPPORTED
     assert plan(10, 10, 0)[1].kernel == B.GEMM_KERNEL_FILL
     assert plan(0, 10, 10)[1].kernel == B.GEMM_KERNEL_NONE
