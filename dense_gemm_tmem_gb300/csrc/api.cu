@@ -53,18 +53,22 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // ------------------------------------------------------------ tile picker --
 // Chooses kernel, tile, split and grid for a shape.  Rules:
-//  * fp32 inputs -> CUDA-core kernel, 128x128 tiles.
-//  * fp16 inputs -> tcgen05 kernel.  Skinny M (M <= 128, N >= 2M, A row-major)
-//    swaps the operands so N fills the 128-row MMA side and M becomes the MMA
-//    N side (16/32/64/128 columns).  Otherwise the tile is 128x256 (128x128
-//    when N <= 128).
+//  * fp32 inputs -> CUDA-core kernel, 128x128 tiles (64x64 when there are
+//    fewer 128-tiles than SMs).
+//  * fp16 inputs -> tcgen05 kernels.  Large shapes whose 256x256 tiles fill
+//    whole waves of CTA pairs -> the two-SM kernel.  Skinny M (M <= 128,
+//    N >= 2M, A row-major) swaps the operands so N fills the 128-row MMA side
+//    and M becomes the MMA N side (16/32/64/128 columns).  Otherwise the tile
+//    is 128x256 (128x128 when N <= 128 or when 256-wide tiles would fill fewer
+//    than half the SMs).
 //  * Decomposition (the Stream-K rule of the leiblog.wang Stream-K post: keep
 //    every SM busy when the tile count leaves waves part-empty):
 //      tiles >= SMs, count a multiple of the SMs or >= 4 full waves: whole tiles;
 //      tiles >= SMs otherwise: whole tiles for all but the last full wave, the
 //        rest (between 1 and 2 waves' worth) split evenly over all SMs;
 //      tiles < SMs: all k-blocks split evenly over up to one CTA per SM, at
-//        least min_split_iters k-blocks each.
+//        least enough k-blocks per CTA that it reads 4x its fp32 partial tile
+//        in operands (else whole tiles, one per CTA).
 int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
              const Options& o, gemm_plan_t* p) {
   if (!p) return GEMM_ERR_INVALID_ARG;
@@ -84,9 +88,10 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
   }
   if (L.in_dtype == GEMM_F32) {
     if (o.force_kernel >= 0 && o.force_kernel != GEMM_KERNEL_SIMT) return GEMM_ERR_UNSUPPORTED;
-    // 128x128 tiles (2 CTAs per SM) when they make at least four waves or
-    // whole waves; otherwise 64x64 tiles (8 CTAs per SM) so the last wave
-    // leaves fewer SMs idle.
+    // 128x128 tiles (256 threads, 2 CTAs per SM).  Only when those tiles
+    // cannot give every SM one, 64x64 tiles (64 threads) spread the work wider;
+    // measured on 2048^3 the smaller CTAs lose more to per-FMA overhead (FMA
+    // pipe 52 % vs 64 % busy) than they win back in balance.
     int tile;
     if (o.force_tile_n > 0) {
       if (o.force_tile_n != kSimtBM && o.force_tile_n != kSimtSmallTile)
@@ -94,8 +99,7 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
       tile = o.force_tile_n;
     } else {
       const int64_t big = ceil_div(M, kSimtBM) * ceil_div(N, kSimtBN);
-      const int64_t slots = int64_t(2) * num_sms;
-      tile = (big >= 4 * slots || big % slots == 0) ? kSimtBM : kSimtSmallTile;
+      tile = big >= num_sms ? kSimtBM : kSimtSmallTile;
     }
     if (ceil_div(M, tile) > 65535) return GEMM_ERR_UNSUPPORTED;
     p->kernel = GEMM_KERNEL_SIMT;
@@ -172,6 +176,9 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
     if (b_mn && bn < 64) bn = 64;
   } else {
     bn = Nm <= 128 ? 128 : 256;
+    // too few 256-wide tiles to fill half the SMs: 128-wide tiles double the
+    // count and halve each split partial
+    if (bn == 256 && ceil_div(Mm, kBM) * ceil_div(Nm, 256) < num_sms / 2) bn = 128;
   }
   const bool bn_ok = swap ? (bn == 16 || bn == 32 || bn == 64 || bn == 128)
                           : (bn == 128 || bn == 256);
@@ -209,7 +216,15 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
     }
   } else {
     const int64_t total = T * I;
-    const int64_t want = std::max<int64_t>(T, total / std::max(1, o.min_split_iters));
+    // A split CTA writes (and the tile's last CTA reads back) a 128 x bn fp32
+    // partial; give each CTA at least 4x that many bytes of operand k-blocks.
+    int min_iters = o.min_split_iters;
+    if (min_iters <= 0) {
+      const int64_t partial = int64_t(kBM) * bn * 4;
+      const int64_t kblock = int64_t(kBM + bn) * kBK * 2;
+      min_iters = int(ceil_div(4 * partial, kblock));
+    }
+    const int64_t want = std::max<int64_t>(T, total / min_iters);
     grid = std::min(max_grid, want);
     if (grid == T) {
       dp = T;  // one whole tile per CTA

@@ -17,7 +17,7 @@ struct Options {
   int force_kernel = -1;
   int force_tile_n = -1;
   int force_grid = -1;
-  int min_split_iters = 2;
+  int min_split_iters = 0;  // 0: per tile width, so k-work outweighs the partial
   int force_swap = -1;
   int group_m = 16;
   int pair = -1;           // two-SM kernel: 0 never, 1 whenever possible, -1 picker's rule

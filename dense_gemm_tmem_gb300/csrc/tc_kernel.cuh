@@ -398,33 +398,51 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         epi_bar_sync();
         if (*last_flag) {
           __threadfence();
+          // Contributors are read kFixBatch at a time (all loads of a batch in
+          // flight together) and added strictly in ascending order, so the sum
+          // is the same whichever CTA arrives last.
+          constexpr int kFixBatch = CW == 32 ? 2 : 4;  // 64 staged floats per thread
 #pragma unroll 1
           for (int c = 0; c < BN / CW; ++c) {
             float own[CW], acc[CW];
             __syncwarp();
             tmem_load_chunk<CW>(taddr + c * CW, own);
 #pragma unroll 1
-            for (int32_t r = first; r <= last; ++r) {
-              float v[CW];
-              if (r == me) {
+            for (int32_t r0 = first; r0 <= last; r0 += kFixBatch) {
+              float4 part[kFixBatch][CW / 4];
 #pragma unroll
-                for (int j = 0; j < CW; ++j) v[j] = own[j];
-              } else {
-                const float4* src = reinterpret_cast<const float4*>(
-                    args.workspace + size_t(split_slot(W, r, st)) * slot_elems +
-                    (size_t(c) * kBM + row) * CW);
+              for (int b = 0; b < kFixBatch; ++b) {
+                const int32_t r = r0 + b;
+                if (r <= last && r != me) {
+                  const float4* src = reinterpret_cast<const float4*>(
+                      args.workspace + size_t(split_slot(W, r, st)) * slot_elems +
+                      (size_t(c) * kBM + row) * CW);
 #pragma unroll
-                for (int j = 0; j < CW / 4; ++j) {
-                  const float4 t = __ldcg(src + j);
-                  v[4 * j] = t.x; v[4 * j + 1] = t.y; v[4 * j + 2] = t.z; v[4 * j + 3] = t.w;
+                  for (int j = 0; j < CW / 4; ++j) part[b][j] = __ldcg(src + j);
                 }
               }
-              if (r == first) {
 #pragma unroll
-                for (int j = 0; j < CW; ++j) acc[j] = v[j];
-              } else {
+              for (int b = 0; b < kFixBatch; ++b) {
+                const int32_t r = r0 + b;
+                if (r > last) break;
+                float v[CW];
+                if (r == me) {
 #pragma unroll
-                for (int j = 0; j < CW; ++j) acc[j] += v[j];
+                  for (int j = 0; j < CW; ++j) v[j] = own[j];
+                } else {
+#pragma unroll
+                  for (int j = 0; j < CW / 4; ++j) {
+                    v[4 * j] = part[b][j].x; v[4 * j + 1] = part[b][j].y;
+                    v[4 * j + 2] = part[b][j].z; v[4 * j + 3] = part[b][j].w;
+                  }
+                }
+                if (r == first) {
+#pragma unroll
+                  for (int j = 0; j < CW; ++j) acc[j] = v[j];
+                } else {
+#pragma unroll
+                  for (int j = 0; j < CW; ++j) acc[j] += v[j];
+                }
               }
             }
             store_chunk<CW, OUT_F16, TRANS>(args, mm, nbase + c * CW, acc);

@@ -98,7 +98,8 @@ enum {
   GEMM_OPT_FORCE_TILE_N = 1,     /* 16, 32, 64, 128, 256 (tensor-core path), or -1 */
   GEMM_OPT_FORCE_GRID = 2,       /* CTA count for the split path, or -1 */
   GEMM_OPT_WAIT_LIMIT_NS = 3,    /* bound on each device-side wait (default 2e9 ns) */
-  GEMM_OPT_MIN_SPLIT_ITERS = 4,  /* fewest k-blocks per CTA when splitting (default 2) */
+  GEMM_OPT_MIN_SPLIT_ITERS = 4,  /* fewest k-blocks per CTA when splitting (default: enough
+                                    that a CTA reads 4x its fp32 partial tile in operands) */
   GEMM_OPT_FORCE_SWAP_AB = 5,    /* 0 or 1, or -1 for the picker's choice */
   GEMM_OPT_GROUP_M = 6,          /* tile raster group height (default 16) */
   GEMM_OPT_PAIR = 7              /* two-SM kernel: 0 never, 1 whenever the shape allows

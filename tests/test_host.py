@@ -95,13 +95,24 @@ def test_picker_pair_rule_falls_back():
     assert rc == 0 and p.swap_ab == 1 and p.kernel != B.GEMM_KERNEL_TC2
 
 
-def test_picker_small_shape_is_split():
+def test_picker_small_shapes():
+    # 512^3: 8 tiles of 256 would fill too few SMs -> 16 tiles of 128; each has
+    # only 8 k-blocks, fewer than the 8 per CTA a split partial costs -> whole tiles
     rc, p = plan(512, 512, 512)
+    assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC
+    assert (p.tile_n, p.tiles_m, p.tiles_n, p.k_iters) == (128, 4, 4, 8)
+    assert (p.dp_tiles, p.sk_tiles, p.grid, p.workspace_bytes) == (16, 0, 16, 0)
+    # deep K: 16 tiles x 128 k-blocks split over 152 CTAs (>= 8 k-blocks each)
+    rc, p = plan(512, 512, 8192)
     assert rc == 0 and p.kernel == B.GEMM_KERNEL_STREAMK
-    assert (p.tile_n, p.tiles_m, p.tiles_n, p.k_iters) == (256, 4, 2, 8)
-    assert p.sk_tiles == 8 and p.dp_tiles == 0
-    assert p.grid == 32  # 64 k-blocks, at least 2 per CTA
-    assert p.workspace_bytes == 2 * 32 * 128 * 256 * 4
+    assert (p.sk_tiles, p.grid) == (16, 152)
+    assert p.workspace_bytes == 2 * 152 * 128 * 128 * 4
+
+
+@pytest.mark.parametrize("bn,iters", [(256, 11), (128, 8), (64, 6), (32, 4), (16, 2)])
+def test_split_granularity_per_tile_width(bn, iters):
+    """The fewest k-blocks a split CTA gets: 4 x partial bytes / k-block bytes."""
+    assert iters == -(-4 * 128 * bn * 4 // ((128 + bn) * 64 * 2))
 
 
 @pytest.mark.parametrize("M,bn", [(1, 16), (16, 16), (64, 64), (128, 128)])
@@ -126,11 +137,10 @@ def test_picker_hybrid_tail():
 
 def test_picker_fp32_and_degenerate():
     rc, p = plan(2048, 2048, 2048, 0, 0, F32, F32)
-    # 256 tiles of 128 would leave half the SMs with one CTA and half with two:
-    # 1024 tiles of 64 (8 resident per SM) balance to 6.7 per SM
-    assert rc == 0 and p.kernel == B.GEMM_KERNEL_SIMT and (p.tile_m, p.grid) == (64, 1024)
-    rc, p = plan(8192, 8192, 512, 0, 0, F32, F32)   # 4096 tiles of 128 >= 4 waves
-    assert rc == 0 and (p.tile_m, p.grid) == (128, 4096)
+    assert rc == 0 and p.kernel == B.GEMM_KERNEL_SIMT and (p.tile_m, p.grid) == (128, 256)
+    # fewer 128-tiles than SMs: 64x64 tiles spread the work over more SMs
+    rc, p = plan(512, 512, 512, 0, 0, F32, F32)
+    assert rc == 0 and (p.tile_m, p.grid) == (64, 64)
     assert plan(64, 64, 64, 0, 0, F32, F16)[0] == B.GEMM_ERR_UNSUPPORTED
     assert plan(10, 10, 0)[1].kernel == B.GEMM_KERNEL_FILL
     assert plan(0, 10, 10)[1].kernel == B.GEMM_KERNEL_NONE
