@@ -85,6 +85,7 @@ def load(build_if_missing: bool = True):
         "gemm_split_contributors": (c_int, [P(gemm_plan_t), c_int, P(c_int32), P(c_int32)]),
         "gemm_simt_smem_strides": (c_int, [P(c_int32), P(c_int32)]),
         "gemm_selftest_wait_timeout": (c_int, [c_void_p, c_int64, c_void_p]),
+        "gemm_set_trace": (c_int, [c_void_p, c_void_p, c_int64]),
         "gemm_run_noalloc": (c_int, [c_int64, c_int64, c_int64, c_void_p, c_void_p, c_void_p,
                                      c_void_p, gemm_layout_t, c_void_p, c_void_p]),
     }
@@ -185,3 +186,12 @@ def gemm_run_noalloc(M, N, K, A_ptr, B_ptr, bias_ptr, C_ptr, lay: gemm_layout_t,
     return load().gemm_run_noalloc(int(M), int(N), int(K), c_void_p(A_ptr), c_void_p(B_ptr),
                                    c_void_p(bias_ptr), c_void_p(C_ptr), lay,
                                    c_void_p(stream_ptr), c_void_p(status_ptr))
+
+
+def gemm_set_trace(h, dev_buf_ptr, ctas: int) -> int:
+    """Points the handle's tensor-core launches at a device buffer of
+    ctas x 8 uint64 phase stamps (None / 0 turns tracing off)."""
+    return load().gemm_set_trace(c_void_p(h), c_void_p(dev_buf_ptr), int(ctas))
+
+
+TRACE_PHASES = ("start", "first_load", "first_data", "mma_done", "last_accum", "end")

@@ -290,6 +290,8 @@ struct gemm_ctx {
   int* tickets = nullptr;
   int* status = nullptr;
   int last_detail = 0;
+  uint64_t* trace = nullptr;  // caller's device buffer for phase stamps, or NULL
+  int64_t trace_ctas = 0;     // CTA rows it holds (kTraceSlots stamps each)
   dg::Options opt;
   std::mutex mu;  // guards the tensor-map cache
   dg::TmapEntry cache[dg::kTmapCacheSize];
@@ -624,6 +626,8 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, co
   a.wait_limit_ns = h->opt.wait_limit_ns;
   a.a_mn = plan.a_mn_major;
   a.b_mn = plan.b_mn_major;
+  // phase stamps only if the caller's buffer holds one row per CTA
+  a.trace = (h->trace && h->trace_ctas >= plan.grid) ? h->trace : nullptr;
   a.idesc = dg::make_idesc_f16(pair ? dg::kPairBM : dg::kBM, plan.tile_n, plan.a_mn_major,
                                plan.b_mn_major);
   return dg::on_device(h->device, [&]() -> int {
@@ -652,6 +656,13 @@ int gemm_status(gemm_handle_t h, void* stream_ptr) {
 }
 
 int gemm_status_detail(gemm_handle_t h) { return h ? h->last_detail : 0; }
+
+int gemm_set_trace(gemm_handle_t h, uint64_t* dev_buf, int64_t ctas) {
+  if (!h || ctas < 0 || (ctas > 0 && !dev_buf)) return GEMM_ERR_INVALID_ARG;
+  h->trace = ctas > 0 ? dev_buf : nullptr;
+  h->trace_ctas = ctas;
+  return GEMM_OK;
+}
 
 int gemm_selftest_wait_timeout(gemm_handle_t h, int64_t limit_ns, void* stream_ptr) {
   if (!h || limit_ns <= 0) return GEMM_ERR_INVALID_ARG;

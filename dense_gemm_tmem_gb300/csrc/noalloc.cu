@@ -186,5 +186,6 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
   a.a_mn = plan.a_mn_major;
   a.b_mn = plan.b_mn_major;
   a.idesc = make_idesc_f16(pair ? kPairBM : kBM, plan.tile_n, plan.a_mn_major, plan.b_mn_major);
+  a.trace = nullptr;
   return launch_tc(L) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }

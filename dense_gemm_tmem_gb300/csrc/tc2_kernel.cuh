@@ -169,6 +169,7 @@ __device__ __forceinline__ void tc2_producer(const CUtensorMap& tmA, const CUten
         tma_load_2d_pair(b_dst, &tmB, fb, b_row, k0);
         tma_load_2d_pair(b_dst + 8192, &tmB, fb, b_row + 64, k0);
       }
+      if (!issued) trace_mark(args, blockIdx.x, kTraceFirstLoad);
       issued |= 1u << s;
       issued_par = (issued_par & ~(1u << s)) | (ph << s);
       if (++s == S) {
@@ -218,6 +219,7 @@ __device__ __forceinline__ void tc2_mma(const TcArgs& args, uint8_t* sA, uint8_t
         break;
       }
       tc_fence_after();
+      if (!any) trace_mark(args, blockIdx.x, kTraceFirstData);
       const uint64_t adesc = make_sdesc_sw128(smem_u32(sA + s * Cfg::kABytes), a_lbo, 1024);
       const uint64_t bdesc = make_sdesc_sw128(smem_u32(sB + s * Cfg::kBBytes), b_lbo, 1024);
 #pragma unroll
@@ -238,6 +240,7 @@ __device__ __forceinline__ void tc2_mma(const TcArgs& args, uint8_t* sA, uint8_t
       aph ^= 1;
     }
   }
+  trace_mark(args, blockIdx.x, kTraceMmaDone);
   if (!ok && any) {  // every MMA issued so far must finish before TMEM is freed
     tc_commit_pair_self(smem_u32(drain));
     wait_drain(smem_u32(drain), 0, wc);
@@ -262,10 +265,13 @@ __device__ __forceinline__ void tc2_epilogue(const TcArgs& args, uint64_t* acc_f
   Unit u;
   int b = 0;
   uint32_t aph = 0;
+  int units = 0;
   while (it.next(W, u)) {
     const bool got = wait_bounded(smem_u32(&acc_full[b]), aph, wc, kSiteEpilogue);
     if (!epi_all(got)) break;
     tc_fence_after();
+    if (threadIdx.x == 64) trace_mark(args, blockIdx.x, kTraceLastAccum);
+    ++units;
     int32_t tm, tn;
     tile_coords(W, u.tile, tm, tn);
     const int32_t mm = tm * kPairBM + int32_t(rank) * kBM + row;
@@ -285,6 +291,10 @@ __device__ __forceinline__ void tc2_epilogue(const TcArgs& args, uint64_t* acc_f
       b = 0;
       aph ^= 1;
     }
+  }
+  if (threadIdx.x == 64) {
+    trace_mark(args, blockIdx.x, kTraceEnd);
+    if (args.trace) args.trace[size_t(blockIdx.x) * kTraceSlots + kTraceUnits] = uint64_t(units);
   }
 }
 
@@ -341,6 +351,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtl wc{args.wait_limit_ns, args.status, abort_flag};
+  if (threadIdx.x == 0) trace_mark(args, blockIdx.x, kTraceStart);
 
   if (warp == 0) {
     if (lane == 0) tc2_producer<S>(tmA, tmB, args, sA, sB, full, empty, wc, rank, cluster_id);

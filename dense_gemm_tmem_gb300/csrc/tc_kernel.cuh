@@ -70,7 +70,24 @@ struct TcArgs {
   uint64_t wait_limit_ns;
   int32_t a_mn, b_mn;     // operand majors in the MMA view (1 = MN-major)
   uint32_t idesc;         // tcgen05 instruction descriptor
+  uint64_t* trace = nullptr;  // NULL, or kTraceSlots %globaltimer stamps per CTA
 };
+
+// Phase stamps a traced launch writes per CTA (trace[cta * kTraceSlots + i]).
+enum TracePhase : int {
+  kTraceStart = 0,      // setup done (barriers, TMEM), roles about to start
+  kTraceFirstLoad = 1,  // producer issued its first TMA load
+  kTraceFirstData = 2,  // MMA issuer saw its first stage land
+  kTraceMmaDone = 3,    // MMA issuer committed its last accumulator
+  kTraceLastAccum = 4,  // epilogue received its last accumulator
+  kTraceEnd = 5,        // epilogue finished (stores and any split fixup)
+  kTraceUnits = 6,      // number of work units (not a time)
+  kTraceSlots = 8
+};
+
+__device__ __forceinline__ void trace_mark(const TcArgs& a, uint32_t cta, int phase) {
+  if (a.trace) a.trace[size_t(cta) * kTraceSlots + phase] = globaltimer_ns();
+}
 
 __device__ __forceinline__ void epi_bar_sync() {
   asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -240,6 +257,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtl wc{args.wait_limit_ns, args.status, abort_flag};
   const WorkSpec& W = args.work;
+  if (threadIdx.x == 0) trace_mark(args, blockIdx.x, kTraceStart);
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
@@ -250,6 +268,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int s = 0;
       uint32_t ph = 0, issued = 0, issued_par = 0;
       bool ok = true;
+      bool first = true;
       while (ok && it.next(W, u)) {
         int32_t tm, tn;
         tile_coords(W, u.tile, tm, tn);
@@ -277,6 +296,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               for (int j = 0; j < BN / 64; ++j)
                 tma_load_2d(b_dst + j * 8192, &tmB, fb, tn * BN + 64 * j, k0);
             }
+          }
+          if (first) {
+            trace_mark(args, blockIdx.x, kTraceFirstLoad);
+            first = false;
           }
           issued |= 1u << s;
           issued_par = (issued_par & ~(1u << s)) | (ph << s);
@@ -318,6 +341,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
           }
           tc_fence_after();
+          if (!any) trace_mark(args, blockIdx.x, kTraceFirstData);
           const uint64_t adesc = make_sdesc_sw128(smem_u32(sA + s * Cfg::kABytes), a_lbo, 1024);
           const uint64_t bdesc = make_sdesc_sw128(smem_u32(sB + s * Cfg::kBBytes), b_lbo, 1024);
 #pragma unroll
@@ -338,6 +362,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           aph ^= 1;
         }
       }
+      trace_mark(args, blockIdx.x, kTraceMmaDone);
       if (!ok && any) {  // every MMA issued so far must finish before TMEM is freed
         tc_commit(smem_u32(drain));
         wait_drain(smem_u32(drain), 0, wc);
@@ -353,10 +378,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     Unit u;
     int b = 0;
     uint32_t aph = 0;
+    int units = 0;
     while (it.next(W, u)) {
       const bool got = wait_bounded(smem_u32(&acc_full[b]), aph, wc, kSiteEpilogue);
       if (!epi_all(got)) break;
       tc_fence_after();
+      if (et == 0) trace_mark(args, blockIdx.x, kTraceLastAccum);
+      ++units;
       int32_t tm, tn;
       tile_coords(W, u.tile, tm, tn);
       const int32_t mm = tm * kBM + row;
@@ -456,6 +484,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         b = 0;
         aph ^= 1;
       }
+    }
+    if (et == 0) {
+      trace_mark(args, blockIdx.x, kTraceEnd);
+      if (args.trace) args.trace[size_t(blockIdx.x) * kTraceSlots + kTraceUnits] = uint64_t(units);
     }
   }
 

@@ -146,6 +146,17 @@ int gemm_status(gemm_handle_t h, void *stream);
  * 5 drain, 6 the self-test below). */
 int gemm_status_detail(gemm_handle_t h);
 
+/* Phase tracing for the tensor-core kernels.  dev_buf: NULL (tracing off) or a
+ * caller-owned DEVICE buffer of ctas x 8 uint64 values; while set, every
+ * tensor-core launch whose grid fits in `ctas` CTAs writes, for CTA i,
+ * %globaltimer nanoseconds to dev_buf[8*i + p] at phase p: 0 setup done,
+ * 1 first TMA load issued, 2 first stage landed (MMA issuer), 3 last
+ * accumulator committed, 4 last accumulator received by the epilogue,
+ * 5 epilogue done; slot 6 holds the CTA's work-unit count.  Slots a CTA never
+ * reaches (e.g. the MMA slots of the second CTA of a pair) are not written.
+ * Launches with more CTAs than `ctas` are not traced.  Errors: INVALID_ARG. */
+int gemm_set_trace(gemm_handle_t h, uint64_t *dev_buf, int64_t ctas);
+
 /* Failure-path self-test: enqueues one CTA whose wait on an mbarrier that
  * nothing completes gives up after limit_ns nanoseconds, records the expiry
  * in the device status word and returns normally (no trap, no fault).  The
