@@ -234,13 +234,14 @@ __device__ __forceinline__ void tc2_mma(const TcArgs& args, uint8_t* sA, uint8_t
       }
     }
     if (!ok) break;
+    // stamped before the commit, so no epilogue can see it first
+    trace_mark(args, blockIdx.x, kTraceMmaDone);
     tc_commit_pair_both(smem_u32(&acc_full[b]));
     if (++b == 2) {
       b = 0;
       aph ^= 1;
     }
   }
-  trace_mark(args, blockIdx.x, kTraceMmaDone);
   if (!ok && any) {  // every MMA issued so far must finish before TMEM is freed
     tc_commit_pair_self(smem_u32(drain));
     wait_drain(smem_u32(drain), 0, wc);

@@ -356,13 +356,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         if (!ok) break;
+        // stamped before the commit, so the epilogue cannot see it first
+        trace_mark(args, blockIdx.x, kTraceMmaDone);
         tc_commit(smem_u32(&acc_full[b]));
         if (++b == 2) {
           b = 0;
           aph ^= 1;
         }
       }
-      trace_mark(args, blockIdx.x, kTraceMmaDone);
       if (!ok && any) {  // every MMA issued so far must finish before TMEM is freed
         tc_commit(smem_u32(drain));
         wait_drain(smem_u32(drain), 0, wc);
