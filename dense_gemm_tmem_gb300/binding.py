@@ -23,9 +23,10 @@ GEMM_ERR_DEVICE_TIMEOUT = -5
 GEMM_F16, GEMM_F32 = 0, 1
 GEMM_ROW_MAJOR, GEMM_COL_MAJOR = 0, 1
 (GEMM_KERNEL_TC, GEMM_KERNEL_STREAMK, GEMM_KERNEL_SIMT, GEMM_KERNEL_FILL, GEMM_KERNEL_NONE,
- GEMM_KERNEL_TC2) = range(6)
+ GEMM_KERNEL_TC2, GEMM_KERNEL_SPLITC) = range(7)
 (GEMM_OPT_FORCE_KERNEL, GEMM_OPT_FORCE_TILE_N, GEMM_OPT_FORCE_GRID, GEMM_OPT_WAIT_LIMIT_NS,
- GEMM_OPT_MIN_SPLIT_ITERS, GEMM_OPT_FORCE_SWAP_AB, GEMM_OPT_GROUP_M, GEMM_OPT_PAIR) = range(8)
+ GEMM_OPT_MIN_SPLIT_ITERS, GEMM_OPT_FORCE_SWAP_AB, GEMM_OPT_GROUP_M, GEMM_OPT_PAIR,
+ GEMM_OPT_CLUSTER_SPLIT) = range(9)
 
 
 class gemm_layout_t(ctypes.Structure):
@@ -37,7 +38,7 @@ class gemm_plan_t(ctypes.Structure):
     _fields_ = [(n, c_int32) for n in (
         "kernel", "swap_ab", "tile_m", "tile_n", "tile_k", "stages", "grid", "tiles_m",
         "tiles_n", "k_iters", "dp_tiles", "sk_tiles", "a_mn_major", "b_mn_major", "group_m",
-        "reserved")] + [("workspace_bytes", c_int64)]
+        "cluster_split")] + [("workspace_bytes", c_int64)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -194,6 +194,54 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
   int64_t dp = 0, sk = 0, grid = 0;
   const int64_t max_grid = o.force_grid > 0 ? std::min<int64_t>(o.force_grid, G) : G;
 
+  // Cluster split: when the tiles fill few SMs, each tile's k-blocks are split
+  // over a cluster of s CTAs (8, 4 or 2: the largest whose clusters all fit at
+  // once and leave every CTA >= 2 k-blocks).  The CTAs of a cluster add their
+  // fp32 partials through distributed shared memory: no global workspace, and
+  // the hardware co-schedules the cluster, so its barrier always completes.
+  {
+    const bool forced = o.force_kernel == GEMM_KERNEL_SPLITC;
+    int64_t cs = 0;
+    auto fits = [&](int s) {
+      const int64_t cap = o.csplit_clusters[s] > 0 ? o.csplit_clusters[s] : G / s;
+      return T <= cap && T * s <= G;
+    };
+    if (forced) {
+      cs = o.csplit >= 2 ? o.csplit : 4;
+      if (I < cs) return GEMM_ERR_UNSUPPORTED;
+    } else if (o.force_kernel < 0 && o.csplit != 0 && o.force_grid <= 0 && T < G) {
+      if (o.csplit >= 2) {
+        if (fits(o.csplit) && I >= 2 * o.csplit) cs = o.csplit;
+      } else {
+        for (int s : {8, 4, 2})
+          if (fits(s) && I >= 2 * s) {
+            cs = s;
+            break;
+          }
+      }
+    }
+    if (cs > 1) {
+      p->kernel = GEMM_KERNEL_SPLITC;
+      p->swap_ab = swap ? 1 : 0;
+      p->tile_m = kBM;
+      p->tile_n = bn;
+      p->tile_k = kBK;
+      p->stages = tc_stages_for(bn);
+      p->grid = int32_t(T * cs);
+      p->tiles_m = int32_t(tiles_m);
+      p->tiles_n = int32_t(tiles_n);
+      p->k_iters = int32_t(I);
+      p->dp_tiles = 0;
+      p->sk_tiles = int32_t(T);
+      p->a_mn_major = a_mn;
+      p->b_mn_major = b_mn;
+      p->group_m = std::max(1, o.group_m);
+      p->cluster_split = int32_t(cs);
+      p->workspace_bytes = 0;
+      return GEMM_OK;
+    }
+  }
+
   if (o.force_kernel == GEMM_KERNEL_TC) {
     dp = T;
     grid = std::min(max_grid, T);
@@ -262,6 +310,7 @@ WorkSpec spec_of(const gemm_plan_t& p) {
   w.sk_tiles = p.sk_tiles;
   w.grid = p.kernel == GEMM_KERNEL_TC2 ? p.grid / 2 : p.grid;  // pairs work as one unit
   w.group_m = p.group_m;
+  w.csplit = p.kernel == GEMM_KERNEL_SPLITC ? p.cluster_split : 0;
   return w;
 }
 
@@ -423,7 +472,7 @@ int gemm_plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t layout, int num
 int gemm_work_units(const gemm_plan_t* plan, int cta, int32_t* out, int max_units) {
   if (!plan || max_units < 0 || (max_units > 0 && !out)) return GEMM_ERR_INVALID_ARG;
   if (plan->kernel != GEMM_KERNEL_TC && plan->kernel != GEMM_KERNEL_STREAMK &&
-      plan->kernel != GEMM_KERNEL_TC2)
+      plan->kernel != GEMM_KERNEL_TC2 && plan->kernel != GEMM_KERNEL_SPLITC)
     return GEMM_ERR_INVALID_ARG;
   // for the two-SM kernel `cta` numbers CTA pairs
   const int units = plan->kernel == GEMM_KERNEL_TC2 ? plan->grid / 2 : plan->grid;
@@ -446,7 +495,8 @@ int gemm_work_units(const gemm_plan_t* plan, int cta, int32_t* out, int max_unit
 
 int gemm_split_contributors(const gemm_plan_t* plan, int sk_tile, int32_t* first,
                             int32_t* last) {
-  if (!plan || !first || !last || sk_tile < 0 || sk_tile >= plan->sk_tiles)
+  if (!plan || !first || !last || plan->kernel != GEMM_KERNEL_STREAMK || sk_tile < 0 ||
+      sk_tile >= plan->sk_tiles)
     return GEMM_ERR_INVALID_ARG;
   const dg::WorkSpec w = dg::spec_of(*plan);
   dg::split_contributors(w, sk_tile, *first, *last);
@@ -476,6 +526,10 @@ int gemm_create(gemm_handle_t* out, int device) {
     h->num_sms = prop.multiProcessorCount;
     const int pairs = dg::tc2_max_active_clusters(true);
     h->opt.pair_clusters = pairs > 0 ? std::min(pairs, h->num_sms / 2) : h->num_sms / 2;
+    for (int s : {2, 4, 8}) {
+      const int n = dg::tc_max_active_clusters(s);
+      h->opt.csplit_clusters[s] = n > 0 ? std::min(n, h->num_sms / s) : h->num_sms / s;
+    }
     h->workspace_bytes = size_t(2) * h->num_sms * dg::kBM * dg::kMaxTileN * sizeof(float);
     if (cudaMalloc(&h->workspace, h->workspace_bytes) != cudaSuccess) return GEMM_ERR_ALLOC;
     if (cudaMalloc(&h->tickets, sizeof(int) * dg::kTicketCap) != cudaSuccess)
@@ -514,7 +568,7 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value) {
   switch (option) {
     case GEMM_OPT_FORCE_KERNEL:
       if (value >= 0 && value != GEMM_KERNEL_TC && value != GEMM_KERNEL_STREAMK &&
-          value != GEMM_KERNEL_SIMT && value != GEMM_KERNEL_TC2)
+          value != GEMM_KERNEL_SIMT && value != GEMM_KERNEL_TC2 && value != GEMM_KERNEL_SPLITC)
         return GEMM_ERR_INVALID_ARG;
       o.force_kernel = value < 0 ? d.force_kernel : int(value);
       return GEMM_OK;
@@ -543,6 +597,10 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value) {
     case GEMM_OPT_PAIR:
       if (value > 1) return GEMM_ERR_INVALID_ARG;
       o.pair = value < 0 ? d.pair : int(value);
+      return GEMM_OK;
+    case GEMM_OPT_CLUSTER_SPLIT:
+      if (value > 0 && value != 2 && value != 4 && value != 8) return GEMM_ERR_INVALID_ARG;
+      o.csplit = value < 0 ? d.csplit : int(value);
       return GEMM_OK;
     default:
       return GEMM_ERR_INVALID_ARG;

@@ -22,6 +22,8 @@ struct Options {
   int group_m = 16;
   int pair = -1;           // two-SM kernel: 0 never, 1 whenever possible, -1 picker's rule
   int pair_clusters = 0;   // CTA pairs resident at once (0: SMs / 2); set per device
+  int csplit = -1;         // cluster split: -1 picker's rule, 0 never, 2/4/8 forced
+  int csplit_clusters[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};  // clusters of s resident (0: SMs/s)
   uint64_t wait_limit_ns = 2000000000ull;
 };
 
@@ -63,6 +65,8 @@ cudaError_t launch_tc_small(const TcLaunch& L);
 cudaError_t launch_tc2(const TcLaunch& L);
 // Clusters of two that fit on the device at once (-1 if the query fails).
 int tc2_max_active_clusters(bool out_f16);
+// Clusters of s one-SM CTAs (cluster split) that fit at once (-1 on failure).
+int tc_max_active_clusters(int s);
 int tc_stages_for(int bn);
 int tc_smem_bytes_for(int bn);
 

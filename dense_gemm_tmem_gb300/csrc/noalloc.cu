@@ -43,6 +43,7 @@ struct DeviceScratch {
   unsigned char* base = nullptr;  // device address of g_noalloc_scratch
   int num_sms = 0;
   int pairs = 0;                  // CTA pairs of the two-SM kernel resident at once
+  int csplit_clusters[9] = {};    // clusters of s one-SM CTAs resident at once
 };
 
 std::mutex g_na_mu;
@@ -70,6 +71,10 @@ int scratch_for_device(int device, DeviceScratch* out) {
     d.num_sms = sms;
     const int pairs = tc2_max_active_clusters(true);
     d.pairs = pairs > 0 ? (pairs < sms / 2 ? pairs : sms / 2) : sms / 2;
+    for (int s : {2, 4, 8}) {
+      const int n = tc_max_active_clusters(s);
+      d.csplit_clusters[s] = n > 0 ? (n < sms / s ? n : sms / s) : sms / s;
+    }
     d.ready = true;
   }
   *out = d;
@@ -120,6 +125,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
 
   Options opt;
   opt.pair_clusters = sc.pairs;
+  for (int s = 0; s < 9; ++s) opt.csplit_clusters[s] = sc.csplit_clusters[s];
   gemm_plan_t plan;
   rc = plan_for(M, N, K, layout, sc.num_sms, opt, &plan);
   if (rc != GEMM_OK) return rc;
@@ -152,7 +158,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
 
   // The counters must start at zero; the array keeps whatever the last call
   // (possibly an aborted one) left there.
-  if (plan.sk_tiles > 0 &&
+  if (plan.kernel == GEMM_KERNEL_STREAMK &&
       cudaMemsetAsync(counters, 0, sizeof(int) * size_t(plan.sk_tiles), stream) != cudaSuccess)
     return GEMM_ERR_CUDA;
 

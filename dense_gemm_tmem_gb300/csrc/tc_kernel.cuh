@@ -82,6 +82,7 @@ enum TracePhase : int {
   kTraceLastAccum = 4,  // epilogue received its last accumulator
   kTraceEnd = 5,        // epilogue finished (stores and any split fixup)
   kTraceUnits = 6,      // number of work units (not a time)
+  kTraceClusterDone = 7,  // cluster split: the cluster's partials added and stored
   kTraceSlots = 8
 };
 
@@ -199,6 +200,60 @@ __device__ __forceinline__ void store_chunk(const TcArgs& a, int32_t mm, int32_t
         else
           reinterpret_cast<float*>(a.C)[off] = v[j] + bv;
       }
+    }
+  }
+}
+
+// One output element of the cluster split (bounds already checked).
+template <bool OUT_F16>
+__device__ __forceinline__ void put_elem(const TcArgs& a, int64_t off, float v) {
+  if constexpr (OUT_F16)
+    reinterpret_cast<__half*>(a.C)[off] = __float2half_rn(v);
+  else
+    reinterpret_cast<float*>(a.C)[off] = v;
+}
+
+// Cluster split: after every CTA of the cluster parked its fp32 partial of the
+// same tile (rows of BN + 1 floats at the start of its shared memory), CTA
+// `rank` adds rows [rank*R, (rank+1)*R), R = 128 / s, over all s partials in
+// rank order -- rank order is ascending k, so the sum does not depend on timing
+// -- adds the bias and writes C.  Threads walk the direction in which C is
+// contiguous: output columns, or (swapped operands, transposed store) rows.
+template <int BN, bool OUT_F16, bool TRANS>
+__device__ __forceinline__ void csplit_reduce(const TcArgs& a, const uint8_t* smem, int et) {
+  const WorkSpec& W = a.work;
+  const int s = W.csplit;
+  const int rank = int(blockIdx.x) % s;
+  const int R = kBM / s;
+  int32_t tm, tn;
+  tile_coords(W, int32_t(blockIdx.x) / s, tm, tn);
+  const uint32_t local = smem_u32(smem);
+  uint32_t peer[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) peer[j] = j < s ? map_to_rank(local, uint32_t(j)) : 0u;
+  const int total = R * BN;
+#pragma unroll 1
+  for (int e = et; e < total; e += kEpiThreads) {
+    const int r = TRANS ? (e % R) : (e / BN);  // row inside this CTA's slice
+    const int col = TRANS ? (e / R) : (e % BN);
+    const int row = rank * R + r;
+    const uint32_t off = uint32_t(row * (BN + 1) + col) * 4u;
+    float part[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) part[j] = j < s ? ld_dsmem_f32(peer[j] + off) : 0.f;
+    float acc = part[0];
+#pragma unroll
+    for (int j = 1; j < 8; ++j)
+      if (j < s) acc += part[j];
+    const int32_t mm = tm * kBM + row;  // MMA-view row
+    const int32_t nn = tn * BN + col;   // MMA-view column
+    if (mm >= a.Mm || nn >= a.Nm) continue;
+    if constexpr (!TRANS) {
+      if (a.bias) acc += __ldg(a.bias + nn);
+      put_elem<OUT_F16>(a, int64_t(mm) * a.ldc + nn, acc);
+    } else {
+      if (a.bias) acc += __ldg(a.bias + mm);
+      put_elem<OUT_F16>(a, int64_t(nn) * a.ldc + mm, acc);
     }
   }
 }
@@ -392,7 +447,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int32_t nbase = tn * BN;
       const uint32_t taddr = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(b * BN);
 
-      if (!unit_is_partial(W, u)) {
+      if (W.csplit > 1) {
+        // Cluster split: park this CTA's fp32 partial in its own (now idle)
+        // stage ring, row r at r * (BN + 1) floats; the cluster adds the
+        // partials after the kernel's roles finish (csplit_reduce).
+        float* park = reinterpret_cast<float*>(smem);
+        fence_proxy_async_smem();  // the ring was last touched by TMA and MMA
+#pragma unroll 1
+        for (int c = 0; c < BN / CW; ++c) {
+          float v[CW];
+          __syncwarp();
+          tmem_load_chunk<CW>(taddr + c * CW, v);
+#pragma unroll
+          for (int j = 0; j < CW; ++j) park[row * (BN + 1) + c * CW + j] = v[j];
+        }
+      } else if (!unit_is_partial(W, u)) {
 #pragma unroll 1
         for (int c = 0; c < BN / CW; ++c) {
           float v[CW];
@@ -493,6 +562,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 
   __syncthreads();
+  if (W.csplit > 1) {
+    // Every thread of every CTA of the cluster reaches both barriers, aborted
+    // or not, so neither can wait forever.
+    cluster_sync_all();  // all partials parked
+    if (warp >= 2) csplit_reduce<BN, OUT_F16, TRANS>(args, smem, threadIdx.x - 64);
+    cluster_sync_all();  // no CTA still reads another's shared memory
+    if (threadIdx.x == 0) trace_mark(args, blockIdx.x, kTraceClusterDone);
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::kTmemCols);

@@ -14,8 +14,49 @@ cudaError_t launch_tc_inst(const TcLaunch& L) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
-  kern<<<L.grid, kTcThreads, Cfg::kSmemBytes, L.stream>>>(L.tmA, L.tmB, L.args);
-  return cudaGetLastError();
+  const int s = L.args.work.csplit;
+  if (s <= 1) {
+    kern<<<L.grid, kTcThreads, Cfg::kSmemBytes, L.stream>>>(L.tmA, L.tmB, L.args);
+    return cudaGetLastError();
+  }
+  // cluster split: clusters of s CTAs along x, one tile per cluster
+  if (s > 8 || L.grid % s != 0) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(s);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(unsigned(L.grid), 1, 1);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = L.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.args);
+}
+
+// Clusters of `s` CTAs of this instantiation that fit on the device at once.
+template <int BN, bool OUT_F16, bool TRANS>
+int max_active_clusters_inst(int s) {
+  using Cfg = TcConfig<BN>;
+  auto kern = tc_gemm_kernel<BN, OUT_F16, TRANS>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg::kSmemBytes) != cudaSuccess)
+    return -1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(s);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(unsigned(s), 1, 1);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  return cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess ? n : -1;
 }
 
 }  // namespace dg

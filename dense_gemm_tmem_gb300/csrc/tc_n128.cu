@@ -7,4 +7,8 @@ cudaError_t launch_tc_n128(const TcLaunch& L) {
     return L.out_f16 ? launch_tc_inst<128, true, true>(L) : launch_tc_inst<128, false, true>(L);
   return L.out_f16 ? launch_tc_inst<128, true, false>(L) : launch_tc_inst<128, false, false>(L);
 }
+
+// Cluster-split capacity: every instantiation uses one CTA per SM and about
+// the same shared memory, so one of them stands for all.
+int tc_max_active_clusters(int s) { return max_active_clusters_inst<128, false, false>(s); }
 }  // namespace dg

@@ -27,6 +27,7 @@ struct WorkSpec {
   int32_t sk_tiles;  // split tiles, numbered dp_tiles .. dp_tiles + sk_tiles - 1
   int32_t grid;      // CTAs
   int32_t group_m;   // raster group height (tile rows)
+  int32_t csplit;    // > 1: cluster split, tile = cta / csplit, k range by rank
 };
 
 struct Unit {
@@ -57,6 +58,18 @@ struct WorkIter {
 
   __host__ __device__ __forceinline__ void init(const WorkSpec& w, int32_t cta) {
     next_dp = cta;
+    if (w.csplit > 1) {
+      // Cluster split (a k-split whose partials are added on chip by the CTAs
+      // of one cluster): CTA `cta` owns tile cta / s and the rank-th of s equal
+      // contiguous k-block ranges, rank = cta % s.  Encoded as a one-iteration
+      // "split region" walk: x = first k-block, end = one past the last.
+      const int32_t s = w.csplit;
+      const int32_t rank = cta % s;
+      next_dp = w.dp_tiles;  // no whole-tile phase
+      x = int64_t(cta / s) * w.k_iters + int64_t(rank) * w.k_iters / s;
+      end = int64_t(cta / s) * w.k_iters + int64_t(rank + 1) * w.k_iters / s;
+      return;
+    }
     if (w.sk_tiles > 0) {
       x = split_start(w, cta);
       end = split_start(w, int64_t(cta) + 1);

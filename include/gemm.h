@@ -66,8 +66,11 @@ enum {
   GEMM_KERNEL_SIMT = 2,     /* CUDA-core fp32 GEMM */
   GEMM_KERNEL_FILL = 3,     /* K == 0: C = bias (or 0) */
   GEMM_KERNEL_NONE = 4,     /* M == 0 or N == 0: nothing to do */
-  GEMM_KERNEL_TC2 = 5       /* two-SM tcgen05 GEMM (CTA pairs, cta_group::2), whole
+  GEMM_KERNEL_TC2 = 5,      /* two-SM tcgen05 GEMM (CTA pairs, cta_group::2), whole
                                256 x 256 tiles; tile_m = tile_n = 256, grid = 2 x pairs */
+  GEMM_KERNEL_SPLITC = 6    /* one-SM tcgen05 GEMM with each tile's k-blocks split over a
+                               cluster of cluster_split CTAs, whose fp32 partials are added
+                               in distributed shared memory (no global workspace) */
 };
 
 /* What gemm_run will launch for a shape.  "MMA view": with swap_ab = 1 the
@@ -88,7 +91,7 @@ typedef struct {
   int32_t a_mn_major;  /* MMA-view A operand is M-contiguous (else K-contiguous) */
   int32_t b_mn_major;  /* MMA-view B operand is N-contiguous (else K-contiguous) */
   int32_t group_m;     /* tile raster: groups of group_m tile rows */
-  int32_t reserved;
+  int32_t cluster_split; /* GEMM_KERNEL_SPLITC: CTAs per tile (2, 4 or 8), else 0 */
   int64_t workspace_bytes; /* fp32 partial-tile bytes the split needs */
 } gemm_plan_t;
 
@@ -102,8 +105,10 @@ enum {
                                     that a CTA reads 4x its fp32 partial tile in operands) */
   GEMM_OPT_FORCE_SWAP_AB = 5,    /* 0 or 1, or -1 for the picker's choice */
   GEMM_OPT_GROUP_M = 6,          /* tile raster group height (default 16) */
-  GEMM_OPT_PAIR = 7              /* two-SM kernel: 0 never, 1 whenever the shape allows
+  GEMM_OPT_PAIR = 7,             /* two-SM kernel: 0 never, 1 whenever the shape allows
                                     (not swapped), -1 the picker's rule */
+  GEMM_OPT_CLUSTER_SPLIT = 8     /* cluster split: 0 never (Stream-K instead), 2/4/8 CTAs
+                                    per tile when a split is chosen, -1 the picker's rule */
 };
 
 /* Creates a handle on CUDA device `device`.  Allocates, on that device, the

@@ -43,6 +43,17 @@ def streamk_ranges(total_iters: int, ctas: int):
             for r in range(ctas)]
 
 
+def cluster_split_units(tiles: int, iters_per_tile: int, split: int):
+    """Plain k-split of every tile into `split` equal contiguous ranges, one
+    per CTA of the tile's cluster: CTA c owns tile c // split and k-blocks
+    floor(r*I/split) .. floor((r+1)*I/split)-1, r = c % split."""
+    out = []
+    for c in range(tiles * split):
+        t, r = divmod(c, split)
+        out.append([(t, r * iters_per_tile // split, (r + 1) * iters_per_tile // split)])
+    return out
+
+
 def streamk_units(dp_tiles: int, sk_tiles: int, iters_per_tile: int, ctas: int):
     """Work units of every CTA, in the order each CTA processes them.
 

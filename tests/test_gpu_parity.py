@@ -15,8 +15,8 @@ from gpu_helpers import (as_f64, check, reset_opts, run, sample_rows, set_opts, 
 
 pytestmark = pytest.mark.gpu
 F16, F32 = inputs.F16, inputs.F32
-TC, SK, SIMT, TC2 = (B.GEMM_KERNEL_TC, B.GEMM_KERNEL_STREAMK, B.GEMM_KERNEL_SIMT,
-                      B.GEMM_KERNEL_TC2)
+TC, SK, SIMT, TC2, SPLITC = (B.GEMM_KERNEL_TC, B.GEMM_KERNEL_STREAMK, B.GEMM_KERNEL_SIMT,
+                              B.GEMM_KERNEL_TC2, B.GEMM_KERNEL_SPLITC)
 
 
 @pytest.fixture(scope="module")
@@ -121,10 +121,31 @@ def test_pair_grid_sizes(g, dev, grid):
     full_check(g, dev, p)
 
 
+@pytest.mark.parametrize("csplit", [2, 4, 8])
+@pytest.mark.parametrize("am,bm", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("odt", [F16, F32])
+def test_cluster_split_layouts(g, dev, csplit, am, bm, odt):
+    """Each tile's 17 k-blocks split over a cluster of 2, 4 or 8 CTAs (ranges
+    of 2 or 3 k-blocks), partials added in distributed shared memory."""
+    set_opts(g, kernel=SPLITC, csplit=csplit)
+    p = problem(296, 520, 1032, am, bm, F16, odt, True, 140 + csplit + am + 2 * bm)
+    pl = g.plan(296, 520, 1032, am, bm, B.GEMM_F16, B.GEMM_F16 if odt == F16 else B.GEMM_F32)
+    assert pl["kernel"] == SPLITC and pl["cluster_split"] == csplit
+    full_check(g, dev, p)
+
+
+@pytest.mark.parametrize("tile_n", [16, 32, 64, 128])
+@pytest.mark.parametrize("csplit", [2, 8])
+def test_cluster_split_swapped(g, dev, tile_n, csplit):
+    set_opts(g, kernel=SPLITC, csplit=csplit, tile_n=tile_n, swap=1)
+    p = problem(72, 640, 1032, 0, 0, F16, F32, True, 150 + tile_n)
+    full_check(g, dev, p)
+
+
 def test_split_many_contributors(g, dev):
     """One output tile whose 256 k-blocks are split over 128 CTAs (2 each):
     the fixup adds 128 partials in batches."""
-    set_opts(g, min_split=2)
+    set_opts(g, kernel=SK, grid=128)
     p = problem(128, 128, 16384, 0, 0, F16, F32, True, 61)
     pl = g.plan(128, 128, 16384)
     assert pl["kernel"] == SK and pl["grid"] == 128
@@ -132,7 +153,7 @@ def test_split_many_contributors(g, dev):
 
 
 # ---------------------------------------------------------- closed forms --
-@pytest.mark.parametrize("kernel", [TC, SK, TC2])
+@pytest.mark.parametrize("kernel", [TC, SK, TC2, SPLITC])
 @pytest.mark.parametrize("bm", [0, 1])
 def test_permutation_rows_exact(g, dev, kernel, bm):
     """A = P: C must be B's rows permuted, exactly (catches swizzle, descriptor
@@ -149,7 +170,7 @@ def test_permutation_rows_exact(g, dev, kernel, bm):
     assert np.array_equal(got, Bl[perm].astype(np.float64))
 
 
-@pytest.mark.parametrize("kernel", [TC, SK, TC2])
+@pytest.mark.parametrize("kernel", [TC, SK, TC2, SPLITC])
 def test_permutation_columns_exact(g, dev, kernel):
     set_opts(g, kernel=kernel)
     n = 512
@@ -172,6 +193,8 @@ def test_permutation_columns_exact(g, dev, kernel):
     ("simt_col", 200, 300, 500, 1, 1, F32, F32, {}),
     ("pair", 520, 776, 1032, 0, 1, F16, F32, {"kernel": TC2}),
     ("pair16", 296, 520, 2048, 1, 0, F16, F16, {"kernel": TC2, "grid": 4}),
+    ("csplit", 296, 520, 2048, 0, 1, F16, F32, {"kernel": SPLITC, "csplit": 8}),
+    ("csplit_swap", 16, 2048, 4096, 0, 0, F16, F16, {"kernel": SPLITC, "csplit": 4}),
 ])
 def test_integer_inputs_exact(g, dev, case):
     """Integer-valued inputs: every partial sum is an integer below 2^24, so
@@ -298,7 +321,7 @@ def test_side_stream(g, dev):
 
 
 # ----------------------------------------------------------- determinism --
-@pytest.mark.parametrize("kernel,grid", [(SK, -1), (SK, 29), (TC, -1), (TC2, -1)])
+@pytest.mark.parametrize("kernel,grid", [(SK, -1), (SK, 29), (TC, -1), (TC2, -1), (SPLITC, -1)])
 def test_bitwise_repeatable(g, dev, kernel, grid):
     set_opts(g, kernel=kernel, grid=grid)
     p = problem(520, 776, 2056, 0, 1, F16, F32, True, 130, kind="normal")

@@ -96,16 +96,21 @@ def test_picker_pair_rule_falls_back():
 
 
 def test_picker_small_shapes():
-    # 512^3: 8 tiles of 256 would fill too few SMs -> 16 tiles of 128; each has
-    # only 8 k-blocks, fewer than the 8 per CTA a split partial costs -> whole tiles
+    # 512^3: 8 tiles of 256 would fill too few SMs -> 16 tiles of 128; 8 k-blocks
+    # each: clusters of 4 CTAs split every tile (8-CTA clusters would leave one
+    # k-block per CTA)
     rc, p = plan(512, 512, 512)
-    assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC
+    assert rc == 0 and p.kernel == B.GEMM_KERNEL_SPLITC
     assert (p.tile_n, p.tiles_m, p.tiles_n, p.k_iters) == (128, 4, 4, 8)
-    assert (p.dp_tiles, p.sk_tiles, p.grid, p.workspace_bytes) == (16, 0, 16, 0)
-    # deep K: 16 tiles x 128 k-blocks split over 152 CTAs (>= 8 k-blocks each)
+    assert (p.cluster_split, p.grid, p.sk_tiles, p.workspace_bytes) == (4, 64, 16, 0)
+    # deep K: 16 tiles in clusters of 8
     rc, p = plan(512, 512, 8192)
+    assert rc == 0 and p.kernel == B.GEMM_KERNEL_SPLITC
+    assert (p.cluster_split, p.grid) == (8, 128)
+    # 80 tiles: clusters of 2 would need 160 CTAs -> Stream-K over 152 CTAs
+    rc, p = plan(1280, 1024, 4096)
     assert rc == 0 and p.kernel == B.GEMM_KERNEL_STREAMK
-    assert (p.sk_tiles, p.grid) == (16, 152)
+    assert (p.tile_n, p.sk_tiles, p.grid, p.cluster_split) == (128, 80, 152, 0)
     assert p.workspace_bytes == 2 * 152 * 128 * 128 * 4
 
 
@@ -119,9 +124,10 @@ def test_split_granularity_per_tile_width(bn, iters):
 def test_picker_skinny_swaps_operands(M, bn):
     rc, p = plan(M, 4096, 4096)
     assert rc == 0 and p.swap_ab == 1 and p.tile_n == bn
-    assert p.kernel == B.GEMM_KERNEL_STREAMK
+    # 32 tiles: clusters of 4 CTAs (128 CTAs), 16 k-blocks each
+    assert p.kernel == B.GEMM_KERNEL_SPLITC and p.cluster_split == 4
     assert (p.tiles_m, p.tiles_n, p.k_iters) == (32, 1, 64)
-    assert p.grid == SMS
+    assert p.grid == 128 and p.workspace_bytes == 0
     assert (p.a_mn_major, p.b_mn_major) == (1, 0)  # Bᵀ is N-contiguous, A is K-contiguous
 
 
@@ -168,11 +174,16 @@ def test_work_units_match_oracle_reading(M, N, K, am, bm):
     assert rc == 0
     # the two-SM kernel hands work to CTA pairs
     units = p.grid // 2 if p.kernel == B.GEMM_KERNEL_TC2 else p.grid
-    ref = schedule.streamk_units(p.dp_tiles, p.sk_tiles, p.k_iters, units)
+    if p.kernel == B.GEMM_KERNEL_SPLITC:
+        ref = schedule.cluster_split_units(p.sk_tiles, p.k_iters, p.cluster_split)
+    else:
+        ref = schedule.streamk_units(p.dp_tiles, p.sk_tiles, p.k_iters, units)
     for c in range(units):
         assert B.gemm_work_units(p, c) == ref[c]
     with pytest.raises(B.GemmError):
         B.gemm_work_units(p, units)
+    if p.kernel != B.GEMM_KERNEL_STREAMK:
+        return
     # contributors of each split tile: the CTAs touching it, in k order
     owners = {}
     for c, units in enumerate(ref):

@@ -54,3 +54,15 @@ def test_streamk_units_partition_every_iteration(dp, sk, I, G):
             if tile < dp:
                 assert (k0, k1) == (0, I) and tile % G == c
     assert len(seen) == (dp + sk) * I
+
+
+@pytest.mark.parametrize("T,I,s", [(32, 64, 4), (16, 8, 4), (1, 256, 8), (5, 3, 2), (7, 17, 8)])
+def test_cluster_split_partitions_every_iteration(T, I, s):
+    units = schedule.cluster_split_units(T, I, s)
+    assert len(units) == T * s
+    seen = set()
+    for c, lst in enumerate(units):
+        (tile, k0, k1), = lst
+        assert tile == c // s and 0 <= k0 <= k1 <= I
+        seen.update((tile, k) for k in range(k0, k1))
+    assert len(seen) == T * I
