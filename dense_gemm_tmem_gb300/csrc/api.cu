@@ -203,8 +203,9 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
     const bool forced = o.force_kernel == GEMM_KERNEL_SPLITC;
     int64_t cs = 0;
     auto fits = [&](int s) {
-      const int64_t cap = o.csplit_clusters[s] > 0 ? o.csplit_clusters[s] : G / s;
-      return T <= cap && T * s <= G;
+      // capacity: measured clusters resident at once; 0 = unknown (SMs / s); < 0 = none
+      const int64_t cap = o.csplit_clusters[s] != 0 ? o.csplit_clusters[s] : G / s;
+      return cap > 0 && T <= cap && T * s <= G;
     };
     if (forced) {
       cs = o.csplit >= 2 ? o.csplit : 4;
@@ -528,7 +529,9 @@ int gemm_create(gemm_handle_t* out, int device) {
     h->opt.pair_clusters = pairs > 0 ? std::min(pairs, h->num_sms / 2) : h->num_sms / 2;
     for (int s : {2, 4, 8}) {
       const int n = dg::tc_max_active_clusters(s);
-      h->opt.csplit_clusters[s] = n > 0 ? std::min(n, h->num_sms / s) : h->num_sms / s;
+      // n == 0: clusters of s cannot be scheduled at all (-1 keeps the picker off them);
+      // a failed query leaves the SMs / s estimate
+      h->opt.csplit_clusters[s] = n > 0 ? std::min(n, h->num_sms / s) : n == 0 ? -1 : h->num_sms / s;
     }
     h->workspace_bytes = size_t(2) * h->num_sms * dg::kBM * dg::kMaxTileN * sizeof(float);
     if (cudaMalloc(&h->workspace, h->workspace_bytes) != cudaSuccess) return GEMM_ERR_ALLOC;

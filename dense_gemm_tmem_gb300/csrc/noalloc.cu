@@ -73,7 +73,7 @@ int scratch_for_device(int device, DeviceScratch* out) {
     d.pairs = pairs > 0 ? (pairs < sms / 2 ? pairs : sms / 2) : sms / 2;
     for (int s : {2, 4, 8}) {
       const int n = tc_max_active_clusters(s);
-      d.csplit_clusters[s] = n > 0 ? (n < sms / s ? n : sms / s) : sms / s;
+      d.csplit_clusters[s] = n > 0 ? (n < sms / s ? n : sms / s) : n == 0 ? -1 : sms / s;
     }
     d.ready = true;
   }
