@@ -41,6 +41,9 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch the timed steps one by one from the host instead of "
+                         "replaying them as one CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target duration of the CPU-baseline sample")
     return ap.parse_args()
@@ -284,12 +287,12 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     launches_per_step = 0 if plan["kernel"] == B.GEMM_KERNEL_NONE else 1
 
-    def step(i):
+    def step(i, s):
         A, Bd, bias, C = sets[i % copies]
-        g.run(A, Bd, C, bias, p.a_major, p.b_major, stream=stream)
+        g.run(A, Bd, C, bias, p.a_major, p.b_major, stream=s)
 
     for i in range(args.warmup):
-        step(i)
+        step(i, stream)
     g.status(stream)
 
     def barrier():
@@ -297,20 +300,44 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
+    # The K timed steps are recorded once as a CUDA graph and replayed on the
+    # launching stream: every step's kernel runs in full, without the host's
+    # per-call launch latency between them (which would dominate microsecond
+    # kernels).  --eager launches them one by one instead.
+    graph = None
+    if not args.eager:
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap, capture_error_mode="relaxed"):
+            for i in range(args.steps):
+                step(i, cap)
+        torch.cuda.synchronize(dev)
+        graph.replay()  # one untimed replay
+        torch.cuda.synchronize(dev)
+        g.status(stream)
+
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.25)  # first sample lands before the region
     barrier()
     ev[0].record(stream)
-    for i in range(args.steps):
-        step(i)
-        ev[i + 1].record(stream)
+    if graph is not None:
+        graph.replay()
+        ev[args.steps].record(stream)
+    else:
+        for i in range(args.steps):
+            step(i, stream)
+            ev[i + 1].record(stream)
     barrier()
     clocks = sampler.stop()
     g.status(stream)
-    per_launch_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
     elapsed_ms = ev[0].elapsed_time(ev[args.steps])
+    if graph is not None:
+        per_launch_ms = [elapsed_ms / args.steps]  # back-to-back launches inside the replay
+    else:
+        per_launch_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
     elapsed = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
     if dist is not None:
         dist.all_reduce(elapsed, op=dist.ReduceOp.MAX)
@@ -399,6 +426,8 @@ def run_ours(args):
                 "out_dtype": p.out_dtype, "bias": p.bias is not None,
                 "accumulate": "f32", "description": w.description,
                 "parallelism": "replicas x%d" % world,
+                "timing": "eager launches" if graph is None
+                else "the K steps replayed as one CUDA graph on the launching stream",
                 "l2": ("inputs exceed L2 (%d MiB per step)" % (step_bytes >> 20)) if copies == 1
                 else "rotating %d input copies (%d MiB) so each step misses L2"
                      % (copies, (copies * step_bytes) >> 20),
