@@ -140,6 +140,16 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
   return v;
 }
 
+// 16-byte load from another CTA's shared memory (address 16-byte aligned).
+__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t cluster_addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(cluster_addr)
+               : "memory");
+  return v;
+}
+
 // Orders this thread's earlier async-proxy accesses (TMA, tcgen05) to shared
 // memory before its following generic-proxy accesses.
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -213,47 +213,117 @@ __device__ __forceinline__ void put_elem(const TcArgs& a, int64_t off, float v) 
     reinterpret_cast<float*>(a.C)[off] = v;
 }
 
+// Parked partial layouts of the cluster split (floats): row-major rows of
+// BN + 4, or column-major columns of 128 + 4 for the transposed store.  The 4
+// extra floats keep 16-byte alignment and spread the column walk over banks.
+template <int BN>
+constexpr int kParkRowStride = BN + 4;
+constexpr int kParkColStride = kBM + 4;
+
+// Four consecutive outputs along C's contiguous direction, `valid` of them
+// inside the matrix; one vector store when aligned and whole.
+template <bool OUT_F16>
+__device__ __forceinline__ void put4(const TcArgs& a, int64_t off, float4 v, int valid) {
+  const float f[4] = {v.x, v.y, v.z, v.w};
+  if constexpr (OUT_F16) {
+    __half* dst = reinterpret_cast<__half*>(a.C) + off;
+    if (valid == 4 && (reinterpret_cast<uintptr_t>(dst) & 7) == 0) {
+      __half2 h0 = __floats2half2_rn(f[0], f[1]);
+      __half2 h1 = __floats2half2_rn(f[2], f[3]);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&h0);
+      pk.y = *reinterpret_cast<uint32_t*>(&h1);
+      *reinterpret_cast<uint2*>(dst) = pk;
+      return;
+    }
+  } else {
+    float* dst = reinterpret_cast<float*>(a.C) + off;
+    if (valid == 4 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+      *reinterpret_cast<float4*>(dst) = v;
+      return;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (j < valid) put_elem<OUT_F16>(a, off + j, f[j]);
+}
+
 // Cluster split: after every CTA of the cluster parked its fp32 partial of the
-// same tile (rows of BN + 1 floats at the start of its shared memory), CTA
-// `rank` adds rows [rank*R, (rank+1)*R), R = 128 / s, over all s partials in
-// rank order -- rank order is ascending k, so the sum does not depend on timing
-// -- adds the bias and writes C.  Threads walk the direction in which C is
-// contiguous: output columns, or (swapped operands, transposed store) rows.
+// same tile at the start of its shared memory, CTA `rank` adds rows
+// [rank*R, (rank+1)*R), R = 128 / s, over all s partials in rank order -- rank
+// order is ascending k, so the sum does not depend on timing -- adds the bias
+// and writes C.  Work goes in groups of 4 floats along the direction in which
+// C is contiguous (output columns, or rows for the transposed store); each
+// thread keeps the s remote 16-byte loads of two groups in flight at once.
 template <int BN, bool OUT_F16, bool TRANS>
 __device__ __forceinline__ void csplit_reduce(const TcArgs& a, const uint8_t* smem, int et) {
   const WorkSpec& W = a.work;
   const int s = W.csplit;
   const int rank = int(blockIdx.x) % s;
-  const int R = kBM / s;
+  const int R = kBM / s;  // 64, 32 or 16 rows
   int32_t tm, tn;
   tile_coords(W, int32_t(blockIdx.x) / s, tm, tn);
   const uint32_t local = smem_u32(smem);
   uint32_t peer[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) peer[j] = j < s ? map_to_rank(local, uint32_t(j)) : 0u;
-  const int total = R * BN;
+  const int groups = TRANS ? BN * (R / 4) : R * (BN / 4);
+  constexpr int kU = 2;
 #pragma unroll 1
-  for (int e = et; e < total; e += kEpiThreads) {
-    const int r = TRANS ? (e % R) : (e / BN);  // row inside this CTA's slice
-    const int col = TRANS ? (e / R) : (e % BN);
-    const int row = rank * R + r;
-    const uint32_t off = uint32_t(row * (BN + 1) + col) * 4u;
-    float part[8];
+  for (int g0 = et; g0 < groups; g0 += kU * kEpiThreads) {
+    float4 part[kU][8];
+    int row[kU], col[kU];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) part[j] = j < s ? ld_dsmem_f32(peer[j] + off) : 0.f;
-    float acc = part[0];
+    for (int u = 0; u < kU; ++u) {
+      const int g = g0 + u * kEpiThreads;
+      if (TRANS) {
+        col[u] = g / (R / 4);
+        row[u] = rank * R + (g % (R / 4)) * 4;
+      } else {
+        row[u] = rank * R + g / (BN / 4);
+        col[u] = (g % (BN / 4)) * 4;
+      }
+      if (g < groups) {
+        const uint32_t off =
+            4u * uint32_t(TRANS ? col[u] * kParkColStride + row[u] : row[u] * kParkRowStride<BN> + col[u]);
 #pragma unroll
-    for (int j = 1; j < 8; ++j)
-      if (j < s) acc += part[j];
-    const int32_t mm = tm * kBM + row;  // MMA-view row
-    const int32_t nn = tn * BN + col;   // MMA-view column
-    if (mm >= a.Mm || nn >= a.Nm) continue;
-    if constexpr (!TRANS) {
-      if (a.bias) acc += __ldg(a.bias + nn);
-      put_elem<OUT_F16>(a, int64_t(mm) * a.ldc + nn, acc);
-    } else {
-      if (a.bias) acc += __ldg(a.bias + mm);
-      put_elem<OUT_F16>(a, int64_t(nn) * a.ldc + mm, acc);
+        for (int j = 0; j < 8; ++j)
+          if (j < s) part[u][j] = ld_dsmem_f32x4(peer[j] + off);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (g0 + u * kEpiThreads >= groups) break;
+      float4 acc = part[u][0];
+#pragma unroll
+      for (int j = 1; j < 8; ++j)
+        if (j < s) {
+          acc.x += part[u][j].x; acc.y += part[u][j].y;
+          acc.z += part[u][j].z; acc.w += part[u][j].w;
+        }
+      const int32_t mm = tm * kBM + row[u];  // MMA-view row (first of 4 when TRANS)
+      const int32_t nn = tn * BN + col[u];   // MMA-view column (first of 4 otherwise)
+      if constexpr (!TRANS) {
+        if (mm >= a.Mm || nn >= a.Nm) continue;
+        const int valid = min(4, a.Nm - nn);
+        if (a.bias) {
+          acc.x += __ldg(a.bias + nn);
+          if (valid > 1) acc.y += __ldg(a.bias + nn + 1);
+          if (valid > 2) acc.z += __ldg(a.bias + nn + 2);
+          if (valid > 3) acc.w += __ldg(a.bias + nn + 3);
+        }
+        put4<OUT_F16>(a, int64_t(mm) * a.ldc + nn, acc, valid);
+      } else {
+        if (mm >= a.Mm || nn >= a.Nm) continue;
+        const int valid = min(4, a.Mm - mm);
+        if (a.bias) {
+          acc.x += __ldg(a.bias + mm);
+          if (valid > 1) acc.y += __ldg(a.bias + mm + 1);
+          if (valid > 2) acc.z += __ldg(a.bias + mm + 2);
+          if (valid > 3) acc.w += __ldg(a.bias + mm + 3);
+        }
+        put4<OUT_F16>(a, int64_t(nn) * a.ldc + mm, acc, valid);
+      }
     }
   }
 }
@@ -449,8 +519,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
       if (W.csplit > 1) {
         // Cluster split: park this CTA's fp32 partial in its own (now idle)
-        // stage ring, row r at r * (BN + 1) floats; the cluster adds the
-        // partials after the kernel's roles finish (csplit_reduce).
+        // stage ring, in the layout the reduction walks (csplit_reduce):
+        // row-major with rows of BN + 4 floats, or, for the transposed store,
+        // column-major with columns of 128 + 4 floats.
         float* park = reinterpret_cast<float*>(smem);
         fence_proxy_async_smem();  // the ring was last touched by TMA and MMA
 #pragma unroll 1
@@ -458,8 +529,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           float v[CW];
           __syncwarp();
           tmem_load_chunk<CW>(taddr + c * CW, v);
+          if constexpr (!TRANS) {
+            float4* dst = reinterpret_cast<float4*>(park + row * kParkRowStride<BN> + c * CW);
 #pragma unroll
-          for (int j = 0; j < CW; ++j) park[row * (BN + 1) + c * CW + j] = v[j];
+            for (int j = 0; j < CW / 4; ++j)
+              dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < CW; ++j) park[(c * CW + j) * kParkColStride + row] = v[j];
+          }
         }
       } else if (!unit_is_partial(W, u)) {
 #pragma unroll 1
