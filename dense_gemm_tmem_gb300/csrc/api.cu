@@ -605,6 +605,10 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value) {
       if (value > 0 && value != 2 && value != 4 && value != 8) return GEMM_ERR_INVALID_ARG;
       o.csplit = value < 0 ? d.csplit : int(value);
       return GEMM_OK;
+    case GEMM_OPT_PDL:
+      if (value > 1) return GEMM_ERR_INVALID_ARG;
+      o.pdl = value < 0 ? d.pdl : int(value);
+      return GEMM_OK;
     default:
       return GEMM_ERR_INVALID_ARG;
   }
@@ -666,6 +670,7 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, co
   L.out_f16 = layout.out_dtype == GEMM_F16;
   L.trans = swap;
   L.pair = pair;
+  L.pdl = h->opt.pdl != 0;
   L.grid = plan.grid;
   L.stream = stream;
   // each CTA loads 128 rows of A; a pair CTA loads half of the 256-column B tile

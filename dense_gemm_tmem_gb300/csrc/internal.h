@@ -23,6 +23,7 @@ struct Options {
   int pair = -1;           // two-SM kernel: 0 never, 1 whenever possible, -1 picker's rule
   int pair_clusters = 0;   // CTA pairs resident at once (0: SMs / 2); set per device
   int csplit = -1;         // cluster split: -1 picker's rule, 0 never, 2/4/8 forced
+  int pdl = 1;             // programmatic dependent launch of the tensor-core kernels
   int csplit_clusters[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};  // clusters of s resident (0: SMs/s)
   uint64_t wait_limit_ns = 2000000000ull;
 };
@@ -47,6 +48,7 @@ struct TcLaunch {
   bool out_f16;
   bool trans;         // swapped operands, transposed store
   bool pair = false;  // two-SM kernel (cluster pairs, 256 x 256 tiles)
+  bool pdl = true;    // programmatic launch: prologue may overlap the previous kernel
   int grid;
   CUtensorMap tmA;
   CUtensorMap tmB;

@@ -112,6 +112,18 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity,
   return true;
 }
 
+// ------------------------------------------------- programmatic launch --
+// Lets the next kernel in the stream start its CTAs (prologue only) while
+// this one finishes.  No-op when the launch did not allow it.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the kernels this one depends on have completed and their
+// memory operations are visible.  No-op when the launch did not allow overlap.
+__device__ __forceinline__ void pdl_wait_prerequisites() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- clusters --
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;

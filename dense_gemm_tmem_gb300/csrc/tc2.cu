@@ -12,8 +12,17 @@ cudaError_t launch_tc2_inst(const TcLaunch& L) {
                                        Tc2Config::kSmemBytes);
   if (e != cudaSuccess) return e;
   // the cluster shape (2, 1, 1) is compiled into the kernel; grid is even
-  kern<<<L.grid, kTcThreads, Tc2Config::kSmemBytes, L.stream>>>(L.tmA, L.tmB, L.args);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(unsigned(L.grid), 1, 1);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = Tc2Config::kSmemBytes;
+  cfg.stream = L.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = L.pdl ? 1u : 0u;
+  return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.args);
 }
 }  // namespace
 

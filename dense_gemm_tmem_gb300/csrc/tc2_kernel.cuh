@@ -332,6 +332,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   cluster_sync_all();  // both CTAs' barriers initialised and TMEM allocated
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // global memory only after the kernels before this one have completed
+  pdl_launch_dependents();
+  pdl_wait_prerequisites();
   const WaitCtl wc{args.wait_limit_ns, args.status, abort_flag};
   if (threadIdx.x == 0) trace_mark(args, blockIdx.x, kTraceStart);
 

@@ -380,6 +380,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Up to here only this CTA's own resources were touched.  Let the next
+  // kernel of the stream start its prologue, and touch global memory
+  // (operands, C, workspace, counters, status, trace) only once the kernels
+  // before this one have completed.
+  pdl_launch_dependents();
+  pdl_wait_prerequisites();
   const WaitCtl wc{args.wait_limit_ns, args.status, abort_flag};
   const WorkSpec& W = args.work;
   if (threadIdx.x == 0) trace_mark(args, blockIdx.x, kTraceStart);

@@ -15,24 +15,31 @@ cudaError_t launch_tc_inst(const TcLaunch& L) {
                                        Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int s = L.args.work.csplit;
-  if (s <= 1) {
-    kern<<<L.grid, kTcThreads, Cfg::kSmemBytes, L.stream>>>(L.tmA, L.tmB, L.args);
-    return cudaGetLastError();
-  }
-  // cluster split: clusters of s CTAs along x, one tile per cluster
-  if (s > 8 || L.grid % s != 0) return cudaErrorInvalidValue;
+  if (s > 8 || (s > 1 && L.grid % s != 0)) return cudaErrorInvalidValue;
+  // Programmatic launch (the prologue may overlap the previous kernel; the
+  // kernel waits for it before touching global memory) and, for the cluster
+  // split, clusters of s CTAs along x, one tile per cluster.
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = unsigned(s);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (L.pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (s > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = unsigned(s);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
   cfg.gridDim = dim3(unsigned(L.grid), 1, 1);
   cfg.blockDim = dim3(kTcThreads, 1, 1);
   cfg.dynamicSmemBytes = Cfg::kSmemBytes;
   cfg.stream = L.stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = unsigned(n);
   return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.args);
 }
 

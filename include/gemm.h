@@ -107,8 +107,11 @@ enum {
   GEMM_OPT_GROUP_M = 6,          /* tile raster group height (default 16) */
   GEMM_OPT_PAIR = 7,             /* two-SM kernel: 0 never, 1 whenever the shape allows
                                     (not swapped), -1 the picker's rule */
-  GEMM_OPT_CLUSTER_SPLIT = 8     /* cluster split: 0 never (Stream-K instead), 2/4/8 CTAs
+  GEMM_OPT_CLUSTER_SPLIT = 8,    /* cluster split: 0 never (Stream-K instead), 2/4/8 CTAs
                                     per tile when a split is chosen, -1 the picker's rule */
+  GEMM_OPT_PDL = 9               /* 1 (default): tensor-core kernels are launched so their
+                                    prologue may overlap the previous kernel on the stream;
+                                    they touch global memory only after it completed. 0: off */
 };
 
 /* Creates a handle on CUDA device `device`.  Allocates, on that device, the
