@@ -162,7 +162,7 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
       p->sk_tiles = 0;
       p->a_mn_major = a_mn;
       p->b_mn_major = b_mn;
-      p->group_m = std::max(1, o.group_m);
+      p->group_m = o.group_m > 0 ? o.group_m : 2048 / kPairBM;
       p->workspace_bytes = 0;
       return GEMM_OK;
     }
@@ -236,7 +236,7 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
       p->sk_tiles = int32_t(T);
       p->a_mn_major = a_mn;
       p->b_mn_major = b_mn;
-      p->group_m = std::max(1, o.group_m);
+      p->group_m = o.group_m > 0 ? o.group_m : 2048 / kBM;
       p->cluster_split = int32_t(cs);
       p->workspace_bytes = 0;
       return GEMM_OK;
@@ -297,7 +297,7 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
   p->sk_tiles = int32_t(sk);
   p->a_mn_major = a_mn;
   p->b_mn_major = b_mn;
-  p->group_m = std::max(1, o.group_m);
+  p->group_m = o.group_m > 0 ? o.group_m : 2048 / kBM;
   p->workspace_bytes = sk > 0 ? int64_t(2) * grid * kBM * bn * 4 : 0;
   return GEMM_OK;
 }

@@ -19,7 +19,7 @@ struct Options {
   int force_grid = -1;
   int min_split_iters = 0;  // 0: per tile width, so k-work outweighs the partial
   int force_swap = -1;
-  int group_m = 16;
+  int group_m = 0;         // tile rows per raster group; 0: 2048 rows of A per group
   int pair = -1;           // two-SM kernel: 0 never, 1 whenever possible, -1 picker's rule
   int pair_clusters = 0;   // CTA pairs resident at once (0: SMs / 2); set per device
   int csplit = -1;         // cluster split: -1 picker's rule, 0 never, 2/4/8 forced

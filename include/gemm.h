@@ -104,7 +104,8 @@ enum {
   GEMM_OPT_MIN_SPLIT_ITERS = 4,  /* fewest k-blocks per CTA when splitting (default: enough
                                     that a CTA reads 4x its fp32 partial tile in operands) */
   GEMM_OPT_FORCE_SWAP_AB = 5,    /* 0 or 1, or -1 for the picker's choice */
-  GEMM_OPT_GROUP_M = 6,          /* tile raster group height (default 16) */
+  GEMM_OPT_GROUP_M = 6,          /* tile rows per raster group (default: 2048 rows of A,
+                                    i.e. 8 pair tiles or 16 one-SM tiles) */
   GEMM_OPT_PAIR = 7,             /* two-SM kernel: 0 never, 1 whenever the shape allows
                                     (not swapped), -1 the picker's rule */
   GEMM_OPT_CLUSTER_SPLIT = 8,    /* cluster split: 0 never (Stream-K instead), 2/4/8 CTAs

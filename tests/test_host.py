@@ -78,6 +78,7 @@ def test_picker_large_square_two_sm_tiles():
     assert (p.tiles_m, p.tiles_n, p.k_iters) == (32, 32, 128)
     assert (p.dp_tiles, p.sk_tiles, p.grid) == (1024, 0, SMS)
     assert (p.swap_ab, p.a_mn_major, p.b_mn_major) == (0, 0, 0)
+    assert p.group_m == 8  # raster groups of 2048 rows of A (8 pair tiles)
     rc, p = plan(16384, 16384, 16384, 0, 0, F16, F16)
     assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC2 and p.b_mn_major == 1
     assert p.dp_tiles == 64 * 64 and p.workspace_bytes == 0
@@ -136,6 +137,7 @@ def test_picker_hybrid_tail():
     rc, p = plan(128 * 157, 256 * 2, 1024)
     assert rc == 0 and p.kernel == B.GEMM_KERNEL_STREAMK
     assert (p.dp_tiles, p.sk_tiles, p.grid) == (152, 162, SMS)
+    assert p.group_m == 16  # 2048 rows of A per raster group (16 one-SM tiles)
     # 200 tiles (1 wave + 48): all split
     rc, p = plan(128 * 10, 256 * 20, 1024)
     assert (p.dp_tiles, p.sk_tiles) == (0, 200)
