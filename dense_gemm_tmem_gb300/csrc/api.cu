@@ -54,7 +54,9 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // ------------------------------------------------------------ tile picker --
 // Chooses kernel, tile, split and grid for a shape.  Rules:
 //  * fp32 inputs -> CUDA-core kernel, 128x128 tiles (64x64 when there are
-//    fewer 128-tiles than SMs).
+//    fewer 128-tiles than SMs).  With 128-tiles the tiles-vs-waves rule below
+//    is applied over the resident CTAs (2 per SM), and a split hands out the
+//    k-blocks in runs of at least 8.
 //  * fp16 inputs -> tcgen05 kernels.  Large shapes whose 256x256 tiles fill
 //    whole waves of CTA pairs -> the two-SM kernel.  Skinny M (M <= 128,
 //    N >= 2M, A row-major) swaps the operands so N fills the 128-row MMA side
@@ -101,17 +103,59 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
       const int64_t big = ceil_div(M, kSimtBM) * ceil_div(N, kSimtBN);
       tile = big >= num_sms ? kSimtBM : kSimtSmallTile;
     }
-    if (ceil_div(M, tile) > 65535) return GEMM_ERR_UNSUPPORTED;
+    const int64_t tiles_m = ceil_div(M, tile), tiles_n = ceil_div(N, tile);
+    const int64_t T = tiles_m * tiles_n;
+    const int64_t I = ceil_div(K, kSimtBK);
+    if (T > INT32_MAX / 2 || I > INT32_MAX / 2 || T * I > (int64_t(1) << 40))
+      return GEMM_ERR_UNSUPPORTED;
+    // Resident CTAs (the split's grid), capped so two partial slots per CTA
+    // fit the handle's workspace.
+    const int64_t per_sm = o.simt_per_sm > 0 ? std::min(o.simt_per_sm, 2) : 2;
+    const int64_t S = per_sm * num_sms;
+    int64_t dp = T, sk = 0, grid = T;
+    if (o.force_grid > 0) {
+      // forced grid: every tile's k-blocks split over that many CTAs
+      dp = 0;
+      sk = T;
+      grid = std::min<int64_t>({o.force_grid, S, T * I});
+      if (grid == T) {
+        dp = T;
+        sk = 0;
+      }
+    } else if (tile == kSimtBM && T >= S) {
+      // the tensor-core rule over resident CTAs: whole waves stay whole; a
+      // part-empty last wave is merged with the wave before it and split
+      const int64_t full = T / S, rem = T % S;
+      if (rem != 0 && full < 4) {
+        dp = (full - 1) * S;
+        sk = T - dp;
+        grid = S;
+      }
+    } else if (tile == kSimtBM) {
+      // fewer tiles than resident CTAs: split all k-blocks over up to S CTAs
+      const int min_iters = o.min_split_iters > 0 ? o.min_split_iters : kSimtMinSplitIters;
+      grid = std::min(S, std::max<int64_t>(T, T * I / min_iters));
+      if (grid > T) {
+        dp = 0;
+        sk = T;
+      } else {
+        grid = T;
+      }
+    }
+    if (sk > kTicketCap) return GEMM_ERR_UNSUPPORTED;
     p->kernel = GEMM_KERNEL_SIMT;
     p->tile_m = tile;
     p->tile_n = tile;
     p->tile_k = kSimtBK;
     p->stages = 2;
-    p->tiles_m = int32_t(ceil_div(M, tile));
-    p->tiles_n = int32_t(ceil_div(N, tile));
-    p->grid = p->tiles_m * p->tiles_n;
-    p->k_iters = int32_t(std::min<int64_t>(ceil_div(K, kSimtBK), INT32_MAX));
-    p->dp_tiles = p->grid;
+    p->tiles_m = int32_t(tiles_m);
+    p->tiles_n = int32_t(tiles_n);
+    p->grid = int32_t(grid);
+    p->k_iters = int32_t(I);
+    p->dp_tiles = int32_t(dp);
+    p->sk_tiles = int32_t(sk);
+    p->group_m = o.group_m > 0 ? o.group_m : 2048 / tile;
+    p->workspace_bytes = sk > 0 ? int64_t(2) * grid * tile * tile * 4 : 0;
     return GEMM_OK;
   }
   // fp16: tensor-core path.
@@ -473,7 +517,8 @@ int gemm_plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t layout, int num
 int gemm_work_units(const gemm_plan_t* plan, int cta, int32_t* out, int max_units) {
   if (!plan || max_units < 0 || (max_units > 0 && !out)) return GEMM_ERR_INVALID_ARG;
   if (plan->kernel != GEMM_KERNEL_TC && plan->kernel != GEMM_KERNEL_STREAMK &&
-      plan->kernel != GEMM_KERNEL_TC2 && plan->kernel != GEMM_KERNEL_SPLITC)
+      plan->kernel != GEMM_KERNEL_TC2 && plan->kernel != GEMM_KERNEL_SPLITC &&
+      plan->kernel != GEMM_KERNEL_SIMT)
     return GEMM_ERR_INVALID_ARG;
   // for the two-SM kernel `cta` numbers CTA pairs
   const int units = plan->kernel == GEMM_KERNEL_TC2 ? plan->grid / 2 : plan->grid;
@@ -496,8 +541,9 @@ int gemm_work_units(const gemm_plan_t* plan, int cta, int32_t* out, int max_unit
 
 int gemm_split_contributors(const gemm_plan_t* plan, int sk_tile, int32_t* first,
                             int32_t* last) {
-  if (!plan || !first || !last || plan->kernel != GEMM_KERNEL_STREAMK || sk_tile < 0 ||
-      sk_tile >= plan->sk_tiles)
+  if (!plan || !first || !last ||
+      (plan->kernel != GEMM_KERNEL_STREAMK && plan->kernel != GEMM_KERNEL_SIMT) ||
+      sk_tile < 0 || sk_tile >= plan->sk_tiles)
     return GEMM_ERR_INVALID_ARG;
   const dg::WorkSpec w = dg::spec_of(*plan);
   dg::split_contributors(w, sk_tile, *first, *last);
@@ -533,6 +579,8 @@ int gemm_create(gemm_handle_t* out, int device) {
       // a failed query leaves the SMs / s estimate
       h->opt.csplit_clusters[s] = n > 0 ? std::min(n, h->num_sms / s) : n == 0 ? -1 : h->num_sms / s;
     }
+    const int simt = dg::simt_ctas_per_sm();
+    h->opt.simt_per_sm = simt > 0 ? simt : 2;
     h->workspace_bytes = size_t(2) * h->num_sms * dg::kBM * dg::kMaxTileN * sizeof(float);
     if (cudaMalloc(&h->workspace, h->workspace_bytes) != cudaSuccess) return GEMM_ERR_ALLOC;
     if (cudaMalloc(&h->tickets, sizeof(int) * dg::kTicketCap) != cudaSuccess)
@@ -649,6 +697,9 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, co
     L.a_major = layout.a_major;
     L.b_major = layout.b_major;
     L.tile = plan.tile_m;
+    L.work = dg::spec_of(plan);
+    L.workspace = h->workspace;
+    L.tickets = h->tickets;
     L.stream = stream;
     return dg::on_device(h->device, [&]() -> int {
       return dg::launch_simt(L) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;

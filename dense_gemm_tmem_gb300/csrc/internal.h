@@ -25,6 +25,7 @@ struct Options {
   int csplit = -1;         // cluster split: -1 picker's rule, 0 never, 2/4/8 forced
   int pdl = 1;             // programmatic dependent launch of the tensor-core kernels
   int csplit_clusters[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};  // clusters of s resident (0: SMs/s)
+  int simt_per_sm = 0;     // 128 x 128 CUDA-core CTAs resident per SM (0: 2); set per device
   uint64_t wait_limit_ns = 2000000000ull;
 };
 
@@ -81,11 +82,17 @@ struct SimtLaunch {
   float* C;
   int a_major, b_major;  // 0 row, 1 column
   int tile = 128;        // square tile edge: kSimtBM (128) or kSimtSmallTile (64)
+  WorkSpec work;         // grid, tiles, raster order and k-split (work.cuh)
+  float* workspace = nullptr;  // split partials (2 tile slots per CTA) when work.sk_tiles > 0
+  int* tickets = nullptr;      // split-tile arrival counters, all 0 between launches
   cudaStream_t stream;
 };
 cudaError_t launch_simt(const SimtLaunch& L);
 constexpr int kSimtBM = 128, kSimtBN = 128, kSimtBK = 8, kSimtThreads = 256;
 constexpr int kSimtSmallTile = 64;  // 64 x 64 tiles, 64 threads
+constexpr int kSimtMinSplitIters = 8;  // fewest k-blocks a split CTA gets
+// CTAs of the 128 x 128 kernel resident on one SM (-1 if the query fails).
+int simt_ctas_per_sm();
 int simt_a_stride();
 int simt_b_stride();
 

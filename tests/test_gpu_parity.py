@@ -191,6 +191,7 @@ def test_permutation_columns_exact(g, dev, kernel):
     ("swap", 16, 2048, 4096, 0, 0, F16, F32, {}),
     ("simt", 200, 300, 500, 0, 0, F32, F32, {}),
     ("simt_col", 200, 300, 500, 1, 1, F32, F32, {}),
+    ("simt_split", 300, 420, 1000, 1, 0, F32, F32, {"grid": 23}),
     ("pair", 520, 776, 1032, 0, 1, F16, F32, {"kernel": TC2}),
     ("pair16", 296, 520, 2048, 1, 0, F16, F16, {"kernel": TC2, "grid": 4}),
     ("csplit", 296, 520, 2048, 0, 1, F16, F32, {"kernel": SPLITC, "csplit": 8}),
@@ -288,6 +289,25 @@ def test_simt_layouts_ragged(g, dev, tile, am, bm, M, N, K):
     full_check(g, dev, p)
 
 
+@pytest.mark.parametrize("tile", [64, 128])
+@pytest.mark.parametrize("grid", [1, 5, 37, 304])
+def test_simt_split_grid_sizes(g, dev, tile, grid):
+    """fp32 Stream-K with awkward CTA counts: ranges start and end mid-tile and
+    the last CTA to arrive adds the partials."""
+    set_opts(g, tile_n=tile, grid=grid)
+    p = problem(392, 600, 1480, 0, 1, F32, F32, True, 60 + grid)
+    pl = g.plan(392, 600, 1480, 0, 1, B.GEMM_F32, B.GEMM_F32)
+    assert pl["kernel"] == SIMT and pl["grid"] == grid
+    full_check(g, dev, p)
+
+
+@pytest.mark.parametrize("am,bm", [(0, 0), (0, 1), (1, 0), (1, 1)])
+def test_simt_split_layouts(g, dev, am, bm):
+    set_opts(g, grid=41)
+    p = problem(300, 452, 1000, am, bm, F32, F32, True, 70 + 2 * am + bm)
+    full_check(g, dev, p)
+
+
 def test_simt_unaligned_pointers(g, dev):
     p = problem(100, 68, 36, 0, 0, F32, F32, False, 111)
     A, Bt, _ = to_dev(p, dev)
@@ -332,6 +352,16 @@ def test_bitwise_repeatable(g, dev, kernel, grid):
     assert torch.equal(C1, C2)
 
 
+def test_simt_split_bitwise_repeatable(g, dev):
+    set_opts(g, grid=29)
+    p = problem(520, 776, 2056, 0, 0, F32, F32, True, 131, kind="normal")
+    A, Bt, bias = to_dev(p, dev)
+    C1 = g(A, Bt, bias, 0, 0)
+    C2 = g(A, Bt, bias, 0, 0)
+    g.status()
+    assert torch.equal(C1, C2)
+
+
 # ------------------------------------------------------ failure detection --
 def test_wait_timeout_selftest(g, dev):
     """A bounded device wait that nothing completes must expire, be reported
@@ -353,7 +383,8 @@ def test_workload_512_full(g, dev):
 
 def test_workload_sgemm2048_full(g, dev):
     p = inputs.WORKLOADS["sgemm2048_f32"].make()
-    assert g.plan(2048, 2048, 2048, 0, 0, B.GEMM_F32, B.GEMM_F32)["kernel"] == SIMT
+    pl = g.plan(2048, 2048, 2048, 0, 0, B.GEMM_F32, B.GEMM_F32)
+    assert pl["kernel"] == SIMT and pl["sk_tiles"] == 256  # split over the resident CTAs
     full_check(g, dev, p)
 
 

@@ -144,8 +144,24 @@ def test_picker_hybrid_tail():
 
 
 def test_picker_fp32_and_degenerate():
+    # 256 tiles of 128 on 2 x 152 resident CTAs: every k-block split evenly
+    # over 304 CTAs (a whole-tile launch would leave 48 SMs with one tile)
     rc, p = plan(2048, 2048, 2048, 0, 0, F32, F32)
-    assert rc == 0 and p.kernel == B.GEMM_KERNEL_SIMT and (p.tile_m, p.grid) == (128, 256)
+    assert rc == 0 and p.kernel == B.GEMM_KERNEL_SIMT and p.tile_m == 128
+    assert (p.grid, p.dp_tiles, p.sk_tiles, p.k_iters) == (304, 0, 256, 256)
+    assert p.workspace_bytes == 2 * 304 * 128 * 128 * 4 and p.group_m == 16
+    # whole waves of resident CTAs stay whole: 608 tiles, 2 waves
+    rc, p = plan(128 * 16, 128 * 38, 512, 0, 0, F32, F32)
+    assert (p.grid, p.dp_tiles, p.sk_tiles) == (608, 608, 0)
+    # 404 tiles = one wave + 100: all split over 304 CTAs
+    rc, p = plan(128 * 4, 128 * 101, 512, 0, 0, F32, F32)
+    assert (p.grid, p.dp_tiles, p.sk_tiles) == (304, 0, 404)
+    # 5 waves + 16: whole tiles
+    rc, p = plan(128 * 8, 128 * 192, 64, 0, 0, F32, F32)
+    assert (p.grid, p.dp_tiles, p.sk_tiles) == (1536, 1536, 0)
+    # shallow K: at least 8 k-blocks per split CTA -> 160 tiles x 2 k-blocks stay whole
+    rc, p = plan(128 * 10, 128 * 16, 16, 0, 0, F32, F32)
+    assert (p.grid, p.dp_tiles, p.sk_tiles) == (160, 160, 0)
     # fewer 128-tiles than SMs: 64x64 tiles spread the work over more SMs
     rc, p = plan(512, 512, 512, 0, 0, F32, F32)
     assert rc == 0 and (p.tile_m, p.grid) == (64, 64)
@@ -165,14 +181,16 @@ def test_picker_fp16_tma_stride_rule():
     assert plan(100, 64, 64, 1, 0)[0] == B.GEMM_ERR_UNSUPPORTED  # A col-major, M % 8
 
 
-PLANS = [(512, 512, 512, 0, 0), (1, 4096, 4096, 0, 0), (16, 4096, 4096, 0, 0),
-         (128, 4096, 4096, 0, 0), (128 * 157, 512, 1024, 0, 0), (1280, 5120, 1024, 0, 0),
-         (296, 520, 200, 0, 1), (1000, 1000, 4000, 1, 1), (8192, 8192, 8192, 0, 1)]
+PLANS = [(512, 512, 512, 0, 0, F16), (1, 4096, 4096, 0, 0, F16), (16, 4096, 4096, 0, 0, F16),
+         (128, 4096, 4096, 0, 0, F16), (128 * 157, 512, 1024, 0, 0, F16),
+         (1280, 5120, 1024, 0, 0, F16), (296, 520, 200, 0, 1, F16), (1000, 1000, 4000, 1, 1, F16),
+         (8192, 8192, 8192, 0, 1, F16), (2048, 2048, 2048, 0, 0, F32),
+         (128 * 4, 128 * 101, 500, 1, 1, F32), (200, 300, 500, 0, 0, F32)]
 
 
-@pytest.mark.parametrize("M,N,K,am,bm", PLANS)
-def test_work_units_match_oracle_reading(M, N, K, am, bm):
-    rc, p = plan(M, N, K, am, bm)
+@pytest.mark.parametrize("M,N,K,am,bm,idt", PLANS)
+def test_work_units_match_oracle_reading(M, N, K, am, bm, idt):
+    rc, p = plan(M, N, K, am, bm, idt, F32)
     assert rc == 0
     # the two-SM kernel hands work to CTA pairs
     units = p.grid // 2 if p.kernel == B.GEMM_KERNEL_TC2 else p.grid
@@ -184,7 +202,7 @@ def test_work_units_match_oracle_reading(M, N, K, am, bm):
         assert B.gemm_work_units(p, c) == ref[c]
     with pytest.raises(B.GemmError):
         B.gemm_work_units(p, units)
-    if p.kernel != B.GEMM_KERNEL_STREAMK:
+    if p.sk_tiles == 0 or p.kernel == B.GEMM_KERNEL_SPLITC:
         return
     # contributors of each split tile: the CTAs touching it, in k order
     owners = {}
