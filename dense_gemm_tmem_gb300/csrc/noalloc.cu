@@ -125,6 +125,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
 
   Options opt;
   opt.pair_clusters = sc.pairs;
+  opt.pair_split = 0;  // two-SM plans stay whole tiles: their split needs more than the array
   for (int s = 0; s < 9; ++s) opt.csplit_clusters[s] = sc.csplit_clusters[s];
   gemm_plan_t plan;
   rc = plan_for(M, N, K, layout, sc.num_sms, opt, &plan);

@@ -15,9 +15,11 @@
 //   - tcgen05.commit with a two-CTA multicast frees the stage in both CTAs and
 //     hands both accumulators to their epilogues; each epilogue warp reports a
 //     drained accumulator to the leader with a remote mbarrier arrive.
-// Whole tiles only (persistent over clusters, grouped raster); the Stream-K
-// split stays on the one-SM kernel, which the picker uses for small shapes.
-// Every wait is bounded as in the one-SM kernel.
+// Persistent over clusters with a grouped raster.  Tiles are whole, except
+// for an optional Stream-K region (work.cuh, counted in pair tiles and pairs):
+// each CTA of a pair publishes its 128-row half of a partial tile, and per
+// half the last pair to arrive adds the halves in ascending k order, so no CTA
+// ever waits for another pair.  Every wait is bounded as in the one-SM kernel.
 #pragma once
 
 #include "tc_kernel.cuh"
@@ -229,12 +231,101 @@ __device__ __forceinline__ void tc2_mma(const TcArgs& args, uint8_t* sA, uint8_t
   }
 }
 
+// Split unit: this CTA's 128-row half of a partial tile.  The half goes to
+// workspace slot 2 * split_slot(pair, tile) + rank (128 x 256 fp32, stored
+// thread-contiguous per 32-column chunk); the half's arrival counter is
+// tickets[2 * tile + rank].  The last of the contributing pairs to arrive adds
+// all halves in ascending pair (= k) order, its own from TMEM in place, and
+// stores the result: the sum is the same whichever pair arrives last.
+template <bool OUT_F16>
+__device__ __forceinline__ void tc2_split_half(const TcArgs& args, uint32_t taddr, int row,
+                                               int32_t mm, int32_t nbase, const Unit& u,
+                                               uint32_t rank, int32_t cluster_id,
+                                               volatile int* last_flag) {
+  const WorkSpec& W = args.work;
+  constexpr int CW = 32;
+  const int32_t st = u.tile - W.dp_tiles;
+  const size_t half_elems = size_t(kBM) * kPairBN;
+  auto half_of = [&](int32_t pair) {
+    return args.workspace + (size_t(split_slot(W, pair, st)) * 2 + rank) * half_elems;
+  };
+  float* mine = half_of(cluster_id);
+#pragma unroll 1
+  for (int c = 0; c < kPairBN / CW; ++c) {
+    float v[CW];
+    __syncwarp();
+    tmem_load_chunk<CW>(taddr + c * CW, v);
+    float4* dst = reinterpret_cast<float4*>(mine + (size_t(c) * kBM + row) * CW);
+#pragma unroll
+    for (int j = 0; j < CW / 4; ++j)
+      __stcg(dst + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+  }
+  __threadfence();
+  epi_bar_sync();
+  int32_t first, last;
+  split_contributors(W, st, first, last);
+  int* ticket = args.tickets + 2 * st + int32_t(rank);
+  if (threadIdx.x == 64) {
+    const int old = atomicAdd(ticket, 1);
+    *last_flag = (old == last - first) ? 1 : 0;
+  }
+  epi_bar_sync();
+  if (!*last_flag) return;
+  __threadfence();
+  constexpr int kFixBatch = 2;  // contributors whose loads are in flight together
+#pragma unroll 1
+  for (int c = 0; c < kPairBN / CW; ++c) {
+    float own[CW], acc[CW];
+    __syncwarp();
+    tmem_load_chunk<CW>(taddr + c * CW, own);
+#pragma unroll 1
+    for (int32_t r0 = first; r0 <= last; r0 += kFixBatch) {
+      float4 part[kFixBatch][CW / 4];
+#pragma unroll
+      for (int bb = 0; bb < kFixBatch; ++bb) {
+        const int32_t r = r0 + bb;
+        if (r <= last && r != cluster_id) {
+          const float4* src =
+              reinterpret_cast<const float4*>(half_of(r) + (size_t(c) * kBM + row) * CW);
+#pragma unroll
+          for (int j = 0; j < CW / 4; ++j) part[bb][j] = __ldcg(src + j);
+        }
+      }
+#pragma unroll
+      for (int bb = 0; bb < kFixBatch; ++bb) {
+        const int32_t r = r0 + bb;
+        if (r > last) break;
+        float v[CW];
+        if (r == cluster_id) {
+#pragma unroll
+          for (int j = 0; j < CW; ++j) v[j] = own[j];
+        } else {
+#pragma unroll
+          for (int j = 0; j < CW / 4; ++j) {
+            v[4 * j] = part[bb][j].x; v[4 * j + 1] = part[bb][j].y;
+            v[4 * j + 2] = part[bb][j].z; v[4 * j + 3] = part[bb][j].w;
+          }
+        }
+        if (r == first) {
+#pragma unroll
+          for (int j = 0; j < CW; ++j) acc[j] = v[j];
+        } else {
+#pragma unroll
+          for (int j = 0; j < CW; ++j) acc[j] += v[j];
+        }
+      }
+    }
+    store_chunk<CW, OUT_F16, false>(args, mm, nbase + c * CW, acc);
+  }
+  if (threadIdx.x == 64) atomicExch(ticket, 0);  // ready for the next launch
+}
+
 // Epilogue (warps 2-5 of each CTA): this CTA's 128 rows of the 256 x 256 tile.
 template <bool OUT_F16>
 __device__ __forceinline__ void tc2_epilogue(const TcArgs& args, uint64_t* acc_full,
                                              uint64_t* acc_empty, const WaitCtl& wc,
                                              uint32_t tmem_base, uint32_t rank,
-                                             int32_t cluster_id) {
+                                             int32_t cluster_id, volatile int* last_flag) {
   const WorkSpec& W = args.work;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -259,12 +350,16 @@ __device__ __forceinline__ void tc2_epilogue(const TcArgs& args, uint64_t* acc_f
     const int32_t mm = tm * kPairBM + int32_t(rank) * kBM + row;
     const int32_t nbase = tn * kPairBN;
     const uint32_t taddr = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(b * kPairBN);
+    if (!unit_is_partial(W, u)) {
 #pragma unroll 1
-    for (int c = 0; c < kPairBN / 32; ++c) {
-      float v[32];
-      __syncwarp();
-      tmem_load_chunk<32>(taddr + c * 32, v);
-      store_chunk<32, OUT_F16, false>(args, mm, nbase + c * 32, v);
+      for (int c = 0; c < kPairBN / 32; ++c) {
+        float v[32];
+        __syncwarp();
+        tmem_load_chunk<32>(taddr + c * 32, v);
+        store_chunk<32, OUT_F16, false>(args, mm, nbase + c * 32, v);
+      }
+    } else {
+      tc2_split_half<OUT_F16>(args, taddr, row, mm, nbase, u, rank, cluster_id, last_flag);
     }
     tc_fence_before();
     __syncwarp();
@@ -301,6 +396,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -318,6 +414,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
+    *last_flag = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -345,7 +442,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
       tc2_mma<S>(args, sA, sB, full, empty, acc_full, acc_empty, drain, wc, tmem_base,
                  cluster_id);
   } else {
-    tc2_epilogue<OUT_F16>(args, acc_full, acc_empty, wc, tmem_base, rank, cluster_id);
+    tc2_epilogue<OUT_F16>(args, acc_full, acc_empty, wc, tmem_base, rank, cluster_id,
+                          last_flag);
   }
 
   __syncthreads();

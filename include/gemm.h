@@ -66,8 +66,10 @@ enum {
   GEMM_KERNEL_SIMT = 2,     /* CUDA-core fp32 GEMM */
   GEMM_KERNEL_FILL = 3,     /* K == 0: C = bias (or 0) */
   GEMM_KERNEL_NONE = 4,     /* M == 0 or N == 0: nothing to do */
-  GEMM_KERNEL_TC2 = 5,      /* two-SM tcgen05 GEMM (CTA pairs, cta_group::2), whole
-                               256 x 256 tiles; tile_m = tile_n = 256, grid = 2 x pairs */
+  GEMM_KERNEL_TC2 = 5,      /* two-SM tcgen05 GEMM (CTA pairs, cta_group::2), 256 x 256
+                               tiles, whole or with a Stream-K tail; tile_m = tile_n = 256,
+                               grid = 2 x pairs; dp_tiles, sk_tiles and the work units
+                               count pair tiles and pairs */
   GEMM_KERNEL_SPLITC = 6    /* one-SM tcgen05 GEMM with each tile's k-blocks split over a
                                cluster of cluster_split CTAs, whose fp32 partials are added
                                in distributed shared memory (no global workspace) */
@@ -110,9 +112,13 @@ enum {
                                     (not swapped), -1 the picker's rule */
   GEMM_OPT_CLUSTER_SPLIT = 8,    /* cluster split: 0 never (Stream-K instead), 2/4/8 CTAs
                                     per tile when a split is chosen, -1 the picker's rule */
-  GEMM_OPT_PDL = 9               /* 1 (default): tensor-core kernels are launched so their
+  GEMM_OPT_PDL = 9,              /* 1 (default): tensor-core kernels are launched so their
                                     prologue may overlap the previous kernel on the stream;
                                     they touch global memory only after it completed. 0: off */
+  GEMM_OPT_PAIR_SPLIT = 10       /* two-SM kernel: -1 (default) or 0 whole tiles only;
+                                    1 every tile's k-blocks split evenly over the pairs
+                                    (Stream-K); 2 the part-empty last wave of pair tiles and
+                                    the wave before it split evenly over the pairs */
 };
 
 /* Creates a handle on CUDA device `device`.  Allocates, on that device, the

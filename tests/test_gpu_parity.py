@@ -121,6 +121,36 @@ def test_pair_grid_sizes(g, dev, grid):
     full_check(g, dev, p)
 
 
+@pytest.mark.parametrize("grid", [2, 10, 38, 152])
+def test_pair_split_grid_sizes(g, dev, grid):
+    """Two-SM Stream-K: every pair tile's k-blocks split over grid / 2 pairs;
+    ranges start and end mid-tile and each CTA half is added by the last pair
+    to arrive."""
+    set_opts(g, kernel=TC2, pair_split=1, grid=grid)
+    p = problem(520, 776, 2056, 0, 1, F16, F32, True, 90 + grid)
+    pl = g.plan(520, 776, 2056, 0, 1)
+    assert pl["kernel"] == TC2 and (pl["dp_tiles"], pl["sk_tiles"]) == (0, 12)
+    full_check(g, dev, p)
+
+
+@pytest.mark.parametrize("am,bm", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("odt", [F16, F32])
+def test_pair_split_layouts(g, dev, am, bm, odt):
+    set_opts(g, kernel=TC2, pair_split=1, grid=22)
+    p = problem(296, 520, 2048, am, bm, F16, odt, True, 150 + 4 * am + 2 * bm + (odt == F32))
+    full_check(g, dev, p)
+
+
+def test_pair_tail_split(g, dev):
+    """Whole pair tiles first, then the last two waves split: 20 pair tiles on
+    6 pairs -> 12 whole, 8 split."""
+    set_opts(g, kernel=TC2, pair_split=2, grid=12)
+    pl = g.plan(1000, 1200, 1000, 0, 1, B.GEMM_F16, B.GEMM_F16)
+    assert (pl["dp_tiles"], pl["sk_tiles"], pl["grid"]) == (12, 8, 12)
+    p = problem(1000, 1200, 1000, 0, 1, F16, F16, True, 95)
+    full_check(g, dev, p)
+
+
 @pytest.mark.parametrize("csplit", [2, 4, 8])
 @pytest.mark.parametrize("am,bm", [(0, 0), (0, 1), (1, 0), (1, 1)])
 @pytest.mark.parametrize("odt", [F16, F32])
@@ -194,6 +224,7 @@ def test_permutation_columns_exact(g, dev, kernel):
     ("simt_split", 300, 420, 1000, 1, 0, F32, F32, {"grid": 23}),
     ("pair", 520, 776, 1032, 0, 1, F16, F32, {"kernel": TC2}),
     ("pair16", 296, 520, 2048, 1, 0, F16, F16, {"kernel": TC2, "grid": 4}),
+    ("pair_split", 520, 776, 1032, 0, 1, F16, F32, {"kernel": TC2, "pair_split": 1, "grid": 14}),
     ("csplit", 296, 520, 2048, 0, 1, F16, F32, {"kernel": SPLITC, "csplit": 8}),
     ("csplit_swap", 16, 2048, 4096, 0, 0, F16, F16, {"kernel": SPLITC, "csplit": 4}),
 ])
@@ -345,6 +376,16 @@ def test_side_stream(g, dev):
 def test_bitwise_repeatable(g, dev, kernel, grid):
     set_opts(g, kernel=kernel, grid=grid)
     p = problem(520, 776, 2056, 0, 1, F16, F32, True, 130, kind="normal")
+    A, Bt, bias = to_dev(p, dev)
+    C1 = g(A, Bt, bias, 0, 1)
+    C2 = g(A, Bt, bias, 0, 1)
+    g.status()
+    assert torch.equal(C1, C2)
+
+
+def test_pair_split_bitwise_repeatable(g, dev):
+    set_opts(g, kernel=TC2, pair_split=1, grid=14)
+    p = problem(520, 776, 2056, 0, 1, F16, F32, True, 132, kind="normal")
     A, Bt, bias = to_dev(p, dev)
     C1 = g(A, Bt, bias, 0, 1)
     C2 = g(A, Bt, bias, 0, 1)

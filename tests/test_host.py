@@ -71,17 +71,18 @@ def plan(M, N, K, am=0, bm=0, idt=F16, odt=F32, sms=SMS):
 
 
 def test_picker_large_square_two_sm_tiles():
-    """Large shapes run on CTA pairs: 256 x 256 tiles, whole waves of 76 pairs."""
+    """Large shapes run on CTA pairs: 256 x 256 whole tiles on 76 pairs (8192^3:
+    1024 pair tiles = 13 waves + 36; a Stream-K tail measured slower)."""
     rc, p = plan(8192, 8192, 8192, 0, 1, F16, F16)
     assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC2
     assert (p.tile_m, p.tile_n, p.tile_k, p.stages) == (256, 256, 64, 6)
     assert (p.tiles_m, p.tiles_n, p.k_iters) == (32, 32, 128)
-    assert (p.dp_tiles, p.sk_tiles, p.grid) == (1024, 0, SMS)
+    assert (p.dp_tiles, p.sk_tiles, p.grid, p.workspace_bytes) == (1024, 0, SMS, 0)
     assert (p.swap_ab, p.a_mn_major, p.b_mn_major) == (0, 0, 0)
     assert p.group_m == 8  # raster groups of 2048 rows of A (8 pair tiles)
     rc, p = plan(16384, 16384, 16384, 0, 0, F16, F16)
     assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC2 and p.b_mn_major == 1
-    assert p.dp_tiles == 64 * 64 and p.workspace_bytes == 0
+    assert p.dp_tiles == 64 * 64 and p.sk_tiles == 0 and p.workspace_bytes == 0
 
 
 def test_picker_pair_rule_falls_back():
