@@ -37,7 +37,9 @@ struct Tc2Config {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 512;  // two 256-column accumulators
   static constexpr int kBarBytes = 256;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+  static constexpr int kEpiStageBytes = 4 * 32 * (32 + 4) * 4;  // store staging, 4 warps
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes + kEpiStageBytes;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static_assert((2 * kStages + 5) * 8 + 16 <= kBarBytes, "barrier area");
 };
 
@@ -232,14 +234,15 @@ __device__ __forceinline__ void tc2_mma(const TcArgs& args, uint8_t* sA, uint8_t
 }
 
 // Split unit: this CTA's 128-row half of a partial tile.  The half goes to
-// workspace slot 2 * split_slot(pair, tile) + rank (128 x 256 fp32, stored
-// thread-contiguous per 32-column chunk); the half's arrival counter is
+// workspace slot 2 * split_slot(pair, tile) + rank (128 x 256 fp32; float4 j of
+// a row's 32-column chunk c at float4 index (c * 8 + j) * 128 + row, so each
+// warp's accesses are contiguous); the half's arrival counter is
 // tickets[2 * tile + rank].  The last of the contributing pairs to arrive adds
 // all halves in ascending pair (= k) order, its own from TMEM in place, and
 // stores the result: the sum is the same whichever pair arrives last.
 template <bool OUT_F16>
-__device__ __forceinline__ void tc2_split_half(const TcArgs& args, uint32_t taddr, int row,
-                                               int32_t mm, int32_t nbase, const Unit& u,
+__device__ __forceinline__ void tc2_split_half(const TcArgs& args, float* sw, uint32_t taddr,
+                                               int row, int32_t mm, int32_t nbase, const Unit& u,
                                                uint32_t rank, int32_t cluster_id,
                                                volatile int* last_flag) {
   const WorkSpec& W = args.work;
@@ -255,10 +258,10 @@ __device__ __forceinline__ void tc2_split_half(const TcArgs& args, uint32_t tadd
     float v[CW];
     __syncwarp();
     tmem_load_chunk<CW>(taddr + c * CW, v);
-    float4* dst = reinterpret_cast<float4*>(mine + (size_t(c) * kBM + row) * CW);
+    float4* dst = reinterpret_cast<float4*>(mine) + size_t(c) * (CW / 4) * kBM + row;
 #pragma unroll
     for (int j = 0; j < CW / 4; ++j)
-      __stcg(dst + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+      __stcg(dst + j * kBM, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
   }
   __threadfence();
   epi_bar_sync();
@@ -286,9 +289,9 @@ __device__ __forceinline__ void tc2_split_half(const TcArgs& args, uint32_t tadd
         const int32_t r = r0 + bb;
         if (r <= last && r != cluster_id) {
           const float4* src =
-              reinterpret_cast<const float4*>(half_of(r) + (size_t(c) * kBM + row) * CW);
+              reinterpret_cast<const float4*>(half_of(r)) + size_t(c) * (CW / 4) * kBM + row;
 #pragma unroll
-          for (int j = 0; j < CW / 4; ++j) part[bb][j] = __ldcg(src + j);
+          for (int j = 0; j < CW / 4; ++j) part[bb][j] = __ldcg(src + j * kBM);
         }
       }
 #pragma unroll
@@ -315,7 +318,7 @@ __device__ __forceinline__ void tc2_split_half(const TcArgs& args, uint32_t tadd
         }
       }
     }
-    store_chunk<CW, OUT_F16, false>(args, mm, nbase + c * CW, acc);
+    store_rows_staged<CW, OUT_F16>(args, sw, mm - (row & 31), row & 31, nbase + c * CW, acc);
   }
   if (threadIdx.x == 64) atomicExch(ticket, 0);  // ready for the next launch
 }
@@ -325,12 +328,14 @@ template <bool OUT_F16>
 __device__ __forceinline__ void tc2_epilogue(const TcArgs& args, uint64_t* acc_full,
                                              uint64_t* acc_empty, const WaitCtl& wc,
                                              uint32_t tmem_base, uint32_t rank,
-                                             int32_t cluster_id, volatile int* last_flag) {
+                                             int32_t cluster_id, volatile int* last_flag,
+                                             float* stage) {
   const WorkSpec& W = args.work;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int q = warp & 3;  // TMEM lane quarter this warp may access
   const int row = q * 32 + lane;
+  float* sw = stage + q * 32 * (32 + 4);  // this warp's store staging block
   const uint32_t leader_empty0 = map_to_rank(smem_u32(&acc_empty[0]), 0);
   const uint32_t leader_empty1 = map_to_rank(smem_u32(&acc_empty[1]), 0);
   WorkIter it;
@@ -356,10 +361,10 @@ __device__ __forceinline__ void tc2_epilogue(const TcArgs& args, uint64_t* acc_f
         float v[32];
         __syncwarp();
         tmem_load_chunk<32>(taddr + c * 32, v);
-        store_chunk<32, OUT_F16, false>(args, mm, nbase + c * 32, v);
+        store_rows_staged<32, OUT_F16>(args, sw, mm - lane, lane, nbase + c * 32, v);
       }
     } else {
-      tc2_split_half<OUT_F16>(args, taddr, row, mm, nbase, u, rank, cluster_id, last_flag);
+      tc2_split_half<OUT_F16>(args, sw, taddr, row, mm, nbase, u, rank, cluster_id, last_flag);
     }
     tc_fence_before();
     __syncwarp();
@@ -443,7 +448,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
                  cluster_id);
   } else {
     tc2_epilogue<OUT_F16>(args, acc_full, acc_empty, wc, tmem_base, rank, cluster_id,
-                          last_flag);
+                          last_flag,
+                          reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) +
+                                                   Cfg::kBarBytes));
   }
 
   __syncthreads();

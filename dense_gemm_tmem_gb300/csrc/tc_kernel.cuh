@@ -53,7 +53,10 @@ struct TcConfig {
   static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;  // power of two >= 32
   static constexpr int kChunk = BN < 32 ? BN : 32;             // TMEM columns per load
   static constexpr int kBarBytes = 256;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+  // epilogue staging: per epilogue warp 32 rows of kChunk + 4 floats
+  static constexpr int kEpiStageBytes = 4 * 32 * (kChunk + 4) * 4;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes + kEpiStageBytes;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128");
   static_assert((2 * kStages + 5) * 8 + 16 <= kBarBytes, "barrier area");
 };
@@ -246,6 +249,57 @@ __device__ __forceinline__ void put4(const TcArgs& a, int64_t off, float4 v, int
 #pragma unroll
   for (int j = 0; j < 4; ++j)
     if (j < valid) put_elem<OUT_F16>(a, off + j, f[j]);
+}
+
+// Row-major store of one epilogue warp's 32 rows x CW columns (lane i holds row
+// mrow0 + i in v).  Written straight out, each store instruction would touch 32
+// rows with 16 bytes each; instead the rows go through the warp's staging block
+// sw (rows of CW + 4 floats: conflict-free 16-byte accesses) and come back out
+// as runs of CW consecutive columns, 32 / (CW / 4) rows per instruction.  The
+// bias is added in fp32 before the single rounding, as in every other store.
+template <int CW, bool OUT_F16>
+__device__ __forceinline__ void store_rows_staged(const TcArgs& a, float* sw, int32_t mrow0,
+                                                  int lane, int32_t nn0, const float (&v)[CW]) {
+  if (mrow0 >= a.Mm || nn0 >= a.Nm) return;  // the same for the whole warp
+  constexpr int LD = CW + 4;
+  constexpr int Q = CW / 4;    // float4 per row
+  constexpr int RPI = 32 / Q;  // rows per pass
+  __syncwarp();                // the previous chunk's reads of sw are done
+  float4* mine = reinterpret_cast<float4*>(sw + lane * LD);
+#pragma unroll
+  for (int j = 0; j < Q; ++j)
+    mine[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+  __syncwarp();
+  const int c4 = lane % Q;
+  const int32_t nn = nn0 + 4 * c4;
+  const int valid = min(4, a.Nm - nn);
+  float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (a.bias && valid > 0) {
+    b4.x = __ldg(a.bias + nn);
+    if (valid > 1) b4.y = __ldg(a.bias + nn + 1);
+    if (valid > 2) b4.z = __ldg(a.bias + nn + 2);
+    if (valid > 3) b4.w = __ldg(a.bias + nn + 3);
+  }
+#pragma unroll
+  for (int it = 0; it < 32 / RPI; ++it) {
+    const int r = it * RPI + lane / Q;
+    const int32_t mm = mrow0 + r;
+    if (mm >= a.Mm || valid <= 0) continue;
+    float4 x = *reinterpret_cast<const float4*>(sw + r * LD + 4 * c4);
+    x.x += b4.x; x.y += b4.y; x.z += b4.z; x.w += b4.w;
+    put4<OUT_F16>(a, int64_t(mm) * a.ldc + nn, x, valid);
+  }
+}
+
+// Any store of an epilogue chunk: transposed stores are already coalesced
+// (lanes are consecutive columns of C); row-major ones go through staging.
+template <int CW, bool OUT_F16, bool TRANS>
+__device__ __forceinline__ void store_out(const TcArgs& a, float* sw, int32_t mm, int lane,
+                                          int32_t nn0, const float (&v)[CW]) {
+  if constexpr (TRANS)
+    store_chunk<CW, OUT_F16, TRANS>(a, mm, nn0, v);
+  else
+    store_rows_staged<CW, OUT_F16>(a, sw, mm - lane, lane, nn0, v);
 }
 
 // Cluster split: after every CTA of the cluster parked its fp32 partial of the
@@ -505,6 +559,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;     // accumulator row inside the tile
     const int et = threadIdx.x - 64;   // 0..127
+    // this warp's store staging block (after the barrier area)
+    float* sw = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + Cfg::kBarBytes) +
+                q * 32 * (CW + 4);
     WorkIter it;
     it.init(W, blockIdx.x);
     Unit u;
@@ -551,23 +608,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           float v[CW];
           __syncwarp();
           tmem_load_chunk<CW>(taddr + c * CW, v);
-          store_chunk<CW, OUT_F16, TRANS>(args, mm, nbase + c * CW, v);
+          store_out<CW, OUT_F16, TRANS>(args, sw, mm, lane, nbase + c * CW, v);
         }
       } else {
         const int32_t st = u.tile - W.dp_tiles;  // split-tile index
         const int32_t me = blockIdx.x;
         const size_t slot_elems = size_t(kBM) * BN;
         float* mine = args.workspace + size_t(split_slot(W, me, st)) * slot_elems;
-        // publish this CTA's fp32 partial (thread-contiguous: 128 B per thread per chunk)
+        // publish this CTA's fp32 partial: float4 j of a row's chunk c at float4
+        // index (c * CW/4 + j) * 128 + row, so a warp's stores are contiguous
 #pragma unroll 1
         for (int c = 0; c < BN / CW; ++c) {
           float v[CW];
           __syncwarp();
           tmem_load_chunk<CW>(taddr + c * CW, v);
-          float4* dst = reinterpret_cast<float4*>(mine + (size_t(c) * kBM + row) * CW);
+          float4* dst = reinterpret_cast<float4*>(mine) + size_t(c) * (CW / 4) * kBM + row;
 #pragma unroll
           for (int j = 0; j < CW / 4; ++j)
-            __stcg(dst + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+            __stcg(dst + j * kBM,
+                   make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
         }
         __threadfence();
         epi_bar_sync();
@@ -596,11 +655,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               for (int b = 0; b < kFixBatch; ++b) {
                 const int32_t r = r0 + b;
                 if (r <= last && r != me) {
-                  const float4* src = reinterpret_cast<const float4*>(
-                      args.workspace + size_t(split_slot(W, r, st)) * slot_elems +
-                      (size_t(c) * kBM + row) * CW);
+                  const float4* src =
+                      reinterpret_cast<const float4*>(args.workspace +
+                                                      size_t(split_slot(W, r, st)) * slot_elems) +
+                      size_t(c) * (CW / 4) * kBM + row;
 #pragma unroll
-                  for (int j = 0; j < CW / 4; ++j) part[b][j] = __ldcg(src + j);
+                  for (int j = 0; j < CW / 4; ++j) part[b][j] = __ldcg(src + j * kBM);
                 }
               }
 #pragma unroll
@@ -627,7 +687,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
               }
             }
-            store_chunk<CW, OUT_F16, TRANS>(args, mm, nbase + c * CW, acc);
+            store_out<CW, OUT_F16, TRANS>(args, sw, mm, lane, nbase + c * CW, acc);
           }
           if (et == 0) atomicExch(&args.tickets[st], 0);  // ready for the next launch
         }
