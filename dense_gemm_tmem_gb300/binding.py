@@ -196,3 +196,6 @@ def gemm_set_trace(h, dev_buf_ptr, ctas: int) -> int:
 
 
 TRACE_PHASES = ("start", "first_load", "first_data", "mma_done", "last_accum", "end")
+TRACE_SLOTS = 12  # per CTA: the phases above, units, cluster done, entry, exit, cluster steps
+TRACE_UNITS, TRACE_CLUSTER_DONE, TRACE_ENTRY, TRACE_EXIT = 6, 7, 8, 9
+TRACE_CLUSTER_PARKED, TRACE_CLUSTER_REDUCED = 10, 11

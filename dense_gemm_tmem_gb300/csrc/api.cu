@@ -52,11 +52,85 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 }  // namespace
 
 // ------------------------------------------------------------ tile picker --
+// The CUDA-core kernel's plan (fp32 inputs, and fp16 inputs the tensor-core
+// path cannot read).
+int plan_simt(int64_t M, int64_t N, int64_t K, int num_sms, const Options& o, gemm_plan_t* p) {
+  // 128x128 tiles (256 threads, 2 CTAs per SM).  Only when those tiles
+  // cannot give every SM one, 64x64 tiles (64 threads) spread the work wider;
+  // measured on 2048^3 the smaller CTAs lose more to per-FMA overhead (FMA
+  // pipe 52 % vs 64 % busy) than they win back in balance.
+  int tile;
+  if (o.force_tile_n > 0) {
+    if (o.force_tile_n != kSimtBM && o.force_tile_n != kSimtSmallTile)
+      return GEMM_ERR_UNSUPPORTED;
+    tile = o.force_tile_n;
+  } else {
+    const int64_t big = ceil_div(M, kSimtBM) * ceil_div(N, kSimtBN);
+    tile = big >= num_sms ? kSimtBM : kSimtSmallTile;
+  }
+  const int64_t tiles_m = ceil_div(M, tile), tiles_n = ceil_div(N, tile);
+  const int64_t T = tiles_m * tiles_n;
+  const int64_t I = ceil_div(K, kSimtBK);
+  if (T > INT32_MAX / 2 || I > INT32_MAX / 2 || T * I > (int64_t(1) << 40))
+    return GEMM_ERR_UNSUPPORTED;
+  // Resident CTAs (the split's grid), capped so two partial slots per CTA
+  // fit the handle's workspace.
+  const int64_t per_sm = o.simt_per_sm > 0 ? std::min(o.simt_per_sm, 2) : 2;
+  const int64_t S = per_sm * num_sms;
+  int64_t dp = T, sk = 0, grid = T;
+  if (o.force_grid > 0) {
+    // forced grid: every tile's k-blocks split over that many CTAs
+    dp = 0;
+    sk = T;
+    grid = std::min<int64_t>({o.force_grid, S, T * I});
+    if (grid == T) {
+      dp = T;
+      sk = 0;
+    }
+  } else if (tile == kSimtBM && T >= S) {
+    // the tensor-core rule over resident CTAs: whole waves stay whole; a
+    // part-empty last wave is merged with the wave before it and split
+    const int64_t full = T / S, rem = T % S;
+    if (rem != 0 && full < 4) {
+      dp = (full - 1) * S;
+      sk = T - dp;
+      grid = S;
+    }
+  } else if (tile == kSimtBM) {
+    // fewer tiles than resident CTAs: split all k-blocks over up to S CTAs
+    const int min_iters = o.min_split_iters > 0 ? o.min_split_iters : kSimtMinSplitIters;
+    grid = std::min(S, std::max<int64_t>(T, T * I / min_iters));
+    if (grid > T) {
+      dp = 0;
+      sk = T;
+    } else {
+      grid = T;
+    }
+  }
+  if (sk > kTicketCap) return GEMM_ERR_UNSUPPORTED;
+  p->kernel = GEMM_KERNEL_SIMT;
+  p->tile_m = tile;
+  p->tile_n = tile;
+  p->tile_k = kSimtBK;
+  p->stages = 2;
+  p->tiles_m = int32_t(tiles_m);
+  p->tiles_n = int32_t(tiles_n);
+  p->grid = int32_t(grid);
+  p->k_iters = int32_t(I);
+  p->dp_tiles = int32_t(dp);
+  p->sk_tiles = int32_t(sk);
+  p->group_m = o.group_m > 0 ? o.group_m : 2048 / tile;
+  p->workspace_bytes = sk > 0 ? int64_t(2) * grid * tile * tile * 4 : 0;
+  return GEMM_OK;
+}
+
 // Chooses kernel, tile, split and grid for a shape.  Rules:
 //  * fp32 inputs -> CUDA-core kernel, 128x128 tiles (64x64 when there are
 //    fewer 128-tiles than SMs).  With 128-tiles the tiles-vs-waves rule below
 //    is applied over the resident CTAs (2 per SM), and a split hands out the
 //    k-blocks in runs of at least 8.
+//  * fp16 inputs whose leading dimensions (or, in gemm_run, base addresses)
+//    break the TMA rules -> the same CUDA-core kernel, fp16 widened to fp32.
 //  * fp16 inputs -> tcgen05 kernels.  Large shapes whose 256x256 tiles fill
 //    whole waves of CTA pairs -> the two-SM kernel.  Skinny M (M <= 128,
 //    N >= 2M, A row-major) swaps the operands so N fills the 128-row MMA side
@@ -90,80 +164,18 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
   }
   if (L.in_dtype == GEMM_F32) {
     if (o.force_kernel >= 0 && o.force_kernel != GEMM_KERNEL_SIMT) return GEMM_ERR_UNSUPPORTED;
-    // 128x128 tiles (256 threads, 2 CTAs per SM).  Only when those tiles
-    // cannot give every SM one, 64x64 tiles (64 threads) spread the work wider;
-    // measured on 2048^3 the smaller CTAs lose more to per-FMA overhead (FMA
-    // pipe 52 % vs 64 % busy) than they win back in balance.
-    int tile;
-    if (o.force_tile_n > 0) {
-      if (o.force_tile_n != kSimtBM && o.force_tile_n != kSimtSmallTile)
-        return GEMM_ERR_UNSUPPORTED;
-      tile = o.force_tile_n;
-    } else {
-      const int64_t big = ceil_div(M, kSimtBM) * ceil_div(N, kSimtBN);
-      tile = big >= num_sms ? kSimtBM : kSimtSmallTile;
-    }
-    const int64_t tiles_m = ceil_div(M, tile), tiles_n = ceil_div(N, tile);
-    const int64_t T = tiles_m * tiles_n;
-    const int64_t I = ceil_div(K, kSimtBK);
-    if (T > INT32_MAX / 2 || I > INT32_MAX / 2 || T * I > (int64_t(1) << 40))
-      return GEMM_ERR_UNSUPPORTED;
-    // Resident CTAs (the split's grid), capped so two partial slots per CTA
-    // fit the handle's workspace.
-    const int64_t per_sm = o.simt_per_sm > 0 ? std::min(o.simt_per_sm, 2) : 2;
-    const int64_t S = per_sm * num_sms;
-    int64_t dp = T, sk = 0, grid = T;
-    if (o.force_grid > 0) {
-      // forced grid: every tile's k-blocks split over that many CTAs
-      dp = 0;
-      sk = T;
-      grid = std::min<int64_t>({o.force_grid, S, T * I});
-      if (grid == T) {
-        dp = T;
-        sk = 0;
-      }
-    } else if (tile == kSimtBM && T >= S) {
-      // the tensor-core rule over resident CTAs: whole waves stay whole; a
-      // part-empty last wave is merged with the wave before it and split
-      const int64_t full = T / S, rem = T % S;
-      if (rem != 0 && full < 4) {
-        dp = (full - 1) * S;
-        sk = T - dp;
-        grid = S;
-      }
-    } else if (tile == kSimtBM) {
-      // fewer tiles than resident CTAs: split all k-blocks over up to S CTAs
-      const int min_iters = o.min_split_iters > 0 ? o.min_split_iters : kSimtMinSplitIters;
-      grid = std::min(S, std::max<int64_t>(T, T * I / min_iters));
-      if (grid > T) {
-        dp = 0;
-        sk = T;
-      } else {
-        grid = T;
-      }
-    }
-    if (sk > kTicketCap) return GEMM_ERR_UNSUPPORTED;
-    p->kernel = GEMM_KERNEL_SIMT;
-    p->tile_m = tile;
-    p->tile_n = tile;
-    p->tile_k = kSimtBK;
-    p->stages = 2;
-    p->tiles_m = int32_t(tiles_m);
-    p->tiles_n = int32_t(tiles_n);
-    p->grid = int32_t(grid);
-    p->k_iters = int32_t(I);
-    p->dp_tiles = int32_t(dp);
-    p->sk_tiles = int32_t(sk);
-    p->group_m = o.group_m > 0 ? o.group_m : 2048 / tile;
-    p->workspace_bytes = sk > 0 ? int64_t(2) * grid * tile * tile * 4 : 0;
-    return GEMM_OK;
+    return plan_simt(M, N, K, num_sms, o, p);
   }
-  // fp16: tensor-core path.
-  if (o.force_kernel == GEMM_KERNEL_SIMT) return GEMM_ERR_UNSUPPORTED;
-  if (M > kMaxCoord || N > kMaxCoord || K > kMaxCoord) return GEMM_ERR_UNSUPPORTED;
+  // fp16: tensor-core path, unless asked for the CUDA-core kernel or the TMA
+  // rules rule it out (int32 coordinates; leading dimensions a multiple of 8
+  // elements, i.e. 16-byte row strides).
   const int64_t lda = L.a_major == GEMM_ROW_MAJOR ? K : M;
   const int64_t ldb = L.b_major == GEMM_ROW_MAJOR ? N : K;
-  if (lda % 8 != 0 || ldb % 8 != 0) return GEMM_ERR_UNSUPPORTED;  // TMA stride rule
+  if (o.force_kernel == GEMM_KERNEL_SIMT || M > kMaxCoord || N > kMaxCoord || K > kMaxCoord ||
+      lda % 8 != 0 || ldb % 8 != 0) {
+    if (o.force_kernel >= 0 && o.force_kernel != GEMM_KERNEL_SIMT) return GEMM_ERR_UNSUPPORTED;
+    return plan_simt(M, N, K, num_sms, o, p);
+  }
 
   const bool forced_pair = o.force_kernel == GEMM_KERNEL_TC2;
   const bool swap = o.force_swap >= 0 ? (o.force_swap != 0)
@@ -716,13 +728,25 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, co
   }
   if (!A || !B) return GEMM_ERR_INVALID_ARG;
 
+  // fp16 operands the TMA cannot read (base not 16-byte aligned): the
+  // CUDA-core kernel instead
+  if (plan.kernel != GEMM_KERNEL_SIMT &&
+      ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15))) {
+    dg::Options o = h->opt;
+    o.force_kernel = GEMM_KERNEL_SIMT;
+    o.force_tile_n = -1;
+    rc = dg::plan_for(M, N, K, layout, h->num_sms, o, &plan);
+    if (rc != GEMM_OK) return rc;
+  }
   if (plan.kernel == GEMM_KERNEL_SIMT) {
     dg::SimtLaunch L;
     L.M = M; L.N = N; L.K = K;
-    L.A = static_cast<const float*>(A);
-    L.B = static_cast<const float*>(B);
+    L.A = A;
+    L.B = B;
     L.bias = bias;
-    L.C = static_cast<float*>(C);
+    L.C = C;
+    L.in_f16 = layout.in_dtype == GEMM_F16;
+    L.out_f16 = layout.out_dtype == GEMM_F16;
     L.a_major = layout.a_major;
     L.b_major = layout.b_major;
     L.tile = plan.tile_m;
@@ -735,9 +759,6 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, co
     });
   }
 
-  // tensor-core path: TMA reads need 16-byte aligned bases
-  if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15))
-    return GEMM_ERR_UNSUPPORTED;
   const bool swap = plan.swap_ab != 0;
   const void* opA = swap ? B : A;  // MMA-view A operand (rows Mm)
   const void* opB = swap ? A : B;  // MMA-view B operand (rows Nm)

@@ -74,13 +74,16 @@ int tc_max_active_clusters(int s);
 int tc_stages_for(int bn);
 int tc_smem_bytes_for(int bn);
 
-// fp32 CUDA-core GEMM (simt.cu).
+// CUDA-core GEMM with fp32 accumulation (simt_kernel.cuh): fp32 inputs
+// (simt.cu), or fp16 inputs the tensor-core path cannot read (simt_f16.cu).
 struct SimtLaunch {
   int64_t M, N, K;
-  const float* A;
-  const float* B;
+  const void* A;         // fp32, or fp16 when in_f16
+  const void* B;
   const float* bias;
-  float* C;
+  void* C;               // fp32, or fp16 when out_f16 (fp16 inputs only)
+  bool in_f16 = false;
+  bool out_f16 = false;
   int a_major, b_major;  // 0 row, 1 column
   int tile = 128;        // square tile edge: kSimtBM (128) or kSimtSmallTile (64)
   WorkSpec work;         // grid, tiles, raster order and k-split (work.cuh)
@@ -89,6 +92,7 @@ struct SimtLaunch {
   cudaStream_t stream;
 };
 cudaError_t launch_simt(const SimtLaunch& L);
+cudaError_t launch_simt_f16(const SimtLaunch& L);
 constexpr int kSimtBM = 128, kSimtBN = 128, kSimtBK = 8, kSimtThreads = 256;
 constexpr int kSimtSmallTile = 64;  // 64 x 64 tiles, 64 threads
 constexpr int kSimtMinSplitIters = 8;  // fewest k-blocks a split CTA gets

@@ -1,333 +1,25 @@
-// simt.cu: fp32 CUDA-core GEMM, C = A·B (+bias), true FFMA (no TF32).
-//
-// Each technique of the "TVM Matrix Multiplication Optimization" ladder
-// (kimm240.github.io/tvm, Steps 1-6) has its place here:
-//   Step 1 data-parallel 2-D thread map    -> one CTA per BM x BN output tile
-//   Step 2 tiling + loop reordering        -> each thread owns an 8x8 register tile
-//                                             and runs the k loop outermost
-//   Step 3 shared memory, cooperative fetch-> all threads stage a BM x 8 A block
-//                                             and an 8 x BN B block per k-step
-//   Step 4 vectorisation + register caching-> float4 global and shared loads;
-//                                             accumulators live in registers
-//   Step 5 software pipelining             -> two shared-memory buffers; the next
-//                                             block is fetched into registers
-//                                             while the current one is consumed
-//   Step 6 unrolling                       -> the k-step and the 8x8 FMA nest are
-//                                             fully unrolled
-// The staging rows are padded as storage_align(factor 32, offset 4) pads them
-// (leiblog.wang, the storage_align answer: the stride is raised to the next
-// value congruent to offset mod factor), 128 -> 132 and 64 -> 68 floats, which
-// makes the transposed A stores free of bank conflicts.
-//
-// Two tile shapes: 128 x 128 with 256 threads, and 64 x 64 with 64 threads for
-// grids too small to balance over the SMs (the 8x8 thread tile, and so the
-// ratio of shared loads to FMAs, is the same in both).
-//
-// Work is handed out as the tensor-core kernels hand it out (work.cuh): whole
-// tiles first, then, when the tile count would leave the last wave of resident
-// CTAs part-empty, the k-blocks of the remaining tiles split evenly over the
-// CTAs (the Stream-K decomposition of the leiblog.wang Stream-K post).  A CTA
-// whose unit covers part of a tile publishes its fp32 partial to the
-// workspace; the last contributor to arrive adds all partials in ascending k
-// order and stores the tile.  No CTA ever waits for another.
-#include "internal.h"
-#include "work.cuh"
+// simt.cu: the fp32-input instantiations of the CUDA-core GEMM
+// (simt_kernel.cuh), its host-side queries, and the K == 0 fill kernel.
+#include "simt_kernel.cuh"
 
 namespace dg {
 
-namespace {
-
-// storage_align(factor, offset) applied to a row of `extent` elements.
-__host__ __device__ constexpr int aligned_stride(int extent, int factor, int offset) {
-  return extent + (factor + offset - extent % factor) % factor;
-}
-static_assert(aligned_stride(128, 32, 4) == 132 && aligned_stride(64, 32, 4) == 68,
-              "padded staging strides");
-
-struct SimtArgs {
-  int64_t M, N, K;
-  const float* A;
-  const float* B;
-  const float* bias;
-  float* C;
-  bool vec_a, vec_b, vec_c;  // float4 access allowed (16-byte aligned rows)
-  WorkSpec work;             // tiles, raster order and split of this launch
-  float* workspace;          // split partials: 2 slots of BM x BN floats per CTA
-  int* tickets;              // one arrival counter per split tile (left at 0)
-};
-
-// One float4-wide piece of a k-block: `count` consecutive elements along the
-// storage row, starting at p; zero outside [0, limit) or when `inside` is false.
-__device__ __forceinline__ void load4(float (&r)[4], const float* p, bool vec, bool inside,
-                                      int64_t first, int64_t limit) {
-  if (vec && inside && first + 3 < limit) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(p));
-    r[0] = v.x; r[1] = v.y; r[2] = v.z; r[3] = v.w;
-  } else {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) r[i] = (inside && first + i < limit) ? __ldg(p + i) : 0.f;
-  }
-}
-
-// BM x BN tile, NT = (BM/8) x (BN/8) threads, each an 8x8 register tile made
-// of two 4-row groups BM/2 apart and two 4-column groups BN/2 apart.  A 1-D
-// grid of a.work.grid CTAs walks the units that WorkIter hands it.  Residency
-// asked of the compiler: 2 CTAs per SM for 128-tiles; 4 for 64-tiles, which the
-// picker uses only while 128-tiles are fewer than the SMs (so fewer than 4 x
-// SMs 64-tiles).
-template <int BM, int BN, bool A_COL, bool B_COL>
-__global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
-    simt_sgemm_kernel(const SimtArgs a) {
-  constexpr int BK = kSimtBK;
-  constexpr int NT = (BM / 8) * (BN / 8);
-  constexpr int AS = aligned_stride(BM, 32, 4);
-  constexpr int BS = aligned_stride(BN, 32, 4);
-  constexpr int AV = BM * BK / 4 / NT;  // float4 pieces of A per thread per k-block
-  constexpr int BV = BN * BK / 4 / NT;
-  static_assert(AV >= 1 && BV >= 1 && AV * NT * 4 == BM * BK && BV * NT * 4 == BN * BK, "");
-  __shared__ __align__(16) float As[2][BK][AS];
-  __shared__ __align__(16) float Bs[2][BK][BS];
-  __shared__ int last_flag;
-
-  const int t = threadIdx.x;
-  const int tx = t % (BN / 8), ty = t / (BN / 8);
-  const int64_t M = a.M, N = a.N, K = a.K;
-  const WorkSpec& W = a.work;
-
-  float ra[AV][4], rb[BV][4];
-  float acc[8][8];
-
-  // Global -> registers for the k-block starting at k0 of the tile at (m0, n0).
-  // Piece f of A is, for row-major A, row f/2 and k-quarter f%2; for
-  // column-major A, k-row f/(BM/4) and m-quarter f%(BM/4).  B likewise.
-  auto fetch = [&](int64_t m0, int64_t n0, int64_t k0) {
-#pragma unroll
-    for (int v = 0; v < AV; ++v) {
-      const int f = t + v * NT;
-      if (!A_COL) {
-        const int64_t m = m0 + (f >> 1), k = k0 + (f & 1) * 4;
-        load4(ra[v], a.A + m * K + k, a.vec_a, m < M, k, K);
-      } else {
-        const int64_t k = k0 + f / (BM / 4), m = m0 + (f % (BM / 4)) * 4;
-        load4(ra[v], a.A + k * M + m, a.vec_a, k < K, m, M);
-      }
-    }
-#pragma unroll
-    for (int v = 0; v < BV; ++v) {
-      const int f = t + v * NT;
-      if (!B_COL) {
-        const int64_t k = k0 + f / (BN / 4), n = n0 + (f % (BN / 4)) * 4;
-        load4(rb[v], a.B + k * N + n, a.vec_b, k < K, n, N);
-      } else {
-        const int64_t n = n0 + (f >> 1), k = k0 + (f & 1) * 4;
-        load4(rb[v], a.B + n * K + k, a.vec_b, n < N, k, K);
-      }
-    }
-  };
-
-  // Registers -> shared buffer `buf`, as As[k][m] and Bs[k][n].
-  auto stage = [&](int buf) {
-#pragma unroll
-    for (int v = 0; v < AV; ++v) {
-      const int f = t + v * NT;
-      if (!A_COL) {
-        const int m = f >> 1, k = (f & 1) * 4;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) As[buf][k + i][m] = ra[v][i];
-      } else {
-        const int k = f / (BM / 4), m = (f % (BM / 4)) * 4;
-        *reinterpret_cast<float4*>(&As[buf][k][m]) =
-            make_float4(ra[v][0], ra[v][1], ra[v][2], ra[v][3]);
-      }
-    }
-#pragma unroll
-    for (int v = 0; v < BV; ++v) {
-      const int f = t + v * NT;
-      if (!B_COL) {
-        const int k = f / (BN / 4), n = (f % (BN / 4)) * 4;
-        *reinterpret_cast<float4*>(&Bs[buf][k][n]) =
-            make_float4(rb[v][0], rb[v][1], rb[v][2], rb[v][3]);
-      } else {
-        const int n = f >> 1, k = (f & 1) * 4;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) Bs[buf][k + i][n] = rb[v][i];
-      }
-    }
-  };
-
-  // Epilogue: + bias[n]; rows ty*4+i (+BM/2), columns tx*4+j (+BN/2).
-  auto store_tile = [&](int64_t m0, int64_t n0) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int64_t m = m0 + (i < 4 ? ty * 4 + i : BM / 2 + ty * 4 + (i - 4));
-      if (m >= M) continue;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int64_t n = n0 + h * (BN / 2) + tx * 4;
-        if (n >= N) continue;
-        float o[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          o[j] = acc[i][h * 4 + j] + ((a.bias && n + j < N) ? __ldg(a.bias + n + j) : 0.f);
-        float* dst = a.C + m * N + n;
-        if (a.vec_c && n + 3 < N) {
-          *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (n + j < N) dst[j] = o[j];
-        }
-      }
-    }
-  };
-
-  // The work iterator lives in shared memory, advanced by thread 0, so none of
-  // its state occupies registers across the k loop.
-  __shared__ WorkIter s_it;
-  __shared__ Unit s_unit;
-  __shared__ int s_more;
-  if (t == 0) s_it.init(W, int32_t(blockIdx.x));
-  for (;;) {
-    if (t == 0) s_more = s_it.next(W, s_unit) ? 1 : 0;
-    __syncthreads();
-    if (!s_more) break;
-    const Unit u = s_unit;
-    int32_t tm, tn;
-    tile_coords(W, u.tile, tm, tn);
-    const int64_t m0 = int64_t(tm) * BM, n0 = int64_t(tn) * BN;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-
-    // The previous unit ended with a barrier after its last shared reads, so
-    // buffer 0 is free.
-    fetch(m0, n0, int64_t(u.kb0) * BK);
-    stage(0);
-    __syncthreads();
-    for (int32_t kt = u.kb0; kt < u.kb1; ++kt) {
-      const int buf = (kt - u.kb0) & 1;
-      if (kt + 1 < u.kb1) fetch(m0, n0, int64_t(kt + 1) * BK);
-#pragma unroll
-      for (int kk = 0; kk < BK; ++kk) {
-        const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
-        const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][BM / 2 + ty * 4]);
-        const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
-        const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][BN / 2 + tx * 4]);
-        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
-      }
-      if (kt + 1 < u.kb1) stage(buf ^ 1);
-      __syncthreads();
-    }
-
-    if (!unit_is_partial(W, u)) {
-      store_tile(m0, n0);
-      continue;
-    }
-    // Split unit.  Publish the fp32 partial: float4 j of thread t (row j/2 of
-    // its register tile, column half j%2) at float4 index j*NT + t of the slot,
-    // so each warp's stores are contiguous.
-    const int32_t st = u.tile - W.dp_tiles;
-    const int32_t me = int32_t(blockIdx.x);
-    const size_t slot_elems = size_t(BM) * BN;
-    float4* mine = reinterpret_cast<float4*>(a.workspace +
-                                             size_t(split_slot(W, me, st)) * slot_elems);
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-      __stcg(mine + j * NT + t, make_float4(acc[j >> 1][(j & 1) * 4], acc[j >> 1][(j & 1) * 4 + 1],
-                                            acc[j >> 1][(j & 1) * 4 + 2],
-                                            acc[j >> 1][(j & 1) * 4 + 3]));
-    __threadfence();
-    __syncthreads();
-    int32_t first, last;
-    split_contributors(W, st, first, last);
-    if (t == 0) {
-      const int old = atomicAdd(&a.tickets[st], 1);
-      last_flag = (old == last - first) ? 1 : 0;
-    }
-    __syncthreads();
-    if (!last_flag) continue;
-    // Last to arrive: every contributor's partial, this CTA's own included,
-    // is in the workspace.  Add them in ascending k order, whichever CTA
-    // arrived last, so the sum is the same on every run.
-    // Every contributor after the first starts its range inside this tile, so
-    // its partial is in its first slot (split_slot gives 2r for it).
-    __threadfence();
-    const int32_t first_slot = split_slot(W, first, st);
-    // four float4 (one register-tile row pair) of every contributor at a time
-#pragma unroll
-    for (int jc = 0; jc < 4; ++jc) {
-      for (int32_t r = first; r <= last; ++r) {
-        const float4* src = reinterpret_cast<const float4*>(
-            a.workspace + size_t(r == first ? first_slot : 2 * r) * slot_elems);
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int j = jc * 4 + jj;
-          const float4 v = __ldcg(src + j * NT + t);
-          float* d = &acc[j >> 1][(j & 1) * 4];
-          if (r == first) {
-            d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
-          } else {
-            d[0] += v.x; d[1] += v.y; d[2] += v.z; d[3] += v.w;
-          }
-        }
-      }
-    }
-    if (t == 0) atomicExch(&a.tickets[st], 0);  // ready for the next launch
-    store_tile(m0, n0);
-  }
-}
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
-
-template <int BM, int BN>
-cudaError_t launch_simt_tile(const SimtArgs& a, int a_major, int b_major, cudaStream_t s) {
-  constexpr int NT = (BM / 8) * (BN / 8);
-  if (a.work.grid <= 0) return cudaErrorInvalidConfiguration;
-  const dim3 grid{unsigned(a.work.grid), 1u, 1u};
-  if (a_major == 0 && b_major == 0)
-    simt_sgemm_kernel<BM, BN, false, false><<<grid, NT, 0, s>>>(a);
-  else if (a_major == 0)
-    simt_sgemm_kernel<BM, BN, false, true><<<grid, NT, 0, s>>>(a);
-  else if (b_major == 0)
-    simt_sgemm_kernel<BM, BN, true, false><<<grid, NT, 0, s>>>(a);
-  else
-    simt_sgemm_kernel<BM, BN, true, true><<<grid, NT, 0, s>>>(a);
-  return cudaGetLastError();
-}
-
-}  // namespace
-
-int simt_a_stride() { return aligned_stride(kSimtBM, 32, 4); }
-int simt_b_stride() { return aligned_stride(kSimtBN, 32, 4); }
+int simt_a_stride() { return simt_detail::aligned_stride(kSimtBM, 32, 4); }
+int simt_b_stride() { return simt_detail::aligned_stride(kSimtBN, 32, 4); }
 
 int simt_ctas_per_sm() {
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-          &n, simt_sgemm_kernel<kSimtBM, kSimtBN, false, false>, kSimtThreads, 0) != cudaSuccess)
+          &n, simt_detail::simt_sgemm_kernel<float, float, kSimtBM, kSimtBN, false, false>,
+          kSimtThreads, 0) != cudaSuccess)
     return -1;
   return n;
 }
 
 cudaError_t launch_simt(const SimtLaunch& L) {
-  SimtArgs a;
-  a.M = L.M; a.N = L.N; a.K = L.K;
-  a.A = L.A; a.B = L.B; a.bias = L.bias; a.C = L.C;
-  a.vec_a = aligned16(L.A) && ((L.a_major == 0 ? L.K : L.M) % 4 == 0);
-  a.vec_b = aligned16(L.B) && ((L.b_major == 0 ? L.N : L.K) % 4 == 0);
-  a.vec_c = aligned16(L.C) && (L.N % 4 == 0);
-  a.work = L.work;
-  a.workspace = L.workspace;
-  a.tickets = L.tickets;
-  if (a.work.sk_tiles > 0 && (!a.workspace || !a.tickets)) return cudaErrorInvalidValue;
-  if (L.tile == kSimtSmallTile)
-    return launch_simt_tile<kSimtSmallTile, kSimtSmallTile>(a, L.a_major, L.b_major, L.stream);
-  return launch_simt_tile<kSimtBM, kSimtBN>(a, L.a_major, L.b_major, L.stream);
+  if (L.in_f16) return launch_simt_f16(L);
+  if (L.out_f16) return cudaErrorInvalidValue;  // fp32 inputs give fp32 outputs
+  return simt_detail::launch_simt_typed<float, float>(L);
 }
 
 // ---------------------------------------------------------------- K == 0 --

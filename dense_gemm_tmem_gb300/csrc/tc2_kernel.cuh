@@ -388,6 +388,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   using Cfg = Tc2Config;
   constexpr int S = Cfg::kStages;
 
+  const uint64_t t_entry = args.trace ? globaltimer_ns() : 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -438,7 +439,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   pdl_launch_dependents();
   pdl_wait_prerequisites();
   const WaitCtl wc{args.wait_limit_ns, args.status, abort_flag};
-  if (threadIdx.x == 0) trace_mark(args, blockIdx.x, kTraceStart);
+  if (threadIdx.x == 0 && args.trace) {
+    args.trace[size_t(blockIdx.x) * kTraceSlots + kTraceEntry] = t_entry;
+    trace_mark(args, blockIdx.x, kTraceStart);
+  }
 
   if (warp == 0) {
     if (lane == 0) tc2_producer<S>(tmA, tmB, args, sA, sB, full, empty, wc, rank, cluster_id);
@@ -459,6 +463,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+    if (lane == 0) trace_mark(args, blockIdx.x, kTraceExit);
   }
 }
 

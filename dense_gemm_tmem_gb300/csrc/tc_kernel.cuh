@@ -86,7 +86,11 @@ enum TracePhase : int {
   kTraceEnd = 5,        // epilogue finished (stores and any split fixup)
   kTraceUnits = 6,      // number of work units (not a time)
   kTraceClusterDone = 7,  // cluster split: the cluster's partials added and stored
-  kTraceSlots = 8
+  kTraceEntry = 8,      // kernel entry (taken first, written after the prerequisite wait)
+  kTraceExit = 9,       // TMEM freed, about to return
+  kTraceClusterParked = 10,   // cluster split: every CTA of the cluster parked its partial
+  kTraceClusterReduced = 11,  // cluster split: thread 0's share of the reduction stored
+  kTraceSlots = 12
 };
 
 __device__ __forceinline__ void trace_mark(const TcArgs& a, uint32_t cta, int phase) {
@@ -307,10 +311,13 @@ __device__ __forceinline__ void store_out(const TcArgs& a, float* sw, int32_t mm
 // [rank*R, (rank+1)*R), R = 128 / s, over all s partials in rank order -- rank
 // order is ascending k, so the sum does not depend on timing -- adds the bias
 // and writes C.  Work goes in groups of 4 floats along the direction in which
-// C is contiguous (output columns, or rows for the transposed store); each
-// thread keeps the s remote 16-byte loads of two groups in flight at once.
+// C is contiguous (output columns, or rows for the transposed store).  All
+// `nthreads` threads of the CTA take part, each with the loads of kU groups
+// (s 16-byte loads each, the own partial from local shared memory) in flight
+// at once: the reduction is bound by the round trip to the peers' memory.
 template <int BN, bool OUT_F16, bool TRANS>
-__device__ __forceinline__ void csplit_reduce(const TcArgs& a, const uint8_t* smem, int et) {
+__device__ __forceinline__ void csplit_reduce(const TcArgs& a, const uint8_t* smem, int tid,
+                                              int nthreads) {
   const WorkSpec& W = a.work;
   const int s = W.csplit;
   const int rank = int(blockIdx.x) % s;
@@ -322,14 +329,14 @@ __device__ __forceinline__ void csplit_reduce(const TcArgs& a, const uint8_t* sm
 #pragma unroll
   for (int j = 0; j < 8; ++j) peer[j] = j < s ? map_to_rank(local, uint32_t(j)) : 0u;
   const int groups = TRANS ? BN * (R / 4) : R * (BN / 4);
-  constexpr int kU = 2;
+  constexpr int kU = 4;
 #pragma unroll 1
-  for (int g0 = et; g0 < groups; g0 += kU * kEpiThreads) {
+  for (int g0 = tid; g0 < groups; g0 += kU * nthreads) {
     float4 part[kU][8];
     int row[kU], col[kU];
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
-      const int g = g0 + u * kEpiThreads;
+      const int g = g0 + u * nthreads;
       if (TRANS) {
         col[u] = g / (R / 4);
         row[u] = rank * R + (g % (R / 4)) * 4;
@@ -342,12 +349,14 @@ __device__ __forceinline__ void csplit_reduce(const TcArgs& a, const uint8_t* sm
             4u * uint32_t(TRANS ? col[u] * kParkColStride + row[u] : row[u] * kParkRowStride<BN> + col[u]);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          if (j < s) part[u][j] = ld_dsmem_f32x4(peer[j] + off);
+          if (j < s)
+            part[u][j] = j == rank ? *reinterpret_cast<const float4*>(smem + off)
+                                   : ld_dsmem_f32x4(peer[j] + off);
       }
     }
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
-      if (g0 + u * kEpiThreads >= groups) break;
+      if (g0 + u * nthreads >= groups) break;
       float4 acc = part[u][0];
 #pragma unroll
       for (int j = 1; j < 8; ++j)
@@ -390,6 +399,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr int S = Cfg::kStages;
   constexpr int CW = Cfg::kChunk;
 
+  const uint64_t t_entry = args.trace ? globaltimer_ns() : 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -442,7 +452,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   pdl_wait_prerequisites();
   const WaitCtl wc{args.wait_limit_ns, args.status, abort_flag};
   const WorkSpec& W = args.work;
-  if (threadIdx.x == 0) trace_mark(args, blockIdx.x, kTraceStart);
+  if (threadIdx.x == 0 && args.trace) {
+    args.trace[size_t(blockIdx.x) * kTraceSlots + kTraceEntry] = t_entry;
+    trace_mark(args, blockIdx.x, kTraceStart);
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
@@ -710,13 +723,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // Every thread of every CTA of the cluster reaches both barriers, aborted
     // or not, so neither can wait forever.
     cluster_sync_all();  // all partials parked
-    if (warp >= 2) csplit_reduce<BN, OUT_F16, TRANS>(args, smem, threadIdx.x - 64);
+    if (threadIdx.x == 0) trace_mark(args, blockIdx.x, kTraceClusterParked);
+    csplit_reduce<BN, OUT_F16, TRANS>(args, smem, threadIdx.x, kTcThreads);
+    if (threadIdx.x == 0) trace_mark(args, blockIdx.x, kTraceClusterReduced);
     cluster_sync_all();  // no CTA still reads another's shared memory
     if (threadIdx.x == 0) trace_mark(args, blockIdx.x, kTraceClusterDone);
   }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    if (lane == 0) trace_mark(args, blockIdx.x, kTraceExit);
   }
 }
 

@@ -63,7 +63,8 @@ typedef struct {
 enum {
   GEMM_KERNEL_TC = 0,       /* tcgen05/TMEM tensor-core GEMM, whole output tiles */
   GEMM_KERNEL_STREAMK = 1,  /* the same kernel with Stream-K (or hybrid) k-splitting */
-  GEMM_KERNEL_SIMT = 2,     /* CUDA-core fp32 GEMM */
+  GEMM_KERNEL_SIMT = 2,     /* CUDA-core GEMM, fp32 accumulation: fp32 inputs, or fp16
+                               inputs the tensor-core path cannot read */
   GEMM_KERNEL_FILL = 3,     /* K == 0: C = bias (or 0) */
   GEMM_KERNEL_NONE = 4,     /* M == 0 or N == 0: nothing to do */
   GEMM_KERNEL_TC2 = 5,      /* two-SM tcgen05 GEMM (CTA pairs, cta_group::2), 256 x 256
@@ -99,7 +100,7 @@ typedef struct {
 
 /* Options for tests and tuning (gemm_set_option).  Values < 0 restore the default. */
 enum {
-  GEMM_OPT_FORCE_KERNEL = 0,     /* GEMM_KERNEL_TC / _STREAMK / _SIMT / _TC2, or -1 */
+  GEMM_OPT_FORCE_KERNEL = 0,     /* GEMM_KERNEL_TC / _STREAMK / _SIMT / _TC2 / _SPLITC, or -1 */
   GEMM_OPT_FORCE_TILE_N = 1,     /* 16, 32, 64, 128, 256 (tensor-core path), or -1 */
   GEMM_OPT_FORCE_GRID = 2,       /* CTA count for the split path, or -1 */
   GEMM_OPT_WAIT_LIMIT_NS = 3,    /* bound on each device-side wait (default 2e9 ns) */
@@ -135,10 +136,11 @@ int gemm_destroy(gemm_handle_t h);
 
 /* Enqueues C = A·B (+bias) on `stream` and returns without waiting.
  * Picks the kernel with the rules gemm_query_plan reports.
- * Requirements for fp16 inputs (tensor-core path, operands read by TMA):
- *   A and B 16-byte aligned and each leading dimension a multiple of 8
- *   elements; otherwise GEMM_ERR_UNSUPPORTED.  C and bias have no alignment
- *   requirement.  fp32 inputs have no alignment requirement.
+ * Alignment: none is required.  fp16 inputs go to the tensor cores (operands
+ *   read by TMA) when A and B are 16-byte aligned and each leading dimension
+ *   is a multiple of 8 elements; otherwise (and for operands with 2^31 or more
+ *   rows or columns) to the CUDA-core kernel, fp16 widened to fp32 with fp32
+ *   accumulation, which is much slower.  gemm_query_plan assumes aligned bases.
  * M == 0 or N == 0: nothing is launched.  K == 0: C = bias (or 0).
  * One handle must not run on two streams at once: its workspace is shared.
  * Device-side wait timeouts are not seen here; call gemm_status.
@@ -162,14 +164,19 @@ int gemm_status(gemm_handle_t h, void *stream);
 int gemm_status_detail(gemm_handle_t h);
 
 /* Phase tracing for the tensor-core kernels.  dev_buf: NULL (tracing off) or a
- * caller-owned DEVICE buffer of ctas x 8 uint64 values; while set, every
+ * caller-owned DEVICE buffer of ctas x 12 uint64 values; while set, every
  * tensor-core launch whose grid fits in `ctas` CTAs writes, for CTA i,
- * %globaltimer nanoseconds to dev_buf[8*i + p] at phase p: 0 setup done,
- * 1 first TMA load issued, 2 first stage landed (MMA issuer), 3 last
+ * %globaltimer nanoseconds to dev_buf[12*i + p] at phase p: 8 kernel entry,
+ * 0 setup done (barriers, TMEM, the wait for the previous kernel on the
+ * stream), 1 first TMA load issued, 2 first stage landed (MMA issuer), 3 last
  * accumulator committed, 4 last accumulator received by the epilogue,
- * 5 epilogue done; slot 6 holds the CTA's work-unit count.  Slots a CTA never
- * reaches (e.g. the MMA slots of the second CTA of a pair) are not written.
- * Launches with more CTAs than `ctas` are not traced.  Errors: INVALID_ARG. */
+ * 5 epilogue done, 10 cluster split: every CTA of the cluster parked its
+ * partial, 11 cluster split: this CTA's share of the reduction stored (by
+ * thread 0), 7 cluster split: the whole cluster done, 9 TMEM freed (about to
+ * return); slot 6 holds the CTA's work-unit count.  Slots a CTA
+ * never reaches (e.g. the MMA slots of the second CTA of a pair) are not
+ * written.  Launches with more CTAs than `ctas` are not traced.
+ * Errors: INVALID_ARG. */
 int gemm_set_trace(gemm_handle_t h, uint64_t *dev_buf, int64_t ctas);
 
 /* Failure-path self-test: enqueues one CTA whose wait on an mbarrier that

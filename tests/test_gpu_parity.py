@@ -222,6 +222,7 @@ def test_permutation_columns_exact(g, dev, kernel):
     ("simt", 200, 300, 500, 0, 0, F32, F32, {}),
     ("simt_col", 200, 300, 500, 1, 1, F32, F32, {}),
     ("simt_split", 300, 420, 1000, 1, 0, F32, F32, {"grid": 23}),
+    ("simt_f16", 300, 420, 1000, 1, 0, F16, F16, {"kernel": SIMT, "grid": 23}),
     ("pair", 520, 776, 1032, 0, 1, F16, F32, {"kernel": TC2}),
     ("pair16", 296, 520, 2048, 1, 0, F16, F16, {"kernel": TC2, "grid": 4}),
     ("pair_split", 520, 776, 1032, 0, 1, F16, F32, {"kernel": TC2, "pair_split": 1, "grid": 14}),
@@ -282,17 +283,54 @@ def test_fp16_alignment_rules(g, dev):
     C = torch.empty((64, 64), dtype=torch.float32, device=dev)
     with pytest.raises(ValueError):
         g.run(A[:, :100], Bt, C)  # not contiguous -> rejected before the C-ABI
-    A2 = torch.zeros((64, 100), dtype=torch.float16, device=dev)  # lda = 100: not % 8
-    with pytest.raises(B.GemmError) as e:
-        g.run(A2, Bt, C)
-    assert e.value.code == B.GEMM_ERR_UNSUPPORTED
-    # a base that is not 16-byte aligned
-    flat = torch.zeros(64 * 64 + 1, dtype=torch.float16, device=dev)
-    A3 = flat[1:].view(64, 64)
-    B3 = torch.zeros((64, 64), dtype=torch.float16, device=dev)
-    rc = B.gemm_run(g.handle, 64, 64, 64, A3.data_ptr(), B3.data_ptr(), None, C.data_ptr(),
-                    B.layout(0, 0, B.GEMM_F16, B.GEMM_F32), 0)
-    assert rc == B.GEMM_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("odt", [F16, F32])
+def test_fp16_odd_leading_dims_run_on_cuda_cores(g, dev, odt):
+    """lda = K = 100 breaks the TMA stride rule: the CUDA-core kernel runs it
+    with fp32 accumulation."""
+    ocode = B.GEMM_F16 if odt == F16 else B.GEMM_F32
+    assert g.plan(70, 64, 100, 0, 0, B.GEMM_F16, ocode)["kernel"] == SIMT
+    p = problem(70, 64, 100, 0, 0, F16, odt, True, 170 + (odt == F32))
+    full_check(g, dev, p)
+
+
+@pytest.mark.parametrize("odt", [F16, F32])
+def test_fp16_unaligned_bases_run_on_cuda_cores(g, dev, odt):
+    """A and B based 2 bytes past a 16-byte boundary: the TMA cannot read them,
+    the CUDA-core kernel does."""
+    M, N, K = 130, 264, 200
+    p = problem(M, N, K, 0, 1, F16, odt, True, 175 + (odt == F32))
+    A, Bt, bias = to_dev(p, dev)
+    af = torch.zeros(A.numel() + 1, dtype=torch.float16, device=dev)
+    af[1:] = A.flatten()
+    bf = torch.zeros(Bt.numel() + 1, dtype=torch.float16, device=dev)
+    bf[1:] = Bt.flatten()
+    C = torch.empty((M, N), dtype=TDT[odt], device=dev)
+    ocode = B.GEMM_F16 if odt == F16 else B.GEMM_F32
+    rc = B.gemm_run(g.handle, M, N, K, af[1:].data_ptr(), bf[1:].data_ptr(), bias.data_ptr(),
+                    C.data_ptr(), B.layout(0, 1, B.GEMM_F16, ocode),
+                    torch.cuda.current_stream(dev).cuda_stream)
+    assert rc == 0
+    g.status()
+    check(as_f64(C), oracle.gemm(p.A, p.B, p.bias, b_major=1), p)
+
+
+@pytest.mark.parametrize("tile", [64, 128])
+@pytest.mark.parametrize("am,bm", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("odt", [F16, F32])
+def test_fp16_cuda_core_layouts(g, dev, tile, am, bm, odt):
+    set_opts(g, kernel=SIMT, tile_n=tile)
+    p = problem(130, 70, 96, am, bm, F16, odt, True, 180 + 4 * am + 2 * bm + (odt == F32))
+    full_check(g, dev, p)
+
+
+@pytest.mark.parametrize("grid", [3, 37, 304])
+def test_fp16_cuda_core_split(g, dev, grid):
+    set_opts(g, kernel=SIMT, grid=grid)
+    p = problem(392, 600, 1480, 0, 1, F16, F16, True, 190 + grid)
+    assert g.plan(392, 600, 1480, 0, 1, B.GEMM_F16, B.GEMM_F16)["grid"] == grid
+    full_check(g, dev, p)
 
 
 def test_unaligned_outputs_and_bias(g, dev):

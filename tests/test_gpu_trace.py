@@ -13,7 +13,8 @@ from gpu_helpers import TDT, set_opts, to_dev
 
 pytestmark = pytest.mark.gpu
 
-START, FIRST_LOAD, FIRST_DATA, MMA_DONE, LAST_ACCUM, END, UNITS = range(7)
+(START, FIRST_LOAD, FIRST_DATA, MMA_DONE, LAST_ACCUM, END, UNITS, CLUSTER_DONE, ENTRY, EXIT,
+ PARKED, REDUCED) = range(12)
 
 
 @pytest.fixture(scope="module")
@@ -24,7 +25,7 @@ def dev():
 
 
 @pytest.mark.parametrize("M,N,K,kernel", [
-    (16, 4096, 4096, -1),                        # swapped split (Stream-K)
+    (16, 4096, 4096, -1),                        # swapped, cluster split
     (1024, 19 * 256, 512, B.GEMM_KERNEL_TC2),     # one wave of CTA pairs
     (600, 1000, 1480, B.GEMM_KERNEL_TC),          # whole tiles, one SM each
 ])
@@ -37,7 +38,7 @@ def test_trace_stamps(dev, M, N, K, kernel):
     plain = g(A, Bt, bias)
     pl = g.plan(M, N, K)
     grid = pl["grid"]
-    buf = torch.zeros((grid, 8), dtype=torch.int64, device=dev)
+    buf = torch.zeros((grid, B.TRACE_SLOTS), dtype=torch.int64, device=dev)
     assert B.gemm_set_trace(g.handle, buf.data_ptr(), grid) == B.GEMM_OK
     traced = g(A, Bt, bias)
     g.status()
@@ -53,7 +54,9 @@ def test_trace_stamps(dev, M, N, K, kernel):
         assert row[UNITS] == n_units
         if n_units == 0:
             continue
-        assert 0 < row[START] <= row[FIRST_LOAD] <= row[END]
+        assert 0 < row[ENTRY] <= row[START] <= row[FIRST_LOAD] <= row[END] <= row[EXIT]
+        if plan.kernel == B.GEMM_KERNEL_SPLITC:
+            assert row[END] <= row[PARKED] <= row[REDUCED] <= row[CLUSTER_DONE] <= row[EXIT]
         assert row[LAST_ACCUM] <= row[END]
         if not pair or cta % 2 == 0:  # the CTA that issues the MMAs
             assert row[FIRST_LOAD] <= row[FIRST_DATA] <= row[MMA_DONE] <= row[LAST_ACCUM]
@@ -66,7 +69,7 @@ def test_trace_stamps(dev, M, N, K, kernel):
 
 def test_trace_buffer_too_small_is_skipped(dev):
     g = Gemm(dev)
-    buf = torch.zeros((4, 8), dtype=torch.int64, device=dev)
+    buf = torch.zeros((4, B.TRACE_SLOTS), dtype=torch.int64, device=dev)
     assert B.gemm_set_trace(g.handle, buf.data_ptr(), 4) == B.GEMM_OK
     p = inputs.make_problem("tr", 16, 4096, 4096, 0, 0, inputs.F16, inputs.F32, "uniform",
                             False, 301)

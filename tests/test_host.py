@@ -176,10 +176,18 @@ def test_picker_fp32_and_degenerate():
 
 
 def test_picker_fp16_tma_stride_rule():
-    assert plan(64, 64, 100)[0] == B.GEMM_ERR_UNSUPPORTED       # A row-major, K % 8
-    assert plan(64, 100, 64)[0] == B.GEMM_ERR_UNSUPPORTED       # B row-major, N % 8
-    assert plan(64, 100, 64, 0, 1)[0] == 0                      # B col-major: ldb = K
-    assert plan(100, 64, 64, 1, 0)[0] == B.GEMM_ERR_UNSUPPORTED  # A col-major, M % 8
+    """fp16 leading dimensions that are not a multiple of 8 elements break the
+    TMA stride rule: those run on the CUDA-core kernel (fp32 accumulation)."""
+    simt = B.GEMM_KERNEL_SIMT
+    for args in [(64, 64, 100), (64, 100, 64), (100, 64, 64, 1, 0)]:  # K, N, M not % 8
+        rc, p = plan(*args)
+        assert rc == 0 and p.kernel == simt and p.tile_m == 64
+    rc, p = plan(64, 100, 64, 0, 1)                             # B col-major: ldb = K
+    assert rc == 0 and p.kernel != simt
+    rc, p = plan(2050, 2048, 2048, 0, 0, F16, F16)              # M is no stride: tensor cores
+    assert rc == 0 and p.kernel != simt
+    rc, p = plan(2048, 2048, 2050, 0, 0, F16, F16)
+    assert rc == 0 and p.kernel == simt and p.sk_tiles == 256 and p.grid == 304
 
 
 PLANS = [(512, 512, 512, 0, 0, F16), (1, 4096, 4096, 0, 0, F16), (16, 4096, 4096, 0, 0, F16),
