@@ -25,9 +25,10 @@ struct TmapKey {
   const void* ptr;
   int64_t rows, k;
   int mn_major, box_rows;
+  int kind;  // 0 fp16 operand, 1 fp32 output, 2 fp16 output
   bool operator==(const TmapKey& o) const {
     return ptr == o.ptr && rows == o.rows && k == o.k && mn_major == o.mn_major &&
-           box_rows == o.box_rows;
+           box_rows == o.box_rows && kind == o.kind;
   }
 };
 
@@ -437,7 +438,7 @@ namespace {
 // 128-byte swizzle; out-of-range elements read as zero.
 int encode_operand(gemm_ctx* h, CUtensorMap* out, const void* ptr, int64_t rows, int64_t K,
                    int mn_major, int box_rows) {
-  const TmapKey key{ptr, rows, K, mn_major, box_rows};
+  const TmapKey key{ptr, rows, K, mn_major, box_rows, 0};
   {
     std::lock_guard<std::mutex> g(h->mu);
     for (auto& e : h->cache)
@@ -477,6 +478,48 @@ int encode_operand(gemm_ctx* h, CUtensorMap* out, const void* ptr, int64_t rows,
   e.valid = true;
   *out = map;
   return GEMM_OK;
+}
+
+// Row-major C (M x N, ldc = N) for the epilogue's TMA stores: 32 x 32 boxes,
+// 128-byte swizzle for fp32 (128-byte box rows), 64-byte for fp16.  Returns
+// false when C cannot take them (base not 16-byte aligned, row pitch not a
+// multiple of 16 bytes, or the encode fails); the epilogue then stores with
+// plain instructions.
+bool encode_output(gemm_ctx* h, CUtensorMap* out, void* C, int64_t M, int64_t N, bool f16) {
+  const int64_t pitch = N * (f16 ? 2 : 4);
+  if ((reinterpret_cast<uintptr_t>(C) & 15) || pitch % 16 != 0 || M > kMaxCoord ||
+      N > kMaxCoord)
+    return false;
+  const TmapKey key{C, M, N, 0, 32, f16 ? 2 : 1};
+  {
+    std::lock_guard<std::mutex> g(h->mu);
+    for (auto& e : h->cache)
+      if (e.valid && e.key == key) {
+        *out = e.map;
+        return true;
+      }
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(N), cuuint64_t(M)};
+  const cuuint64_t strides[1] = {cuuint64_t(pitch)};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  CUtensorMap map;
+  const CUresult r =
+      fn(&map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, C,
+         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         f16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> g(h->mu);
+  TmapEntry& e = h->cache[h->cache_next];
+  h->cache_next = (h->cache_next + 1) % kTmapCacheSize;
+  e.key = key;
+  e.map = map;
+  e.valid = true;
+  *out = map;
+  return true;
 }
 
 // Runs `f` with the handle's device current, restoring the caller's.
@@ -698,6 +741,10 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value) {
       if (value > 2) return GEMM_ERR_INVALID_ARG;
       o.pair_split = value < 0 ? d.pair_split : int(value);
       return GEMM_OK;
+    case GEMM_OPT_TMA_STORE:
+      if (value > 1) return GEMM_ERR_INVALID_ARG;
+      o.tma_store = value < 0 ? d.tma_store : int(value);
+      return GEMM_OK;
     default:
       return GEMM_ERR_INVALID_ARG;
   }
@@ -793,6 +840,13 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, co
   a.wait_limit_ns = h->opt.wait_limit_ns;
   a.a_mn = plan.a_mn_major;
   a.b_mn = plan.b_mn_major;
+  // row-major output chunks of 32 columns leave by TMA store when C allows it
+  std::memset(&L.tmC, 0, sizeof(L.tmC));
+  a.c_tma = (h->opt.tma_store && !swap && plan.tile_n >= 32 &&
+             plan.kernel != GEMM_KERNEL_SPLITC &&
+             dg::encode_output(h, &L.tmC, C, M, N, layout.out_dtype == GEMM_F16))
+                ? 1
+                : 0;
   // phase stamps only if the caller's buffer holds one row per CTA
   a.trace = (h->trace && h->trace_ctas >= plan.grid) ? h->trace : nullptr;
   a.idesc = dg::make_idesc_f16(pair ? dg::kPairBM : dg::kBM, plan.tile_n, plan.a_mn_major,

@@ -25,6 +25,7 @@ struct Options {
   int csplit = -1;         // cluster split: -1 picker's rule, 0 never, 2/4/8 forced
   int pdl = 1;             // programmatic dependent launch of the tensor-core kernels
   int pair_split = -1;     // two-SM kernel k-split: -1/0 none, 1 all tiles, 2 the tail
+  int tma_store = 1;       // epilogue output by TMA store where C allows it
   int csplit_clusters[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};  // clusters of s resident (0: SMs/s)
   int simt_per_sm = 0;     // 128 x 128 CUDA-core CTAs resident per SM (0: 2); set per device
   uint64_t wait_limit_ns = 2000000000ull;
@@ -54,6 +55,7 @@ struct TcLaunch {
   int grid;
   CUtensorMap tmA;
   CUtensorMap tmB;
+  CUtensorMap tmC;  // row-major C, 32 x 32 boxes; used only when args.c_tma
   TcArgs args;
   cudaStream_t stream;
 };

@@ -16,6 +16,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "internal.h"
@@ -194,5 +195,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
   a.b_mn = plan.b_mn_major;
   a.idesc = make_idesc_f16(pair ? kPairBM : kBM, plan.tile_n, plan.a_mn_major, plan.b_mn_major);
   a.trace = nullptr;
+  std::memset(&L.tmC, 0, sizeof(L.tmC));
+  a.c_tma = 0;  // plain stores: no output tensor map to encode and keep
   return launch_tc(L) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }

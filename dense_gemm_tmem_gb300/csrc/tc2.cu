@@ -22,7 +22,7 @@ cudaError_t launch_tc2_inst(const TcLaunch& L) {
   cfg.stream = L.stream;
   cfg.attrs = attr;
   cfg.numAttrs = L.pdl ? 1u : 0u;
-  return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.args);
+  return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.tmC, L.args);
 }
 }  // namespace
 

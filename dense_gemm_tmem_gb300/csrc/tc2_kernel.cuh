@@ -37,7 +37,9 @@ struct Tc2Config {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 512;  // two 256-column accumulators
   static constexpr int kBarBytes = 256;
-  static constexpr int kEpiStageBytes = 4 * 32 * (32 + 4) * 4;  // store staging, 4 warps
+  // epilogue staging (after the stages, so 1024-byte aligned), 4 warps: padded
+  // rows of 36 floats, or a 4 KiB swizzled TMA store box each
+  static constexpr int kEpiStageBytes = 4 * 32 * (32 + 4) * 4;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes + kEpiStageBytes;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static_assert((2 * kStages + 5) * 8 + 16 <= kBarBytes, "barrier area");
@@ -241,8 +243,9 @@ __device__ __forceinline__ void tc2_mma(const TcArgs& args, uint8_t* sA, uint8_t
 // all halves in ascending pair (= k) order, its own from TMEM in place, and
 // stores the result: the sum is the same whichever pair arrives last.
 template <bool OUT_F16>
-__device__ __forceinline__ void tc2_split_half(const TcArgs& args, float* sw, uint32_t taddr,
-                                               int row, int32_t mm, int32_t nbase, const Unit& u,
+__device__ __forceinline__ void tc2_split_half(const TcArgs& args, const CUtensorMap* tmC,
+                                               uint8_t* stage, uint32_t taddr, int row,
+                                               int32_t mm, int32_t nbase, const Unit& u,
                                                uint32_t rank, int32_t cluster_id,
                                                volatile int* last_flag) {
   const WorkSpec& W = args.work;
@@ -318,7 +321,7 @@ __device__ __forceinline__ void tc2_split_half(const TcArgs& args, float* sw, ui
         }
       }
     }
-    store_rows_staged<CW, OUT_F16>(args, sw, mm - (row & 31), row & 31, nbase + c * CW, acc);
+    store_out<CW, OUT_F16, false>(args, tmC, stage, row >> 5, mm, row & 31, nbase + c * CW, acc);
   }
   if (threadIdx.x == 64) atomicExch(ticket, 0);  // ready for the next launch
 }
@@ -329,13 +332,12 @@ __device__ __forceinline__ void tc2_epilogue(const TcArgs& args, uint64_t* acc_f
                                              uint64_t* acc_empty, const WaitCtl& wc,
                                              uint32_t tmem_base, uint32_t rank,
                                              int32_t cluster_id, volatile int* last_flag,
-                                             float* stage) {
+                                             uint8_t* stage, const CUtensorMap* tmC) {
   const WorkSpec& W = args.work;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int q = warp & 3;  // TMEM lane quarter this warp may access
   const int row = q * 32 + lane;
-  float* sw = stage + q * 32 * (32 + 4);  // this warp's store staging block
   const uint32_t leader_empty0 = map_to_rank(smem_u32(&acc_empty[0]), 0);
   const uint32_t leader_empty1 = map_to_rank(smem_u32(&acc_empty[1]), 0);
   WorkIter it;
@@ -361,10 +363,11 @@ __device__ __forceinline__ void tc2_epilogue(const TcArgs& args, uint64_t* acc_f
         float v[32];
         __syncwarp();
         tmem_load_chunk<32>(taddr + c * 32, v);
-        store_rows_staged<32, OUT_F16>(args, sw, mm - lane, lane, nbase + c * 32, v);
+        store_out<32, OUT_F16, false>(args, tmC, stage, q, mm, lane, nbase + c * 32, v);
       }
     } else {
-      tc2_split_half<OUT_F16>(args, sw, taddr, row, mm, nbase, u, rank, cluster_id, last_flag);
+      tc2_split_half<OUT_F16>(args, tmC, stage, taddr, row, mm, nbase, u, rank, cluster_id,
+                              last_flag);
     }
     tc_fence_before();
     __syncwarp();
@@ -374,6 +377,9 @@ __device__ __forceinline__ void tc2_epilogue(const TcArgs& args, uint64_t* acc_f
       aph ^= 1;
     }
   }
+  // every bulk store this warp issued has landed before the CTA moves on
+  if (args.c_tma && lane == 0) bulk_wait_all();
+  __syncwarp();
   if (threadIdx.x == 64) {
     trace_mark(args, blockIdx.x, kTraceEnd);
     if (args.trace) args.trace[size_t(blockIdx.x) * kTraceSlots + kTraceUnits] = uint64_t(units);
@@ -384,7 +390,8 @@ __device__ __forceinline__ void tc2_epilogue(const TcArgs& args, uint64_t* acc_f
 template <bool OUT_F16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                    const __grid_constant__ CUtensorMap tmB, const TcArgs args) {
+                    const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC, const TcArgs args) {
   using Cfg = Tc2Config;
   constexpr int S = Cfg::kStages;
 
@@ -394,7 +401,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + S * Cfg::kABytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * Cfg::kBBytes);
+  uint8_t* stage = sB + S * Cfg::kBBytes;  // epilogue staging, 1024-byte aligned
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stage + Cfg::kEpiStageBytes);
   uint64_t* full = bars;               // leader's counts both CTAs' bytes
   uint64_t* empty = bars + S;          // one multicast commit per phase, in both CTAs
   uint64_t* acc_full = bars + 2 * S;   // one multicast commit per unit, in both CTAs
@@ -426,6 +434,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmB);
+    if (args.c_tma) tma_prefetch_map(&tmC);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_slot), Cfg::kTmemCols);
@@ -452,9 +461,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
                  cluster_id);
   } else {
     tc2_epilogue<OUT_F16>(args, acc_full, acc_empty, wc, tmem_base, rank, cluster_id,
-                          last_flag,
-                          reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) +
-                                                   Cfg::kBarBytes));
+                          last_flag, stage, &tmC);
   }
 
   __syncthreads();

@@ -53,8 +53,11 @@ struct TcConfig {
   static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;  // power of two >= 32
   static constexpr int kChunk = BN < 32 ? BN : 32;             // TMEM columns per load
   static constexpr int kBarBytes = 256;
-  // epilogue staging: per epilogue warp 32 rows of kChunk + 4 floats
+  // epilogue staging (after the stages, so 1024-byte aligned): per epilogue
+  // warp 32 rows of kChunk + 4 floats, or a 4 KiB swizzled TMA store box
   static constexpr int kEpiStageBytes = 4 * 32 * (kChunk + 4) * 4;
+  static_assert(kEpiStageBytes % 1024 == 0 && (kChunk != 32 || kEpiStageBytes >= 4 * 4096),
+                "staging area");
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes + kEpiStageBytes;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128");
@@ -72,6 +75,7 @@ struct TcArgs {
   int* status;            // device status word
   uint64_t wait_limit_ns;
   int32_t a_mn, b_mn;     // operand majors in the MMA view (1 = MN-major)
+  int32_t c_tma = 0;      // 1: row-major C chunks leave by TMA store (tmC is valid)
   uint32_t idesc;         // tcgen05 instruction descriptor
   uint64_t* trace = nullptr;  // NULL, or kTraceSlots %globaltimer stamps per CTA
 };
@@ -284,26 +288,102 @@ __device__ __forceinline__ void store_rows_staged(const TcArgs& a, float* sw, in
     if (valid > 2) b4.z = __ldg(a.bias + nn + 2);
     if (valid > 3) b4.w = __ldg(a.bias + nn + 3);
   }
+  // All shared reads first, then all global stores: a store through the
+  // generic C pointer could alias the staging block as far as the compiler
+  // knows, so interleaving them would serialise every read behind the store
+  // before it.
+  constexpr int kPasses = 32 / RPI;
+  float4 x[kPasses];
 #pragma unroll
-  for (int it = 0; it < 32 / RPI; ++it) {
-    const int r = it * RPI + lane / Q;
-    const int32_t mm = mrow0 + r;
-    if (mm >= a.Mm || valid <= 0) continue;
-    float4 x = *reinterpret_cast<const float4*>(sw + r * LD + 4 * c4);
-    x.x += b4.x; x.y += b4.y; x.z += b4.z; x.w += b4.w;
-    put4<OUT_F16>(a, int64_t(mm) * a.ldc + nn, x, valid);
+  for (int it = 0; it < kPasses; ++it)
+    x[it] = *reinterpret_cast<const float4*>(sw + (it * RPI + lane / Q) * LD + 4 * c4);
+  if (valid <= 0) return;
+#pragma unroll
+  for (int it = 0; it < kPasses; ++it) {
+    const int32_t mm = mrow0 + it * RPI + lane / Q;
+    if (mm >= a.Mm) continue;
+    float4 y = x[it];
+    y.x += b4.x; y.y += b4.y; y.z += b4.z; y.w += b4.w;
+    put4<OUT_F16>(a, int64_t(mm) * a.ldc + nn, y, valid);
+  }
+}
+
+// Row-major store of one epilogue warp's 32 rows x 32 columns by TMA: lane i
+// writes row mrow0 + i (bias added, rounded once to the output type) into the
+// warp's 4 KiB box in shared memory, in the layout the tensor map's swizzle
+// expects (128-byte rows for fp32, 16-byte piece k at k ^ (row % 8); 64-byte
+// rows for fp16, piece k at k ^ ((row / 2) % 4)), which also keeps the shared
+// stores free of bank conflicts; lane 0 then issues one bulk store of the box.
+// Rows and columns past the matrix are dropped by the TMA unit.  The box is
+// reused only after the previous bulk store from it has read it.
+template <bool OUT_F16>
+__device__ __forceinline__ void store_rows_tma(const CUtensorMap* tmC, const TcArgs& a,
+                                               uint8_t* box, int32_t mrow0, int lane,
+                                               int32_t nn0, const float (&v)[32]) {
+  if (mrow0 >= a.Mm || nn0 >= a.Nm) return;  // the same for the whole warp
+  if (lane == 0) bulk_wait_read_all();
+  __syncwarp();
+  float o[32];
+  const float* bp = a.bias ? a.bias + nn0 : nullptr;
+  if (bp && nn0 + 32 <= a.Nm && (reinterpret_cast<uintptr_t>(bp) & 15) == 0) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+      const float4 b4 = __ldg(reinterpret_cast<const float4*>(bp + j));
+      o[j] = v[j] + b4.x; o[j + 1] = v[j + 1] + b4.y;
+      o[j + 2] = v[j + 2] + b4.z; o[j + 3] = v[j + 3] + b4.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) o[j] = v[j] + ((bp && nn0 + j < a.Nm) ? __ldg(bp + j) : 0.f);
+  }
+  const uint32_t base = smem_u32(box);
+  if constexpr (OUT_F16) {
+    const uint32_t row = base + uint32_t(lane) * 64u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t h[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half2 p = __floats2half2_rn(o[8 * k + 2 * i], o[8 * k + 2 * i + 1]);
+        h[i] = *reinterpret_cast<const uint32_t*>(&p);
+      }
+      st_shared_v4(row + uint32_t((k ^ ((lane >> 1) & 3)) * 16), h[0], h[1], h[2], h[3]);
+    }
+  } else {
+    const uint32_t row = base + uint32_t(lane) * 128u;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      st_shared_v4(row + uint32_t((k ^ (lane & 7)) * 16), __float_as_uint(o[4 * k]),
+                   __float_as_uint(o[4 * k + 1]), __float_as_uint(o[4 * k + 2]),
+                   __float_as_uint(o[4 * k + 3]));
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmC, base, nn0, mrow0);
+    bulk_commit_group();
   }
 }
 
 // Any store of an epilogue chunk: transposed stores are already coalesced
-// (lanes are consecutive columns of C); row-major ones go through staging.
+// (lanes are consecutive columns of C); row-major ones leave by TMA store when
+// the launch set one up (32-column chunks), else through the padded staging.
 template <int CW, bool OUT_F16, bool TRANS>
-__device__ __forceinline__ void store_out(const TcArgs& a, float* sw, int32_t mm, int lane,
+__device__ __forceinline__ void store_out(const TcArgs& a, const CUtensorMap* tmC,
+                                          uint8_t* stage, int q, int32_t mm, int lane,
                                           int32_t nn0, const float (&v)[CW]) {
-  if constexpr (TRANS)
+  if constexpr (TRANS) {
     store_chunk<CW, OUT_F16, TRANS>(a, mm, nn0, v);
-  else
-    store_rows_staged<CW, OUT_F16>(a, sw, mm - lane, lane, nn0, v);
+  } else if constexpr (CW == 32) {
+    if (a.c_tma)
+      store_rows_tma<OUT_F16>(tmC, a, stage + q * 4096, mm - lane, lane, nn0, v);
+    else
+      store_rows_staged<CW, OUT_F16>(a, reinterpret_cast<float*>(stage) + q * 32 * (CW + 4),
+                                     mm - lane, lane, nn0, v);
+  } else {
+    store_rows_staged<CW, OUT_F16>(a, reinterpret_cast<float*>(stage) + q * 32 * (CW + 4),
+                                   mm - lane, lane, nn0, v);
+  }
 }
 
 // Cluster split: after every CTA of the cluster parked its fp32 partial of the
@@ -394,7 +474,8 @@ __device__ __forceinline__ void csplit_reduce(const TcArgs& a, const uint8_t* sm
 template <int BN, bool OUT_F16, bool TRANS>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                   const __grid_constant__ CUtensorMap tmB, const TcArgs args) {
+                   const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const TcArgs args) {
   using Cfg = TcConfig<BN>;
   constexpr int S = Cfg::kStages;
   constexpr int CW = Cfg::kChunk;
@@ -405,7 +486,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;                         // S x 16 KiB
   uint8_t* sB = smem + S * Cfg::kABytes;      // S x BN*128 B
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * Cfg::kBBytes);
+  uint8_t* stage = sB + S * Cfg::kBBytes;     // epilogue staging, 1024-byte aligned
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stage + Cfg::kEpiStageBytes);
   uint64_t* full = bars;                      // TMA bytes landed in stage s
   uint64_t* empty = bars + S;                 // MMAs reading stage s are done
   uint64_t* acc_full = bars + 2 * S;          // accumulator b finished
@@ -435,6 +517,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmB);
+    if (args.c_tma) tma_prefetch_map(&tmC);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
@@ -572,9 +655,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;     // accumulator row inside the tile
     const int et = threadIdx.x - 64;   // 0..127
-    // this warp's store staging block (after the barrier area)
-    float* sw = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + Cfg::kBarBytes) +
-                q * 32 * (CW + 4);
     WorkIter it;
     it.init(W, blockIdx.x);
     Unit u;
@@ -621,7 +701,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           float v[CW];
           __syncwarp();
           tmem_load_chunk<CW>(taddr + c * CW, v);
-          store_out<CW, OUT_F16, TRANS>(args, sw, mm, lane, nbase + c * CW, v);
+          store_out<CW, OUT_F16, TRANS>(args, &tmC, stage, q, mm, lane, nbase + c * CW, v);
         }
       } else {
         const int32_t st = u.tile - W.dp_tiles;  // split-tile index
@@ -700,7 +780,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
               }
             }
-            store_out<CW, OUT_F16, TRANS>(args, sw, mm, lane, nbase + c * CW, acc);
+            store_out<CW, OUT_F16, TRANS>(args, &tmC, stage, q, mm, lane, nbase + c * CW,
+                                          acc);
           }
           if (et == 0) atomicExch(&args.tickets[st], 0);  // ready for the next launch
         }
@@ -712,6 +793,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         aph ^= 1;
       }
     }
+    // every bulk store this warp issued has landed before the CTA moves on
+    if (args.c_tma && lane == 0) bulk_wait_all();
+    __syncwarp();
     if (et == 0) {
       trace_mark(args, blockIdx.x, kTraceEnd);
       if (args.trace) args.trace[size_t(blockIdx.x) * kTraceSlots + kTraceUnits] = uint64_t(units);

@@ -40,7 +40,7 @@ cudaError_t launch_tc_inst(const TcLaunch& L) {
   cfg.stream = L.stream;
   cfg.attrs = attr;
   cfg.numAttrs = unsigned(n);
-  return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.args);
+  return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.tmC, L.args);
 }
 
 // Clusters of `s` CTAs of this instantiation that fit on the device at once.

@@ -116,10 +116,13 @@ enum {
   GEMM_OPT_PDL = 9,              /* 1 (default): tensor-core kernels are launched so their
                                     prologue may overlap the previous kernel on the stream;
                                     they touch global memory only after it completed. 0: off */
-  GEMM_OPT_PAIR_SPLIT = 10       /* two-SM kernel: -1 (default) or 0 whole tiles only;
+  GEMM_OPT_PAIR_SPLIT = 10,      /* two-SM kernel: -1 (default) or 0 whole tiles only;
                                     1 every tile's k-blocks split evenly over the pairs
                                     (Stream-K); 2 the part-empty last wave of pair tiles and
                                     the wave before it split evenly over the pairs */
+  GEMM_OPT_TMA_STORE = 11        /* 1 (default): row-major output tiles leave the tensor-core
+                                    kernels by TMA store when C is 16-byte aligned with a row
+                                    pitch that is a multiple of 16 bytes; 0: plain stores */
 };
 
 /* Creates a handle on CUDA device `device`.  Allocates, on that device, the

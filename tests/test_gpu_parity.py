@@ -63,6 +63,26 @@ def test_tc_layouts_ragged(g, dev, kernel, am, bm, odt, bias):
     full_check(g, dev, p)
 
 
+@pytest.mark.parametrize("kernel", [TC, SK, TC2])
+@pytest.mark.parametrize("odt", [F16, F32])
+def test_plain_store_path(g, dev, kernel, odt):
+    """The epilogue's plain-store path on an output the TMA could take
+    (GEMM_OPT_TMA_STORE = 0): same results as the TMA-store path."""
+    set_opts(g, kernel=kernel, tma_store=0)
+    p = problem(296, 520, 200, 0, 1, F16, odt, True, 160 + (odt == F32))
+    full_check(g, dev, p)
+
+
+@pytest.mark.parametrize("kernel", [TC, TC2])
+@pytest.mark.parametrize("odt", [F16, F32])
+def test_output_pitch_not_16_bytes(g, dev, kernel, odt):
+    """C rows of 536 or 1064 bytes: no TMA store; the plain stores write C."""
+    N = 268 if odt == F16 else 266
+    set_opts(g, kernel=kernel)
+    p = problem(300, N, 200, 0, 1, F16, odt, True, 165 + (odt == F32))
+    full_check(g, dev, p)
+
+
 @pytest.mark.parametrize("tile_n", [128, 256])
 @pytest.mark.parametrize("kernel", [TC, SK])
 def test_tc_tile_widths(g, dev, tile_n, kernel):
