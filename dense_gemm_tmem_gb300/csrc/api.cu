@@ -745,6 +745,10 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value) {
       if (value > 1) return GEMM_ERR_INVALID_ARG;
       o.tma_store = value < 0 ? d.tma_store : int(value);
       return GEMM_OK;
+    case GEMM_OPT_BIAS_INIT:
+      if (value > 1) return GEMM_ERR_INVALID_ARG;
+      o.bias_init = value < 0 ? d.bias_init : int(value);
+      return GEMM_OK;
     default:
       return GEMM_ERR_INVALID_ARG;
   }
@@ -847,6 +851,7 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, co
              dg::encode_output(h, &L.tmC, C, M, N, layout.out_dtype == GEMM_F16))
                 ? 1
                 : 0;
+  a.bias_init = (h->opt.bias_init && bias) ? 1 : 0;
   // phase stamps only if the caller's buffer holds one row per CTA
   a.trace = (h->trace && h->trace_ctas >= plan.grid) ? h->trace : nullptr;
   a.idesc = dg::make_idesc_f16(pair ? dg::kPairBM : dg::kBM, plan.tile_n, plan.a_mn_major,

@@ -26,6 +26,7 @@ struct Options {
   int pdl = 1;             // programmatic dependent launch of the tensor-core kernels
   int pair_split = -1;     // two-SM kernel k-split: -1/0 none, 1 all tiles, 2 the tail
   int tma_store = 1;       // epilogue output by TMA store where C allows it
+  int bias_init = 0;       // seed the accumulators with the bias
   int csplit_clusters[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};  // clusters of s resident (0: SMs/s)
   int simt_per_sm = 0;     // 128 x 128 CUDA-core CTAs resident per SM (0: 2); set per device
   uint64_t wait_limit_ns = 2000000000ull;

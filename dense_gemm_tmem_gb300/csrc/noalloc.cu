@@ -197,5 +197,6 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
   a.trace = nullptr;
   std::memset(&L.tmC, 0, sizeof(L.tmC));
   a.c_tma = 0;  // plain stores: no output tensor map to encode and keep
+  a.bias_init = 0;
   return launch_tc(L) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }

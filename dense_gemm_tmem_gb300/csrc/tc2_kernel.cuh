@@ -194,12 +194,15 @@ __device__ __forceinline__ void tc2_mma(const TcArgs& args, uint8_t* sA, uint8_t
   const uint32_t a_step = args.a_mn ? (2048u >> 4) : (32u >> 4);
   const uint32_t b_step = args.b_mn ? (2048u >> 4) : (32u >> 4);
   while (ok && it.next(W, u)) {
-    if (!wait_bounded(smem_u32(&acc_empty[b]), aph ^ 1, wc, kSiteMmaAccum)) {
+    // both CTAs' epilogues release each buffer once before its first use
+    // (after seeding it, if asked) and once after each drain
+    if (!wait_bounded(smem_u32(&acc_empty[b]), aph, wc, kSiteMmaAccum)) {
       ok = false;
       break;
     }
     tc_fence_after();
     const uint32_t d_tmem = tmem_base + uint32_t(b * kPairBN);
+    const bool seeded = args.bias_init && u.kb0 == 0;  // accumulate onto the bias
     for (int32_t kb = u.kb0; kb < u.kb1; ++kb) {
       if (!wait_bounded(smem_u32(&full[s]), ph, wc, kSiteMmaFull)) {
         ok = false;
@@ -212,7 +215,7 @@ __device__ __forceinline__ void tc2_mma(const TcArgs& args, uint8_t* sA, uint8_t
 #pragma unroll
       for (int kk = 0; kk < kBK / 16; ++kk)
         tc_mma_f16_pair(d_tmem, adesc + uint64_t(kk * a_step), bdesc + uint64_t(kk * b_step),
-                        args.idesc, (kb > u.kb0 || kk > 0) ? 1u : 0u);
+                        args.idesc, (kb > u.kb0 || kk > 0 || seeded) ? 1u : 0u);
       any = true;
       tc_commit_pair_both(smem_u32(&empty[s]));
       if (++s == S) {
@@ -340,9 +343,26 @@ __device__ __forceinline__ void tc2_epilogue(const TcArgs& args, uint64_t* acc_f
   const int row = q * 32 + lane;
   const uint32_t leader_empty0 = map_to_rank(smem_u32(&acc_empty[0]), 0);
   const uint32_t leader_empty1 = map_to_rank(smem_u32(&acc_empty[1]), 0);
-  WorkIter it;
+  // `ahead` runs two units ahead of `it`: the unit that will next use the
+  // buffer just drained, which is seeded with the bias before its release
+  WorkIter it, ahead;
   it.init(W, cluster_id);
-  Unit u;
+  ahead.init(W, cluster_id);
+  Unit u, un;
+  auto release = [&](int buf, bool have_next) {
+    if (have_next && args.bias_init && un.kb0 == 0) {
+      int32_t tm2, tn2;
+      tile_coords(W, un.tile, tm2, tn2);
+      seed_bias<kPairBN, 32, false>(
+          args, tmem_base + (uint32_t(q * 32) << 16) + uint32_t(buf * kPairBN),
+          tm2 * kPairBM + int32_t(rank) * kBM + row, tn2 * kPairBN);
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cluster(buf == 0 ? leader_empty0 : leader_empty1);
+  };
+  release(0, ahead.next(W, un));
+  release(1, ahead.next(W, un));
   int b = 0;
   uint32_t aph = 0;
   int units = 0;
@@ -369,9 +389,7 @@ __device__ __forceinline__ void tc2_epilogue(const TcArgs& args, uint64_t* acc_f
       tc2_split_half<OUT_F16>(args, tmC, stage, taddr, row, mm, nbase, u, rank, cluster_id,
                               last_flag);
     }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive_cluster(b == 0 ? leader_empty0 : leader_empty1);
+    release(b, ahead.next(W, un));
     if (++b == 2) {
       b = 0;
       aph ^= 1;

@@ -76,6 +76,7 @@ struct TcArgs {
   uint64_t wait_limit_ns;
   int32_t a_mn, b_mn;     // operand majors in the MMA view (1 = MN-major)
   int32_t c_tma = 0;      // 1: row-major C chunks leave by TMA store (tmC is valid)
+  int32_t bias_init = 0;  // 1: each tile's k-block-0 accumulator is seeded with the bias
   uint32_t idesc;         // tcgen05 instruction descriptor
   uint64_t* trace = nullptr;  // NULL, or kTraceSlots %globaltimer stamps per CTA
 };
@@ -99,6 +100,12 @@ enum TracePhase : int {
 
 __device__ __forceinline__ void trace_mark(const TcArgs& a, uint32_t cta, int phase) {
   if (a.trace) a.trace[size_t(cta) * kTraceSlots + phase] = globaltimer_ns();
+}
+
+// The bias the output stores add: none when the accumulators were seeded
+// with it (it is then already in the sum exactly once per tile).
+__device__ __forceinline__ const float* out_bias(const TcArgs& a) {
+  return a.bias_init ? nullptr : a.bias;
 }
 
 __device__ __forceinline__ void epi_bar_sync() {
@@ -144,6 +151,36 @@ __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float (&v)[CW]) 
   }
 }
 
+// Seeds one accumulator buffer with the bias before the first MMA of a unit
+// that starts at k-block 0 (the reduction then starts from the bias instead
+// of zero: the FuseReductionEpilogue reading of the kimm240.github.io/tvm
+// series).  `taddr` addresses this warp's 32-lane quarter of the buffer; lane
+// `row` of it is output row mm (MMA view), columns nbase ... nbase + BN - 1.
+// Not TRANS: every row of column n holds bias[n]; TRANS (C stored
+// transposed): every column of row mm holds bias[mm].  0 outside the matrix.
+template <int BN, int CW, bool TRANS>
+__device__ __forceinline__ void seed_bias(const TcArgs& a, uint32_t taddr, int32_t mm,
+                                          int32_t nbase) {
+  static_assert(CW == 32 || CW == 16, "chunk width");
+  const float rowv = (TRANS && mm < a.Mm) ? __ldg(a.bias + mm) : 0.f;
+#pragma unroll 1
+  for (int c = 0; c < BN / CW; ++c) {
+    uint32_t r[CW];
+#pragma unroll
+    for (int j = 0; j < CW; ++j) {
+      const int32_t n = nbase + c * CW + j;
+      const float v = TRANS ? rowv : (n < a.Nm ? __ldg(a.bias + n) : 0.f);
+      r[j] = __float_as_uint(v);
+    }
+    __syncwarp();
+    if constexpr (CW == 32)
+      tmem_st32(taddr + c * CW, r);
+    else
+      tmem_st16(taddr + c * CW, r);
+  }
+  tmem_wait_st();
+}
+
 // Writes one chunk of CW accumulator columns held by this thread.
 // Not TRANS: C[mm][nn0 + j] = v[j] + bias[nn0 + j]  (thread = output row).
 // TRANS:     C[nn0 + j][mm] = v[j] + bias[mm]       (thread = output column).
@@ -154,7 +191,8 @@ __device__ __forceinline__ void store_chunk(const TcArgs& a, int32_t mm, int32_t
   const int32_t ncols = (a.Nm - nn0) < CW ? (a.Nm - nn0) : CW;
   if constexpr (!TRANS) {
     float o[CW];
-    const float* bp = a.bias ? a.bias + nn0 : nullptr;
+    const float* ob = out_bias(a);
+    const float* bp = ob ? ob + nn0 : nullptr;
     const bool full = ncols == CW;
     if (bp && full && (reinterpret_cast<uintptr_t>(bp) & 15) == 0) {
 #pragma unroll
@@ -201,7 +239,8 @@ __device__ __forceinline__ void store_chunk(const TcArgs& a, int32_t mm, int32_t
       }
     }
   } else {
-    const float bv = a.bias ? __ldg(a.bias + mm) : 0.f;
+    const float* ob = out_bias(a);
+    const float bv = ob ? __ldg(ob + mm) : 0.f;
 #pragma unroll
     for (int j = 0; j < CW; ++j) {
       if (j < ncols) {
@@ -282,11 +321,12 @@ __device__ __forceinline__ void store_rows_staged(const TcArgs& a, float* sw, in
   const int32_t nn = nn0 + 4 * c4;
   const int valid = min(4, a.Nm - nn);
   float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (a.bias && valid > 0) {
-    b4.x = __ldg(a.bias + nn);
-    if (valid > 1) b4.y = __ldg(a.bias + nn + 1);
-    if (valid > 2) b4.z = __ldg(a.bias + nn + 2);
-    if (valid > 3) b4.w = __ldg(a.bias + nn + 3);
+  const float* ob = out_bias(a);
+  if (ob && valid > 0) {
+    b4.x = __ldg(ob + nn);
+    if (valid > 1) b4.y = __ldg(ob + nn + 1);
+    if (valid > 2) b4.z = __ldg(ob + nn + 2);
+    if (valid > 3) b4.w = __ldg(ob + nn + 3);
   }
   // All shared reads first, then all global stores: a store through the
   // generic C pointer could alias the staging block as far as the compiler
@@ -324,7 +364,8 @@ __device__ __forceinline__ void store_rows_tma(const CUtensorMap* tmC, const TcA
   if (lane == 0) bulk_wait_read_all();
   __syncwarp();
   float o[32];
-  const float* bp = a.bias ? a.bias + nn0 : nullptr;
+  const float* ob = out_bias(a);
+  const float* bp = ob ? ob + nn0 : nullptr;
   if (bp && nn0 + 32 <= a.Nm && (reinterpret_cast<uintptr_t>(bp) & 15) == 0) {
 #pragma unroll
     for (int j = 0; j < 32; j += 4) {
@@ -409,6 +450,7 @@ __device__ __forceinline__ void csplit_reduce(const TcArgs& a, const uint8_t* sm
 #pragma unroll
   for (int j = 0; j < 8; ++j) peer[j] = j < s ? map_to_rank(local, uint32_t(j)) : 0u;
   const int groups = TRANS ? BN * (R / 4) : R * (BN / 4);
+  const float* ob = out_bias(a);
   constexpr int kU = 4;
 #pragma unroll 1
   for (int g0 = tid; g0 < groups; g0 += kU * nthreads) {
@@ -449,21 +491,21 @@ __device__ __forceinline__ void csplit_reduce(const TcArgs& a, const uint8_t* sm
       if constexpr (!TRANS) {
         if (mm >= a.Mm || nn >= a.Nm) continue;
         const int valid = min(4, a.Nm - nn);
-        if (a.bias) {
-          acc.x += __ldg(a.bias + nn);
-          if (valid > 1) acc.y += __ldg(a.bias + nn + 1);
-          if (valid > 2) acc.z += __ldg(a.bias + nn + 2);
-          if (valid > 3) acc.w += __ldg(a.bias + nn + 3);
+        if (ob) {
+          acc.x += __ldg(ob + nn);
+          if (valid > 1) acc.y += __ldg(ob + nn + 1);
+          if (valid > 2) acc.z += __ldg(ob + nn + 2);
+          if (valid > 3) acc.w += __ldg(ob + nn + 3);
         }
         put4<OUT_F16>(a, int64_t(mm) * a.ldc + nn, acc, valid);
       } else {
         if (mm >= a.Mm || nn >= a.Nm) continue;
         const int valid = min(4, a.Mm - mm);
-        if (a.bias) {
-          acc.x += __ldg(a.bias + mm);
-          if (valid > 1) acc.y += __ldg(a.bias + mm + 1);
-          if (valid > 2) acc.z += __ldg(a.bias + mm + 2);
-          if (valid > 3) acc.w += __ldg(a.bias + mm + 3);
+        if (ob) {
+          acc.x += __ldg(ob + mm);
+          if (valid > 1) acc.y += __ldg(ob + mm + 1);
+          if (valid > 2) acc.z += __ldg(ob + mm + 2);
+          if (valid > 3) acc.w += __ldg(ob + mm + 3);
         }
         put4<OUT_F16>(a, int64_t(nn) * a.ldc + mm, acc, valid);
       }
@@ -610,12 +652,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t a_step = args.a_mn ? (2048u >> 4) : (32u >> 4);
       const uint32_t b_step = args.b_mn ? (2048u >> 4) : (32u >> 4);
       while (ok && it.next(W, u)) {
-        if (!wait_bounded(smem_u32(&acc_empty[b]), aph ^ 1, wc, kSiteMmaAccum)) {
+        // the epilogue releases each buffer once before its first use (after
+        // seeding it, if asked) and once after each drain
+        if (!wait_bounded(smem_u32(&acc_empty[b]), aph, wc, kSiteMmaAccum)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(b * BN);
+        const bool seeded = args.bias_init && u.kb0 == 0;  // accumulate onto the bias
         for (int32_t kb = u.kb0; kb < u.kb1; ++kb) {
           if (!wait_bounded(smem_u32(&full[s]), ph, wc, kSiteMmaFull)) {
             ok = false;
@@ -628,7 +673,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             tc_mma_f16(d_tmem, adesc + uint64_t(kk * a_step), bdesc + uint64_t(kk * b_step),
-                       args.idesc, (kb > u.kb0 || kk > 0) ? 1u : 0u);
+                       args.idesc, (kb > u.kb0 || kk > 0 || seeded) ? 1u : 0u);
           any = true;
           tc_commit(smem_u32(&empty[s]));
           if (++s == S) {
@@ -655,9 +700,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;     // accumulator row inside the tile
     const int et = threadIdx.x - 64;   // 0..127
-    WorkIter it;
+    // `ahead` runs two units ahead of `it`: the unit that will next use the
+    // buffer just drained, which is seeded with the bias before its release
+    WorkIter it, ahead;
     it.init(W, blockIdx.x);
-    Unit u;
+    ahead.init(W, blockIdx.x);
+    Unit u, un;
+    auto release = [&](int buf, bool have_next) {
+      if (have_next && args.bias_init && un.kb0 == 0) {
+        int32_t tm2, tn2;
+        tile_coords(W, un.tile, tm2, tn2);
+        seed_bias<BN, CW, TRANS>(args, tmem_base + (uint32_t(q * 32) << 16) + uint32_t(buf * BN),
+                                 tm2 * kBM + row, tn2 * BN);
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&acc_empty[buf]));
+    };
+    release(0, ahead.next(W, un));
+    release(1, ahead.next(W, un));
     int b = 0;
     uint32_t aph = 0;
     int units = 0;
@@ -786,8 +846,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (et == 0) atomicExch(&args.tickets[st], 0);  // ready for the next launch
         }
       }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&acc_empty[b]));
+      release(b, ahead.next(W, un));
       if (++b == 2) {
         b = 0;
         aph ^= 1;

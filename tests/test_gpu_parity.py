@@ -63,6 +63,39 @@ def test_tc_layouts_ragged(g, dev, kernel, am, bm, odt, bias):
     full_check(g, dev, p)
 
 
+@pytest.mark.parametrize("case", [
+    ("tc", 296, 520, 200, 0, 1, {"kernel": TC}),
+    ("tc_persistent", 600, 1000, 328, 1, 0, {"kernel": TC, "grid": 5}),
+    ("streamk", 392, 600, 1480, 0, 1, {"kernel": SK, "grid": 37}),
+    ("pair", 520, 776, 1032, 0, 0, {"kernel": TC2}),
+    ("pair_persistent", 1000, 1000, 1480, 0, 1, {"kernel": TC2, "grid": 6}),
+    ("pair_split", 520, 776, 2056, 0, 1, {"kernel": TC2, "pair_split": 1, "grid": 14}),
+    ("csplit", 296, 520, 2048, 0, 1, {"kernel": SPLITC, "csplit": 4}),
+    ("swapped", 16, 2048, 4096, 0, 0, {}),
+    ("swapped_sk", 40, 3000, 1000, 0, 1, {"kernel": SK, "swap": 1, "grid": 29}),
+])
+@pytest.mark.parametrize("odt", [F16, F32])
+def test_bias_as_reduction_init(g, dev, case, odt):
+    """GEMM_OPT_BIAS_INIT: each tile's reduction starts from the bias seeded
+    into the accumulator (split tiles: only the k-block-0 part carries it)."""
+    name, M, N, K, am, bm, opts = case
+    set_opts(g, bias_init=1, **opts)
+    p = problem(M, N, K, am, bm, F16, odt, True, 200 + len(name) + (odt == F32))
+    full_check(g, dev, p)
+
+
+def test_bias_as_reduction_init_exact(g, dev):
+    """Integer-valued inputs and bias: seeding the reduction with the bias
+    gives the same exact values as adding it last."""
+    for opts in ({"kernel": TC}, {"kernel": SK, "grid": 23}, {"kernel": TC2},
+                 {"kernel": SPLITC, "csplit": 8}):
+        set_opts(g, bias_init=1, **opts)
+        p = problem(384, 520, 1024, 0, 1, F16, F32, True, 210, kind="int")
+        ref = oracle.gemm(p.A, p.B, p.bias, b_major=1)
+        assert np.array_equal(as_f64(run(g, p, dev)), ref)
+        reset_opts(g)
+
+
 @pytest.mark.parametrize("kernel", [TC, SK, TC2])
 @pytest.mark.parametrize("odt", [F16, F32])
 def test_plain_store_path(g, dev, kernel, odt):
