@@ -143,5 +143,7 @@ WORKLOADS = {
         Workload("gemm16384_f16_f16out", 16384, 16384, 16384, ROW, ROW, F16, F16,
                  "uniform", False, 5,
                  "M=N=K=16384 fp16 row-major A and B, U[-1,1], fp16 output"),
+        Workload("tile128_f16_f32out", 128, 128, 64, ROW, COL, F16, F32, "uniform", False, 6,
+                 "one 128 x 128 output tile with K=64 (one k-block): the fixed cost of a launch"),
     ]
 }

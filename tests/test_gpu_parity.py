@@ -513,6 +513,11 @@ def test_workload_512_full(g, dev):
     full_check(g, dev, p)
 
 
+def test_workload_tile128_full(g, dev):
+    p = inputs.WORKLOADS["tile128_f16_f32out"].make()
+    full_check(g, dev, p)
+
+
 def test_workload_sgemm2048_full(g, dev):
     p = inputs.WORKLOADS["sgemm2048_f32"].make()
     pl = g.plan(2048, 2048, 2048, 0, 0, B.GEMM_F32, B.GEMM_F32)
