@@ -68,6 +68,7 @@ cudaError_t launch_tc(const TcLaunch& L);
 cudaError_t launch_tc_n256(const TcLaunch& L);
 cudaError_t launch_tc_n128(const TcLaunch& L);
 cudaError_t launch_tc_small(const TcLaunch& L);
+cudaError_t launch_tc_narrow(const TcLaunch& L);
 // Two-SM kernel (tc2.cu): even grid, not swapped, whole 256 x 256 tiles.
 cudaError_t launch_tc2(const TcLaunch& L);
 // Clusters of two that fit on the device at once (-1 if the query fails).

@@ -144,6 +144,6 @@ WORKLOADS = {
                  "uniform", False, 5,
                  "M=N=K=16384 fp16 row-major A and B, U[-1,1], fp16 output"),
         Workload("tile128_f16_f32out", 128, 128, 64, ROW, COL, F16, F32, "uniform", False, 6,
-                 "one 128 x 128 output tile with K=64 (one k-block): the fixed cost of a launch"),
+                 "a 128 x 128 output with K=64 (one k-block): the fixed cost of a launch"),
     ]
 }

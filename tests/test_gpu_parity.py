@@ -116,6 +116,18 @@ def test_output_pitch_not_16_bytes(g, dev, kernel, odt):
     full_check(g, dev, p)
 
 
+@pytest.mark.parametrize("tile_n,bm", [(32, 1), (64, 0), (64, 1)])
+@pytest.mark.parametrize("kernel", [TC, SK])
+@pytest.mark.parametrize("odt", [F16, F32])
+def test_narrow_tiles(g, dev, tile_n, bm, kernel, odt):
+    """32- and 64-column tiles without swapping (a row-major B needs 64)."""
+    set_opts(g, kernel=kernel, tile_n=tile_n)
+    p = problem(300, 520, 328, 0, bm, F16, odt, True, 220 + tile_n + bm)
+    pl = g.plan(300, 520, 328, 0, bm, B.GEMM_F16, B.GEMM_F16 if odt == F16 else B.GEMM_F32)
+    assert pl["tile_n"] == tile_n and pl["swap_ab"] == 0
+    full_check(g, dev, p)
+
+
 @pytest.mark.parametrize("tile_n", [128, 256])
 @pytest.mark.parametrize("kernel", [TC, SK])
 def test_tc_tile_widths(g, dev, tile_n, kernel):

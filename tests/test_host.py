@@ -98,13 +98,18 @@ def test_picker_pair_rule_falls_back():
 
 
 def test_picker_small_shapes():
-    # 512^3: 8 tiles of 256 would fill too few SMs -> 16 tiles of 128; 8 k-blocks
-    # each: clusters of 4 CTAs split every tile (8-CTA clusters would leave one
-    # k-block per CTA)
+    # 512^3: 8 k-blocks per tile is shallow -> 32 whole tiles 64 columns wide
     rc, p = plan(512, 512, 512)
+    assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC
+    assert (p.tile_n, p.tiles_m, p.tiles_n, p.k_iters) == (64, 4, 8, 8)
+    assert (p.grid, p.dp_tiles, p.sk_tiles, p.workspace_bytes) == (32, 32, 0, 0)
+    rc, p = plan(1024, 1024, 768)  # 12 k-blocks: still narrow whole tiles
+    assert (p.kernel, p.tile_n, p.grid) == (B.GEMM_KERNEL_TC, 64, 128)
+    # 16 k-blocks: 16 tiles of 128, clusters of 8 CTAs split every tile (2 k-blocks each)
+    rc, p = plan(512, 512, 1024)
     assert rc == 0 and p.kernel == B.GEMM_KERNEL_SPLITC
-    assert (p.tile_n, p.tiles_m, p.tiles_n, p.k_iters) == (128, 4, 4, 8)
-    assert (p.cluster_split, p.grid, p.sk_tiles, p.workspace_bytes) == (4, 64, 16, 0)
+    assert (p.tile_n, p.tiles_m, p.tiles_n, p.k_iters) == (128, 4, 4, 16)
+    assert (p.cluster_split, p.grid, p.sk_tiles, p.workspace_bytes) == (8, 128, 16, 0)
     # deep K: 16 tiles in clusters of 8
     rc, p = plan(512, 512, 8192)
     assert rc == 0 and p.kernel == B.GEMM_KERNEL_SPLITC
