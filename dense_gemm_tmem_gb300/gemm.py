@@ -22,13 +22,27 @@ def problem_dims(A: torch.Tensor, Bm: torch.Tensor, a_major: int, b_major: int):
     return int(M), int(N), int(K)
 
 
+_LAYOUTS = {}  # (a_major, b_major, in, out) -> gemm_layout_t, built once
+
+
+def _layout(a_major, b_major, in_code, out_code):
+    key = (a_major, b_major, in_code, out_code)
+    lay = _LAYOUTS.get(key)
+    if lay is None:
+        lay = _LAYOUTS[key] = B.layout(a_major, b_major, in_code, out_code)
+    return lay
+
+
 class Gemm:
     """One library handle on one CUDA device."""
 
     def __init__(self, device=0):
         dev = torch.device("cuda", device) if isinstance(device, int) else torch.device(device)
+        if dev.index is None:
+            dev = torch.device("cuda", 0)
         self.device = dev
-        self.handle = B.gemm_create(dev.index if dev.index is not None else 0)
+        self.handle = B.gemm_create(dev.index)
+        self._run = B.load().gemm_run  # argument types set once by the binding
 
     def close(self):
         if getattr(self, "handle", None):
@@ -49,25 +63,27 @@ class Gemm:
         return s.cuda_stream
 
     def layout(self, A, Bm, C, a_major, b_major):
-        return B.layout(a_major, b_major, _DT[A.dtype], _DT[C.dtype])
+        return _layout(a_major, b_major, _DT[A.dtype], _DT[C.dtype])
 
     def run(self, A, Bm, C, bias=None, a_major=ROW, b_major=ROW, stream=None) -> None:
         """Enqueues C = A·B (+bias) into the preallocated row-major C."""
         M, N, K = problem_dims(A, Bm, a_major, b_major)
+        idx = self.device.index
         for t in (A, Bm, C) + ((bias,) if bias is not None else ()):
-            if t.device != self.device:
+            if t.get_device() != idx:
                 raise ValueError("tensor on %s, handle on %s" % (t.device, self.device))
             if not t.is_contiguous():
                 raise ValueError("tensors must be contiguous")
-        if A.dtype != Bm.dtype or A.dtype not in _DT or C.dtype not in _DT:
+        in_code, out_code = _DT.get(A.dtype), _DT.get(C.dtype)
+        if A.dtype != Bm.dtype or in_code is None or out_code is None:
             raise TypeError("A, B: both float16 or both float32; C: float16 or float32")
-        if tuple(C.shape) != (M, N):
+        if C.dim() != 2 or C.shape[0] != M or C.shape[1] != N:
             raise ValueError("C has shape %s, expected (%d, %d)" % (tuple(C.shape), M, N))
         if bias is not None and (bias.dtype != torch.float32 or tuple(bias.shape) != (N,)):
             raise ValueError("bias must be float32 of shape (N,)")
-        rc = B.gemm_run(self.handle, M, N, K, A.data_ptr(), Bm.data_ptr(),
-                        bias.data_ptr() if bias is not None else None, C.data_ptr(),
-                        self.layout(A, Bm, C, a_major, b_major), self._stream(stream))
+        rc = self._run(self.handle, M, N, K, A.data_ptr(), Bm.data_ptr(),
+                       bias.data_ptr() if bias is not None else None, C.data_ptr(),
+                       _layout(a_major, b_major, in_code, out_code), self._stream(stream))
         if rc != B.GEMM_OK:
             raise B.GemmError(rc, "gemm_run")
 
