@@ -17,10 +17,15 @@
 //                      k-block, hands the accumulator to the epilogue.  Warp 1
 //                      also allocates and frees TMEM.
 //   warps 2-5          epilogue: tcgen05.ld 32 lanes x 32 columns, + bias[n] in
-//                      fp32, one rounding to the output type, store.  For a
-//                      Stream-K partial unit: publish the fp32 partial, take a
-//                      ticket, and the last contributor sums all partials in
-//                      ascending k order before the same epilogue.
+//                      fp32, one rounding to the output type, then a TMA store
+//                      of the warp's 32 x 32 block from a swizzled shared box
+//                      (plain stores where C cannot take TMA; lane-per-column
+//                      stores for swapped operands).  For a Stream-K partial
+//                      unit: publish the fp32 partial, take a ticket, and the
+//                      last contributor sums all partials in ascending k order
+//                      before the same epilogue.  Each drained accumulator is
+//                      released to the MMA issuer, after seeding it with the
+//                      next unit's bias when the reduction starts from the bias.
 // The pipeline overlap of the A500 ladder's software-pipelining step
 // (kimm240.github.io/tvm, Step 5) is the S-stage ring plus the two accumulators:
 // the MMA of tile i+1 runs while the epilogue drains tile i.
@@ -181,75 +186,24 @@ __device__ __forceinline__ void seed_bias(const TcArgs& a, uint32_t taddr, int32
   tmem_wait_st();
 }
 
-// Writes one chunk of CW accumulator columns held by this thread.
-// Not TRANS: C[mm][nn0 + j] = v[j] + bias[nn0 + j]  (thread = output row).
-// TRANS:     C[nn0 + j][mm] = v[j] + bias[mm]       (thread = output column).
-template <int CW, bool OUT_F16, bool TRANS>
-__device__ __forceinline__ void store_chunk(const TcArgs& a, int32_t mm, int32_t nn0,
-                                            const float (&v)[CW]) {
+// Writes one chunk of CW accumulator columns held by this thread, for the
+// transposed store of swapped operands: C[nn0 + j][mm] = v[j] + bias[mm]
+// (thread = output column, so a warp's stores are consecutive in C).
+template <int CW, bool OUT_F16>
+__device__ __forceinline__ void store_chunk_trans(const TcArgs& a, int32_t mm, int32_t nn0,
+                                                  const float (&v)[CW]) {
   if (mm >= a.Mm || nn0 >= a.Nm) return;
   const int32_t ncols = (a.Nm - nn0) < CW ? (a.Nm - nn0) : CW;
-  if constexpr (!TRANS) {
-    float o[CW];
-    const float* ob = out_bias(a);
-    const float* bp = ob ? ob + nn0 : nullptr;
-    const bool full = ncols == CW;
-    if (bp && full && (reinterpret_cast<uintptr_t>(bp) & 15) == 0) {
+  const float* ob = out_bias(a);
+  const float bv = ob ? __ldg(ob + mm) : 0.f;
 #pragma unroll
-      for (int j = 0; j < CW; j += 4) {
-        const float4 b4 = __ldg(reinterpret_cast<const float4*>(bp + j));
-        o[j] = v[j] + b4.x; o[j + 1] = v[j + 1] + b4.y;
-        o[j + 2] = v[j + 2] + b4.z; o[j + 3] = v[j + 3] + b4.w;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < CW; ++j) o[j] = v[j] + ((bp && j < ncols) ? __ldg(bp + j) : 0.f);
-    }
-    if constexpr (OUT_F16) {
-      __half* row = reinterpret_cast<__half*>(a.C) + int64_t(mm) * a.ldc + nn0;
-      if (full && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
-#pragma unroll
-        for (int j = 0; j < CW; j += 8) {
-          uint4 pk;
-          __half2 h0 = __floats2half2_rn(o[j], o[j + 1]);
-          __half2 h1 = __floats2half2_rn(o[j + 2], o[j + 3]);
-          __half2 h2 = __floats2half2_rn(o[j + 4], o[j + 5]);
-          __half2 h3 = __floats2half2_rn(o[j + 6], o[j + 7]);
-          pk.x = *reinterpret_cast<uint32_t*>(&h0);
-          pk.y = *reinterpret_cast<uint32_t*>(&h1);
-          pk.z = *reinterpret_cast<uint32_t*>(&h2);
-          pk.w = *reinterpret_cast<uint32_t*>(&h3);
-          *reinterpret_cast<uint4*>(row + j) = pk;
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < CW; ++j)
-          if (j < ncols) row[j] = __float2half_rn(o[j]);
-      }
-    } else {
-      float* row = reinterpret_cast<float*>(a.C) + int64_t(mm) * a.ldc + nn0;
-      if (full && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
-#pragma unroll
-        for (int j = 0; j < CW; j += 4)
-          *reinterpret_cast<float4*>(row + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < CW; ++j)
-          if (j < ncols) row[j] = o[j];
-      }
-    }
-  } else {
-    const float* ob = out_bias(a);
-    const float bv = ob ? __ldg(ob + mm) : 0.f;
-#pragma unroll
-    for (int j = 0; j < CW; ++j) {
-      if (j < ncols) {
-        const int64_t off = int64_t(nn0 + j) * a.ldc + mm;
-        if constexpr (OUT_F16)
-          reinterpret_cast<__half*>(a.C)[off] = __float2half_rn(v[j] + bv);
-        else
-          reinterpret_cast<float*>(a.C)[off] = v[j] + bv;
-      }
+  for (int j = 0; j < CW; ++j) {
+    if (j < ncols) {
+      const int64_t off = int64_t(nn0 + j) * a.ldc + mm;
+      if constexpr (OUT_F16)
+        reinterpret_cast<__half*>(a.C)[off] = __float2half_rn(v[j] + bv);
+      else
+        reinterpret_cast<float*>(a.C)[off] = v[j] + bv;
     }
   }
 }
@@ -414,7 +368,7 @@ __device__ __forceinline__ void store_out(const TcArgs& a, const CUtensorMap* tm
                                           uint8_t* stage, int q, int32_t mm, int lane,
                                           int32_t nn0, const float (&v)[CW]) {
   if constexpr (TRANS) {
-    store_chunk<CW, OUT_F16, TRANS>(a, mm, nn0, v);
+    store_chunk_trans<CW, OUT_F16>(a, mm, nn0, v);
   } else if constexpr (CW == 32) {
     if (a.c_tma)
       store_rows_tma<OUT_F16>(tmC, a, stage + q * 4096, mm - lane, lane, nn0, v);

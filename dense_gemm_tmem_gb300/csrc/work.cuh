@@ -15,6 +15,7 @@
 // exactly what the kernel does.
 #pragma once
 
+#include <climits>
 #include <cstdint>
 
 namespace dg {
@@ -63,11 +64,15 @@ struct WorkIter {
       // of one cluster): CTA `cta` owns tile cta / s and the rank-th of s equal
       // contiguous k-block ranges, rank = cta % s.  Encoded as a one-iteration
       // "split region" walk: x = first k-block, end = one past the last.
+      // s is 2, 4 or 8: shifts instead of divisions (a 64-bit division is a
+      // long subroutine on the device, paid before the first load)
       const int32_t s = w.csplit;
-      const int32_t rank = cta % s;
+      const int sh = s == 8 ? 3 : s == 4 ? 2 : 1;
+      const int32_t rank = cta & (s - 1);
+      const int64_t base = int64_t(cta >> sh) * w.k_iters;
       next_dp = w.dp_tiles;  // no whole-tile phase
-      x = int64_t(cta / s) * w.k_iters + int64_t(rank) * w.k_iters / s;
-      end = int64_t(cta / s) * w.k_iters + int64_t(rank + 1) * w.k_iters / s;
+      x = base + ((int64_t(rank) * w.k_iters) >> sh);
+      end = base + ((int64_t(rank + 1) * w.k_iters) >> sh);
       return;
     }
     if (w.sk_tiles > 0) {
@@ -87,7 +92,9 @@ struct WorkIter {
       return true;
     }
     if (x < end) {
-      const int32_t t = int32_t(x / w.k_iters);
+      // 32-bit division when x fits (always, but for huge split regions)
+      const int32_t t = x <= INT32_MAX ? int32_t(uint32_t(x) / uint32_t(w.k_iters))
+                                       : int32_t(x / w.k_iters);
       const int32_t k0 = int32_t(x - int64_t(t) * w.k_iters);
       const int64_t left = end - x;
       const int32_t k1 = (left < int64_t(w.k_iters - k0)) ? int32_t(k0 + left) : w.k_iters;
