@@ -619,7 +619,11 @@ int gemm_work_units(const gemm_plan_t* plan, int cta, int32_t* out, int max_unit
   if (cta < 0 || cta >= units) return GEMM_ERR_INVALID_ARG;
   const dg::WorkSpec w = dg::spec_of(*plan);
   dg::WorkIter it;
-  it.init(w, cta);
+  // what the kernel runs: the tensor-core kernels use init_tc
+  if (plan->kernel == GEMM_KERNEL_SIMT)
+    it.init(w, cta);
+  else
+    it.init_tc(w, cta);
   dg::Unit u;
   int n = 0;
   while (it.next(w, u)) {

@@ -121,7 +121,7 @@ __device__ __forceinline__ void tc2_producer(const CUtensorMap& tmA, const CUten
   using Cfg = Tc2Config;
   const WorkSpec& W = args.work;
   WorkIter it;
-  it.init(W, cluster_id);
+  it.init_tc(W, cluster_id);
   Unit u;
   int s = 0;
   uint32_t ph = 0, issued = 0, issued_par = 0;
@@ -184,7 +184,7 @@ __device__ __forceinline__ void tc2_mma(const TcArgs& args, uint8_t* sA, uint8_t
   using Cfg = Tc2Config;
   const WorkSpec& W = args.work;
   WorkIter it;
-  it.init(W, cluster_id);
+  it.init_tc(W, cluster_id);
   Unit u;
   int s = 0, b = 0;
   uint32_t ph = 0, aph = 0;
@@ -346,8 +346,8 @@ __device__ __forceinline__ void tc2_epilogue(const TcArgs& args, uint64_t* acc_f
   // `ahead` runs two units ahead of `it`: the unit that will next use the
   // buffer just drained, which is seeded with the bias before its release
   WorkIter it, ahead;
-  it.init(W, cluster_id);
-  ahead.init(W, cluster_id);
+  it.init_tc(W, cluster_id);
+  ahead.init_tc(W, cluster_id);
   Unit u, un;
   auto release = [&](int buf, bool have_next) {
     if (have_next && args.bias_init && un.kb0 == 0) {

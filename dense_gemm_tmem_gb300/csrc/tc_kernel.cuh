@@ -540,7 +540,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
       WorkIter it;
-      it.init(W, blockIdx.x);
+      it.init_tc(W, blockIdx.x);
       Unit u;
       int s = 0;
       uint32_t ph = 0, issued = 0, issued_par = 0;
@@ -595,7 +595,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // -------------------------------------------------------- MMA issuer --
     if (lane == 0) {
       WorkIter it;
-      it.init(W, blockIdx.x);
+      it.init_tc(W, blockIdx.x);
       Unit u;
       int s = 0, b = 0;
       uint32_t ph = 0, aph = 0;
@@ -657,8 +657,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // `ahead` runs two units ahead of `it`: the unit that will next use the
     // buffer just drained, which is seeded with the bias before its release
     WorkIter it, ahead;
-    it.init(W, blockIdx.x);
-    ahead.init(W, blockIdx.x);
+    it.init_tc(W, blockIdx.x);
+    ahead.init_tc(W, blockIdx.x);
     Unit u, un;
     auto release = [&](int buf, bool have_next) {
       if (have_next && args.bias_init && un.kb0 == 0) {

@@ -15,7 +15,6 @@
 // exactly what the kernel does.
 #pragma once
 
-#include <climits>
 #include <cstdint>
 
 namespace dg {
@@ -64,15 +63,11 @@ struct WorkIter {
       // of one cluster): CTA `cta` owns tile cta / s and the rank-th of s equal
       // contiguous k-block ranges, rank = cta % s.  Encoded as a one-iteration
       // "split region" walk: x = first k-block, end = one past the last.
-      // s is 2, 4 or 8: shifts instead of divisions (a 64-bit division is a
-      // long subroutine on the device, paid before the first load)
       const int32_t s = w.csplit;
-      const int sh = s == 8 ? 3 : s == 4 ? 2 : 1;
-      const int32_t rank = cta & (s - 1);
-      const int64_t base = int64_t(cta >> sh) * w.k_iters;
+      const int32_t rank = cta % s;
       next_dp = w.dp_tiles;  // no whole-tile phase
-      x = base + ((int64_t(rank) * w.k_iters) >> sh);
-      end = base + ((int64_t(rank + 1) * w.k_iters) >> sh);
+      x = int64_t(cta / s) * w.k_iters + int64_t(rank) * w.k_iters / s;
+      end = int64_t(cta / s) * w.k_iters + int64_t(rank + 1) * w.k_iters / s;
       return;
     }
     if (w.sk_tiles > 0) {
@@ -81,6 +76,22 @@ struct WorkIter {
     } else {
       x = end = 0;
     }
+  }
+
+  // The same as init for the tensor-core kernels, whose cluster splits have
+  // s = 2, 4 or 8: shifts instead of divisions (a 64-bit division is a long
+  // subroutine on the device, paid before the first load).
+  __host__ __device__ __forceinline__ void init_tc(const WorkSpec& w, int32_t cta) {
+    if (w.csplit == 2 || w.csplit == 4 || w.csplit == 8) {
+      const int sh = w.csplit == 8 ? 3 : w.csplit == 4 ? 2 : 1;
+      const int32_t rank = cta & (w.csplit - 1);
+      const int64_t base = int64_t(cta >> sh) * w.k_iters;
+      next_dp = w.dp_tiles;  // no whole-tile phase
+      x = base + ((int64_t(rank) * w.k_iters) >> sh);
+      end = base + ((int64_t(rank + 1) * w.k_iters) >> sh);
+      return;
+    }
+    init(w, cta);
   }
 
   __host__ __device__ __forceinline__ bool next(const WorkSpec& w, Unit& u) {
@@ -92,9 +103,7 @@ struct WorkIter {
       return true;
     }
     if (x < end) {
-      // 32-bit division when x fits (always, but for huge split regions)
-      const int32_t t = x <= INT32_MAX ? int32_t(uint32_t(x) / uint32_t(w.k_iters))
-                                       : int32_t(x / w.k_iters);
+      const int32_t t = int32_t(x / w.k_iters);
       const int32_t k0 = int32_t(x - int64_t(t) * w.k_iters);
       const int64_t left = end - x;
       const int32_t k1 = (left < int64_t(w.k_iters - k0)) ? int32_t(k0 + left) : w.k_iters;

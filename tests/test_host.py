@@ -45,6 +45,24 @@ def test_no_library_gemm_or_cuda_driver_link(lib):
     assert "libcuda.so" not in deps and "libcublas" not in deps
 
 
+@pytest.mark.parametrize("src", ["simt.cu", "tc2.cu", "tc_n256.cu", "tc_small.cu"])
+def test_kernels_keep_registers_without_spills(src):
+    """The hot kernels fit their registers: ptxas reports no spill stores (the
+    128 x 128 CUDA-core kernel sits at the 128-register cap of 2 CTAs per SM,
+    where a small change elsewhere can push it into local memory)."""
+    from dense_gemm_tmem_gb300 import build as bld
+    try:
+        nvcc = bld._nvcc()
+    except Exception:
+        pytest.skip("nvcc not found")
+    csrc = os.path.join(os.path.dirname(bld.__file__), "csrc")
+    r = subprocess.run([nvcc] + bld.NVCC_FLAGS + ["-Xptxas", "-v", "-c", os.path.join(csrc, src),
+                        "-o", os.devnull], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-2000:]
+    spills = [int(m) for m in re.findall(r"(\d+) bytes spill stores", r.stderr)]
+    assert spills and max(spills) == 0, spills
+
+
 def test_sources_use_no_multicast_loads_or_wgmma():
     """No TMA multicast loads (every CTA fetches its own operand tiles), and no
     Hopper/legacy MMA forms.  A tcgen05.commit multicast (a completion signal to
