@@ -152,6 +152,11 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
   return v;
 }
 
+// fp32 store into a cluster CTA's shared memory (distributed shared memory).
+__device__ __forceinline__ void st_dsmem_f32(uint32_t cluster_addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
+}
+
 // 16-byte load from another CTA's shared memory (address 16-byte aligned).
 __device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t cluster_addr) {
   float4 v;

@@ -467,6 +467,53 @@ __device__ __forceinline__ void csplit_reduce(const TcArgs& a, const uint8_t* sm
   }
 }
 
+// Cluster split with swapped operands and a narrow tile (BN <= 32): every CTA
+// pushes the rows of its fp32 partial that rank j adds straight into rank j's
+// staging area (idle in this kernel: transposed output needs no staging), as
+// slot[src][column][row], R = 128 / s rows per rank, with remote stores that
+// need no round trip.  After one cluster barrier each CTA adds the s slots of
+// its own rows in source-rank order -- ascending k, so the sum does not depend
+// on timing -- adds the bias and writes C; no CTA reads another's memory after
+// the barrier, so none has to wait for the others before it exits.
+template <int BN>
+constexpr bool kPushReduce = BN <= 32;
+
+template <int BN, bool OUT_F16>
+__device__ __forceinline__ void csplit_reduce_pushed(const TcArgs& a, const uint8_t* stage,
+                                                     int tid, int nthreads) {
+  const WorkSpec& W = a.work;
+  const int s = W.csplit;
+  const int rank = int(blockIdx.x) % s;
+  const int R = kBM / s;
+  int32_t tm, tn;
+  tile_coords(W, int32_t(blockIdx.x) / s, tm, tn);
+  const float* slot = reinterpret_cast<const float*>(stage);
+  const float* ob = out_bias(a);
+  const int groups = BN * (R / 4);  // 4 consecutive rows of one column each
+#pragma unroll 1
+  for (int g = tid; g < groups; g += nthreads) {
+    const int col = g / (R / 4);
+    const int r4 = (g % (R / 4)) * 4;
+    float4 acc = *reinterpret_cast<const float4*>(slot + (0 * BN + col) * R + r4);
+#pragma unroll 1
+    for (int src = 1; src < s; ++src) {
+      const float4 v = *reinterpret_cast<const float4*>(slot + (src * BN + col) * R + r4);
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    const int32_t mm = tm * kBM + rank * R + r4;  // MMA-view row: C column
+    const int32_t nn = tn * BN + col;             // MMA-view column: C row
+    if (mm >= a.Mm || nn >= a.Nm) continue;
+    const int valid = min(4, a.Mm - mm);
+    if (ob) {
+      acc.x += __ldg(ob + mm);
+      if (valid > 1) acc.y += __ldg(ob + mm + 1);
+      if (valid > 2) acc.z += __ldg(ob + mm + 2);
+      if (valid > 3) acc.w += __ldg(ob + mm + 3);
+    }
+    put4<OUT_F16>(a, int64_t(nn) * a.ldc + mm, acc, valid);
+  }
+}
+
 template <int BN, bool OUT_F16, bool TRANS>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -687,7 +734,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int32_t nbase = tn * BN;
       const uint32_t taddr = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(b * BN);
 
-      if (W.csplit > 1) {
+      if (TRANS && kPushReduce<BN> && W.csplit > 1) {
+        // Cluster split, narrow swapped tile: push each row of the partial to
+        // the rank that adds it (csplit_reduce_pushed).
+        static_assert(!kPushReduce<BN> || kBM * BN * 4 <= Cfg::kEpiStageBytes, "slots");
+        const int s = W.csplit;
+        const int R = kBM / s;
+        const int owner = row / R;
+        const int r_in = row - owner * R;
+        const int src = int(blockIdx.x) % s;
+        const uint32_t dst = map_to_rank(smem_u32(stage), uint32_t(owner));
+        float v[CW];
+        __syncwarp();
+        tmem_load_chunk<CW>(taddr, v);
+#pragma unroll
+        for (int j = 0; j < CW; ++j)
+          if (j < BN) st_dsmem_f32(dst + 4u * uint32_t((src * BN + j) * R + r_in), v[j]);
+      } else if (W.csplit > 1) {
         // Cluster split: park this CTA's fp32 partial in its own (now idle)
         // stage ring, in the layout the reduction walks (csplit_reduce):
         // row-major with rows of BN + 4 floats, or, for the transposed store,
@@ -817,14 +880,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   __syncthreads();
   if (W.csplit > 1) {
-    // Every thread of every CTA of the cluster reaches both barriers, aborted
-    // or not, so neither can wait forever.
-    cluster_sync_all();  // all partials parked
+    // Every thread of every CTA of the cluster reaches the barriers, aborted
+    // or not, so none can wait forever.
+    cluster_sync_all();  // all partials parked (or pushed to their owners)
     if (threadIdx.x == 0) trace_mark(args, blockIdx.x, kTraceClusterParked);
-    csplit_reduce<BN, OUT_F16, TRANS>(args, smem, threadIdx.x, kTcThreads);
-    if (threadIdx.x == 0) trace_mark(args, blockIdx.x, kTraceClusterReduced);
-    cluster_sync_all();  // no CTA still reads another's shared memory
-    if (threadIdx.x == 0) trace_mark(args, blockIdx.x, kTraceClusterDone);
+    if constexpr (TRANS && kPushReduce<BN>) {
+      csplit_reduce_pushed<BN, OUT_F16>(args, stage, threadIdx.x, kTcThreads);
+      if (threadIdx.x == 0) {
+        trace_mark(args, blockIdx.x, kTraceClusterReduced);
+        trace_mark(args, blockIdx.x, kTraceClusterDone);
+      }
+    } else {
+      csplit_reduce<BN, OUT_F16, TRANS>(args, smem, threadIdx.x, kTcThreads);
+      if (threadIdx.x == 0) trace_mark(args, blockIdx.x, kTraceClusterReduced);
+      cluster_sync_all();  // no CTA still reads another's shared memory
+      if (threadIdx.x == 0) trace_mark(args, blockIdx.x, kTraceClusterDone);
+    }
   }
   if (warp == 1) {
     tc_fence_after();
