@@ -60,7 +60,9 @@ struct TcConfig {
   static constexpr int kBarBytes = 256;
   // epilogue staging (after the stages, so 1024-byte aligned): per epilogue
   // warp 32 rows of kChunk + 4 floats, or a 4 KiB swizzled TMA store box
-  static constexpr int kEpiStageBytes = 4 * 32 * (kChunk + 4) * 4;
+  // (64-column tiles: 32 KiB, which also holds the pushed partials of a
+  // swapped cluster split, 128 rows x 64 columns of fp32)
+  static constexpr int kEpiStageBytes = BN == 64 ? 32768 : 4 * 32 * (kChunk + 4) * 4;
   static_assert(kEpiStageBytes % 1024 == 0 && (kChunk != 32 || kEpiStageBytes >= 4 * 4096),
                 "staging area");
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes + kEpiStageBytes;
@@ -467,7 +469,7 @@ __device__ __forceinline__ void csplit_reduce(const TcArgs& a, const uint8_t* sm
   }
 }
 
-// Cluster split with swapped operands and a narrow tile (BN <= 32): every CTA
+// Cluster split with swapped operands and a narrow tile (BN <= 64): every CTA
 // pushes the rows of its fp32 partial that rank j adds straight into rank j's
 // staging area (idle in this kernel: transposed output needs no staging), as
 // slot[src][column][row], R = 128 / s rows per rank, with remote stores that
@@ -476,7 +478,7 @@ __device__ __forceinline__ void csplit_reduce(const TcArgs& a, const uint8_t* sm
 // on timing -- adds the bias and writes C; no CTA reads another's memory after
 // the barrier, so none has to wait for the others before it exits.
 template <int BN>
-constexpr bool kPushReduce = BN <= 32;
+constexpr bool kPushReduce = BN <= 64;
 
 template <int BN, bool OUT_F16>
 __device__ __forceinline__ void csplit_reduce_pushed(const TcArgs& a, const uint8_t* stage,
@@ -744,12 +746,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int r_in = row - owner * R;
         const int src = int(blockIdx.x) % s;
         const uint32_t dst = map_to_rank(smem_u32(stage), uint32_t(owner));
-        float v[CW];
-        __syncwarp();
-        tmem_load_chunk<CW>(taddr, v);
+#pragma unroll 1
+        for (int c = 0; c < BN / CW; ++c) {
+          float v[CW];
+          __syncwarp();
+          tmem_load_chunk<CW>(taddr + c * CW, v);
 #pragma unroll
-        for (int j = 0; j < CW; ++j)
-          if (j < BN) st_dsmem_f32(dst + 4u * uint32_t((src * BN + j) * R + r_in), v[j]);
+          for (int j = 0; j < CW; ++j)
+            st_dsmem_f32(dst + 4u * uint32_t((src * BN + c * CW + j) * R + r_in), v[j]);
+        }
       } else if (W.csplit > 1) {
         // Cluster split: park this CTA's fp32 partial in its own (now idle)
         // stage ring, in the layout the reduction walks (csplit_reduce):

@@ -230,10 +230,13 @@ def test_cluster_split_layouts(g, dev, csplit, am, bm, odt):
 
 
 @pytest.mark.parametrize("tile_n", [16, 32, 64, 128])
-@pytest.mark.parametrize("csplit", [2, 8])
-def test_cluster_split_swapped(g, dev, tile_n, csplit):
+@pytest.mark.parametrize("csplit", [2, 4, 8])
+@pytest.mark.parametrize("odt", [F16, F32])
+def test_cluster_split_swapped(g, dev, tile_n, csplit, odt):
+    """Swapped cluster splits: tiles of up to 64 columns push their partials
+    to the owning CTA, wider ones are read from the peers."""
     set_opts(g, kernel=SPLITC, csplit=csplit, tile_n=tile_n, swap=1)
-    p = problem(72, 640, 1032, 0, 0, F16, F32, True, 150 + tile_n)
+    p = problem(72, 640, 1032, 0, 0, F16, odt, True, 150 + tile_n + (odt == F32))
     full_check(g, dev, p)
 
 
