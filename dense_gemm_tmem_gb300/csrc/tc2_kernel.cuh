@@ -128,12 +128,19 @@ __device__ __forceinline__ void tc2_producer(const CUtensorMap& tmA, const CUten
   bool ok = true;
   const int32_t row_off = int32_t(rank) * kBM;      // this CTA's rows of the A tile
   const int32_t col_off = int32_t(rank) * kHalfBN;  // this CTA's columns of the B tile
+  int32_t nunit = 0;
   while (ok && it.next(W, u)) {
     int32_t tm, tn;
     tile_coords(W, u.tile, tm, tn);
     const int32_t a_row = tm * kPairBM + row_off;
     const int32_t b_row = tn * kPairBN + col_off;
-    for (int32_t kb = u.kb0; kb < u.kb1; ++kb) {
+    // Every other unit walks k from the last block to the first: the pairs'
+    // next wave of tiles shares the raster group's A row panels with the wave
+    // before, and starting from the k-panels that wave loaded last finds them
+    // still in L2.  tc2_mma follows the same order.
+    const bool rev = (nunit++ & 1) != 0;
+    for (int32_t i = 0; i < u.kb1 - u.kb0; ++i) {
+      const int32_t kb = rev ? u.kb1 - 1 - i : u.kb0 + i;
       if (!wait_bounded(smem_u32(&empty[s]), ph ^ 1, wc, kSiteProducer)) {
         ok = false;
         break;
@@ -203,7 +210,9 @@ __device__ __forceinline__ void tc2_mma(const TcArgs& args, uint8_t* sA, uint8_t
     tc_fence_after();
     const uint32_t d_tmem = tmem_base + uint32_t(b * kPairBN);
     const bool seeded = args.bias_init && u.kb0 == 0;  // accumulate onto the bias
-    for (int32_t kb = u.kb0; kb < u.kb1; ++kb) {
+    // stages arrive in the producer's order (k ascending, or descending on
+    // every other unit); the first MMA of the unit starts the sum
+    for (int32_t i = 0; i < u.kb1 - u.kb0; ++i) {
       if (!wait_bounded(smem_u32(&full[s]), ph, wc, kSiteMmaFull)) {
         ok = false;
         break;
@@ -215,7 +224,7 @@ __device__ __forceinline__ void tc2_mma(const TcArgs& args, uint8_t* sA, uint8_t
 #pragma unroll
       for (int kk = 0; kk < kBK / 16; ++kk)
         tc_mma_f16_pair(d_tmem, adesc + uint64_t(kk * a_step), bdesc + uint64_t(kk * b_step),
-                        args.idesc, (kb > u.kb0 || kk > 0 || seeded) ? 1u : 0u);
+                        args.idesc, (i > 0 || kk > 0 || seeded) ? 1u : 0u);
       any = true;
       tc_commit_pair_both(smem_u32(&empty[s]));
       if (++s == S) {
