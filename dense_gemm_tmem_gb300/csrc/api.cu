@@ -133,20 +133,20 @@ int plan_simt(int64_t M, int64_t N, int64_t K, int num_sms, const Options& o, ge
 //    k-blocks in runs of at least 8.
 //  * fp16 inputs whose leading dimensions (or, in gemm_run, base addresses)
 //    break the TMA rules -> the same CUDA-core kernel, fp16 widened to fp32.
-//  * fp16 inputs -> tcgen05 kernels.  Large shapes whose 256x256 tiles fill
-//    whole waves of CTA pairs -> the two-SM kernel.  Skinny M (M <= 128,
+//  * fp16 inputs -> tcgen05 kernels.  Shapes with at least half as many
+//    256x256 tiles as CTA pairs -> the two-SM kernel.  Skinny M (M <= 128,
 //    N >= 2M, A row-major) swaps the operands so N fills the 128-row MMA side
 //    and M becomes the MMA N side (16/32/64/128 columns).  Otherwise the tile
 //    is 128x256 (128x128 when N <= 128 or when 256-wide tiles would fill fewer
 //    than half the SMs).
-//  * Decomposition (the Stream-K rule of the leiblog.wang Stream-K post: keep
-//    every SM busy when the tile count leaves waves part-empty):
-//      tiles >= SMs, count a multiple of the SMs or >= 4 full waves: whole tiles;
-//      tiles >= SMs otherwise: whole tiles for all but the last full wave, the
-//        rest (between 1 and 2 waves' worth) split evenly over all SMs;
-//      tiles < SMs: all k-blocks split evenly over up to one CTA per SM, at
-//        least enough k-blocks per CTA that it reads 4x its fp32 partial tile
-//        in operands (else whole tiles, one per CTA).
+//  * Decomposition of the one-SM kernel (the k-split the leiblog.wang
+//    Stream-K post uses to keep SMs busy, where it pays here):
+//      tiles fill under half the SMs: a cluster split of each tile's k-blocks
+//        (partials added on chip), or, for shallow K, narrow whole tiles;
+//        failing both, all k-blocks split evenly over up to one CTA per SM
+//        (Stream-K), at least enough k-blocks per CTA that it reads 4x its
+//        fp32 partial tile in operands (else whole tiles, one per CTA);
+//      otherwise whole tiles, persistent over the SMs.
 int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
              const Options& o, gemm_plan_t* p) {
   if (!p) return GEMM_ERR_INVALID_ARG;
@@ -188,10 +188,12 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
   const int a_mn = swap ? (L.b_major == GEMM_ROW_MAJOR) : (L.a_major == GEMM_COL_MAJOR);
   const int b_mn = swap ? (L.a_major == GEMM_COL_MAJOR) : (L.b_major == GEMM_ROW_MAJOR);
 
-  // Two-SM kernel (CTA pairs, 256 x 256 tiles, whole tiles only): when asked
-  // for, or when the pair tiles fill whole waves of pairs (a multiple of the
-  // resident pairs, or at least four waves) the same way the one-SM rule below
-  // decides for whole tiles.
+  // Two-SM kernel (CTA pairs, 256 x 256 tiles, whole tiles): when asked for,
+  // or when there are at least half as many pair tiles as resident pairs.  A
+  // part-empty last wave of pair tiles costs less than splitting k: measured
+  // (graph replay, cold inputs, TFLOP/s, two-SM kernel vs the one-SM
+  // Stream-K/hybrid split) 2048^3 891 vs 458, 3072^3 1200 vs 828, 4096^3 1568
+  // vs 1308, 4096x4096x1024 1043 vs 711, 1024x4096x4096 1014 vs 608.
   const int64_t pairs = o.pair_clusters > 0 ? o.pair_clusters : num_sms / 2;
   if (forced_pair && (swap || pairs < 1 || o.force_tile_n > 0)) return GEMM_ERR_UNSUPPORTED;
   if (!swap && pairs >= 1 && o.force_tile_n <= 0 &&
@@ -200,8 +202,7 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
     const int64_t T2 = t2m * t2n;
     const int64_t I2 = ceil_div(K, kBK);
     bool use = forced_pair || o.pair == 1;
-    if (!use && o.force_grid <= 0 && T2 >= pairs)
-      use = (T2 % pairs == 0) || (T2 / pairs >= 4);
+    if (!use && o.force_grid <= 0) use = 2 * T2 >= pairs;
     if (use) {
       if (T2 > INT32_MAX / 2 || I2 > INT32_MAX / 2) return GEMM_ERR_UNSUPPORTED;
       int64_t np = std::min(pairs, T2);
@@ -344,20 +345,19 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
   } else if (o.force_kernel == GEMM_KERNEL_STREAMK) {
     sk = T;
     grid = std::min(max_grid, T * I);
-  } else if (T >= G) {
-    const int64_t full = T / G, rem = T % G;
-    if (rem == 0 || full >= 4) {
-      dp = T;
-    } else {
-      dp = (full - 1) * G;
-      sk = T - dp;
-    }
-    grid = G;
-    if (max_grid < G) {  // a forced smaller grid: split everything over it
-      dp = 0;
-      sk = T;
-      grid = max_grid;
-    }
+  } else if (max_grid < G && T > max_grid) {
+    // a forced smaller grid: split everything over it
+    sk = T;
+    grid = max_grid;
+  } else if (2 * T >= G) {
+    // At least half as many tiles as SMs: whole tiles, a part-empty last wave
+    // and all.  The Stream-K or hybrid split the leiblog.wang post suggests for
+    // that tail measured slower here (graph replay, cold inputs, TFLOP/s):
+    // 4096^3 1383 whole vs 1308 hybrid, 1024x2048x4096 707 vs 516 split,
+    // 1536x1536x4096 796 vs 596, 2048x1024x2048 565 vs 337, 512x4096x8192 810
+    // vs 665 -- its fixup reads every other contributor's partial serially.
+    dp = T;
+    grid = std::min(T, G);
   } else {
     const int64_t total = T * I;
     // A split CTA writes (and the tile's last CTA reads back) a 128 x bn fp32

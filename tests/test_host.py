@@ -103,13 +103,20 @@ def test_picker_large_square_two_sm_tiles():
     assert p.dp_tiles == 64 * 64 and p.sk_tiles == 0 and p.workspace_bytes == 0
 
 
-def test_picker_pair_rule_falls_back():
-    # 100 pair tiles on 76 pairs: 1.3 waves -> the one-SM rules decide
-    rc, p = plan(1280, 5120, 1024)
-    assert rc == 0 and p.kernel == B.GEMM_KERNEL_STREAMK and p.tile_m == 128
-    # exactly one wave of pairs: 76 = 4 x 19 tiles
-    rc, p = plan(1024, 19 * 256, 512)
+def test_picker_pair_rule():
+    # at least half as many pair tiles as pairs (38 of 76): the two-SM kernel,
+    # whole tiles, even when the last wave is part-empty
+    rc, p = plan(1280, 5120, 1024)  # 100 pair tiles: 1.3 waves
+    assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC2
+    assert (p.grid, p.dp_tiles, p.sk_tiles) == (SMS, 100, 0)
+    rc, p = plan(2048, 2048, 2048)  # 64 pair tiles on 64 pairs
+    assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC2 and (p.grid, p.dp_tiles) == (128, 64)
+    rc, p = plan(1024, 19 * 256, 512)  # one wave: 76 = 4 x 19
     assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC2 and p.grid == 152
+    # fewer pair tiles (32): the one-SM rules (here 128 whole tiles of 128 x 128)
+    rc, p = plan(1024, 2048, 4096)
+    assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC
+    assert (p.tile_n, p.grid, p.dp_tiles, p.sk_tiles) == (128, 128, 128, 0)
     # skinny shapes swap operands and never pair
     rc, p = plan(64, 65536, 4096)
     assert rc == 0 and p.swap_ab == 1 and p.kernel != B.GEMM_KERNEL_TC2
@@ -132,11 +139,13 @@ def test_picker_small_shapes():
     rc, p = plan(512, 512, 8192)
     assert rc == 0 and p.kernel == B.GEMM_KERNEL_SPLITC
     assert (p.cluster_split, p.grid) == (8, 128)
-    # 80 tiles: clusters of 2 would need 160 CTAs -> Stream-K over 152 CTAs
+    # 80 tiles: clusters of 2 would need 160 CTAs -> whole tiles, one per CTA
     rc, p = plan(1280, 1024, 4096)
-    assert rc == 0 and p.kernel == B.GEMM_KERNEL_STREAMK
-    assert (p.tile_n, p.sk_tiles, p.grid, p.cluster_split) == (128, 80, 152, 0)
-    assert p.workspace_bytes == 2 * 152 * 128 * 128 * 4
+    assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC
+    assert (p.tile_n, p.dp_tiles, p.grid, p.cluster_split) == (128, 80, 80, 0)
+    # deep K with 48 tiles and no cluster capacity assumed away: clusters of 2
+    rc, p = plan(768, 1024, 8192)
+    assert rc == 0 and p.kernel == B.GEMM_KERNEL_SPLITC and p.cluster_split == 2
 
 
 @pytest.mark.parametrize("bn,iters", [(256, 11), (128, 8), (64, 6), (32, 4), (16, 2)])
@@ -156,15 +165,16 @@ def test_picker_skinny_swaps_operands(M, bn):
     assert (p.a_mn_major, p.b_mn_major) == (1, 0)  # Bᵀ is N-contiguous, A is K-contiguous
 
 
-def test_picker_hybrid_tail():
-    # 314 tiles on 152 SMs: one whole wave, then 162 tiles split evenly
-    rc, p = plan(128 * 157, 256 * 2, 1024)
-    assert rc == 0 and p.kernel == B.GEMM_KERNEL_STREAMK
-    assert (p.dp_tiles, p.sk_tiles, p.grid) == (152, 162, SMS)
-    assert p.group_m == 16  # 2048 rows of A per raster group (16 one-SM tiles)
-    # 200 tiles (1 wave + 48): all split
-    rc, p = plan(128 * 10, 256 * 20, 1024)
-    assert (p.dp_tiles, p.sk_tiles) == (0, 200)
+def test_picker_part_empty_waves_stay_whole():
+    # swapped skinny shape with 314 tiles of 128 x 64 on 152 SMs: whole tiles,
+    # persistent (2.07 waves); a k-split of the tail measured slower
+    rc, p = plan(64, 128 * 314, 1024)
+    assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC and p.swap_ab == 1
+    assert (p.dp_tiles, p.sk_tiles, p.grid) == (314, 0, SMS)
+    assert p.group_m == 16  # 2048 rows of the MMA A side per raster group
+    # 80 tiles (at least half the SMs): one whole tile per CTA
+    rc, p = plan(128 * 10, 128 * 8, 4096)
+    assert (p.kernel, p.dp_tiles, p.sk_tiles, p.grid) == (B.GEMM_KERNEL_TC, 80, 0, 80)
 
 
 def test_picker_fp32_and_degenerate():
