@@ -57,10 +57,13 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // The CUDA-core kernel's plan (fp32 inputs, and fp16 inputs the tensor-core
 // path cannot read).
 int plan_simt(int64_t M, int64_t N, int64_t K, int num_sms, const Options& o, gemm_plan_t* p) {
-  // 128x128 tiles (256 threads, 2 CTAs per SM).  Only when those tiles
-  // cannot give every SM one, 64x64 tiles (64 threads) spread the work wider;
-  // measured on 2048^3 the smaller CTAs lose more to per-FMA overhead (FMA
-  // pipe 52 % vs 64 % busy) than they win back in balance.
+  // 128x128 tiles (256 threads, 2 CTAs per SM), their k-blocks split over the
+  // resident CTAs when the tiles are too few.  Only when even that split
+  // would run fewer than 8 CTAs do 64x64 tiles (64 threads) spread the work
+  // wider.  Measured (graph replay, cold inputs, TFLOP/s, 128-tile split vs
+  // 64-tiles): 1024^3 35.1 vs 22.7, 512^3 10.9 vs 5.5, 1536^3 47.0 vs 41.1,
+  // 4096x256x4096 47.4 vs 23.8; 128^3 (one 128-tile) 0.25 vs 0.37.
+  const int min_iters = o.min_split_iters > 0 ? o.min_split_iters : kSimtMinSplitIters;
   int tile;
   if (o.force_tile_n > 0) {
     if (o.force_tile_n != kSimtBM && o.force_tile_n != kSimtSmallTile)
@@ -68,7 +71,8 @@ int plan_simt(int64_t M, int64_t N, int64_t K, int num_sms, const Options& o, ge
     tile = o.force_tile_n;
   } else {
     const int64_t big = ceil_div(M, kSimtBM) * ceil_div(N, kSimtBN);
-    tile = big >= num_sms ? kSimtBM : kSimtSmallTile;
+    const int64_t big_split = std::max(big, big * ceil_div(K, kSimtBK) / min_iters);
+    tile = big_split >= 8 ? kSimtBM : kSimtSmallTile;
   }
   const int64_t tiles_m = ceil_div(M, tile), tiles_n = ceil_div(N, tile);
   const int64_t T = tiles_m * tiles_n;
@@ -100,7 +104,6 @@ int plan_simt(int64_t M, int64_t N, int64_t K, int num_sms, const Options& o, ge
     }
   } else if (tile == kSimtBM) {
     // fewer tiles than resident CTAs: split all k-blocks over up to S CTAs
-    const int min_iters = o.min_split_iters > 0 ? o.min_split_iters : kSimtMinSplitIters;
     grid = std::min(S, std::max<int64_t>(T, T * I / min_iters));
     if (grid > T) {
       dp = 0;
@@ -127,10 +130,10 @@ int plan_simt(int64_t M, int64_t N, int64_t K, int num_sms, const Options& o, ge
 }
 
 // Chooses kernel, tile, split and grid for a shape.  Rules:
-//  * fp32 inputs -> CUDA-core kernel, 128x128 tiles (64x64 when there are
-//    fewer 128-tiles than SMs).  With 128-tiles the tiles-vs-waves rule below
-//    is applied over the resident CTAs (2 per SM), and a split hands out the
-//    k-blocks in runs of at least 8.
+//  * fp32 inputs -> CUDA-core kernel, 128x128 tiles (64x64 only when a split
+//    of the 128-tiles would still run fewer than 8 CTAs).  With 128-tiles
+//    the tiles-vs-waves rule below is applied over the resident CTAs (2 per
+//    SM), and a split hands out the k-blocks in runs of at least 8.
 //  * fp16 inputs whose leading dimensions (or, in gemm_run, base addresses)
 //    break the TMA rules -> the same CUDA-core kernel, fp16 widened to fp32.
 //  * fp16 inputs -> tcgen05 kernels.  Shapes with at least half as many

@@ -97,7 +97,7 @@ struct SimtLaunch {
 };
 cudaError_t launch_simt(const SimtLaunch& L);
 cudaError_t launch_simt_f16(const SimtLaunch& L);
-constexpr int kSimtBM = 128, kSimtBN = 128, kSimtBK = 8, kSimtThreads = 256;
+constexpr int kSimtBM = 128, kSimtBN = 128, kSimtBK = 16, kSimtThreads = 256;
 constexpr int kSimtSmallTile = 64;  // 64 x 64 tiles, 64 threads
 constexpr int kSimtMinSplitIters = 8;  // fewest k-blocks a split CTA gets
 // CTAs of the 128 x 128 kernel resident on one SM (-1 if the query fails).

@@ -7,8 +7,8 @@
 //   Step 1 data-parallel 2-D thread map    -> one CTA per BM x BN output tile
 //   Step 2 tiling + loop reordering        -> each thread owns an 8x8 register tile
 //                                             and runs the k loop outermost
-//   Step 3 shared memory, cooperative fetch-> all threads stage a BM x 8 A block
-//                                             and an 8 x BN B block per k-step
+//   Step 3 shared memory, cooperative fetch-> all threads stage a BM x 16 A block
+//                                             and a 16 x BN B block per k-step
 //   Step 4 vectorisation + register caching-> float4 global and shared loads;
 //                                             accumulators live in registers
 //   Step 5 software pipelining             -> two shared-memory buffers; the next
@@ -22,8 +22,9 @@
 // makes the transposed A stores free of bank conflicts.
 //
 // Two tile shapes: 128 x 128 with 256 threads, and 64 x 64 with 64 threads for
-// grids too small to balance over the SMs (the 8x8 thread tile, and so the
-// ratio of shared loads to FMAs, is the same in both).
+// products too small to give even a k-split of 128-tiles 8 CTAs (the 8x8
+// thread tile, and so the ratio of shared loads to FMAs, is the same in
+// both).
 //
 // Work is handed out as the tensor-core kernels hand it out (work.cuh): whole
 // tiles first, then, when the tile count would leave the last wave of resident
@@ -150,15 +151,25 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
   float ra[AV][4], rb[BV][4];
   float acc[8][8];
 
+  // Piece v of this thread for an operand stored k-contiguous (row-major A,
+  // column-major B): pairs of threads cover 8 consecutive k of one row (a
+  // 32-byte sector), RP = NT/2 rows per pass, the next 8 k in a later pass.
+  // That keeps the transposed shared stores free of bank conflicts with the
+  // padded stride (a warp's 32 stores hit 16 rows x 2 k-quarters 16 banks
+  // apart).  An operand stored m/n-contiguous is read as piece f = t + v*NT:
+  // k-row f/(BM/4), run of 4 f%(BM/4).
+  constexpr int RP = NT / 2;
+  static_assert(BK % 8 == 0 && BM % RP == 0 && BN % RP == 0, "piece map");
+  auto kc_row = [&](int v, int rows) { return (t >> 1) + (v % (rows / RP)) * RP; };
+  auto kc_kq = [&](int v, int rows) { return 2 * (v / (rows / RP)) + (t & 1); };
+
   // Global -> registers for the k-block starting at k0 of the tile at (m0, n0).
-  // Piece f of A is, for row-major A, row f/2 and k-quarter f%2; for
-  // column-major A, k-row f/(BM/4) and m-quarter f%(BM/4).  B likewise.
   auto fetch = [&](int64_t m0, int64_t n0, int64_t k0) {
 #pragma unroll
     for (int v = 0; v < AV; ++v) {
       const int f = t + v * NT;
       if (!A_COL) {
-        const int64_t m = m0 + (f >> 1), k = k0 + (f & 1) * 4;
+        const int64_t m = m0 + kc_row(v, BM), k = k0 + kc_kq(v, BM) * 4;
         load4(ra[v], Ap + m * K + k, a.vec_a, m < M, k, K);
       } else {
         const int64_t k = k0 + f / (BM / 4), m = m0 + (f % (BM / 4)) * 4;
@@ -172,7 +183,7 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
         const int64_t k = k0 + f / (BN / 4), n = n0 + (f % (BN / 4)) * 4;
         load4(rb[v], Bp + k * N + n, a.vec_b, k < K, n, N);
       } else {
-        const int64_t n = n0 + (f >> 1), k = k0 + (f & 1) * 4;
+        const int64_t n = n0 + kc_row(v, BN), k = k0 + kc_kq(v, BN) * 4;
         load4(rb[v], Bp + n * K + k, a.vec_b, n < N, k, K);
       }
     }
@@ -184,7 +195,7 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
     for (int v = 0; v < AV; ++v) {
       const int f = t + v * NT;
       if (!A_COL) {
-        const int m = f >> 1, k = (f & 1) * 4;
+        const int m = kc_row(v, BM), k = kc_kq(v, BM) * 4;
 #pragma unroll
         for (int i = 0; i < 4; ++i) As[buf][k + i][m] = ra[v][i];
       } else {
@@ -201,7 +212,7 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
         *reinterpret_cast<float4*>(&Bs[buf][k][n]) =
             make_float4(rb[v][0], rb[v][1], rb[v][2], rb[v][3]);
       } else {
-        const int n = f >> 1, k = (f & 1) * 4;
+        const int n = kc_row(v, BN), k = kc_kq(v, BN) * 4;
 #pragma unroll
         for (int i = 0; i < 4; ++i) Bs[buf][k + i][n] = rb[v][i];
       }

@@ -426,6 +426,22 @@ def test_simt_layouts_ragged(g, dev, tile, am, bm, M, N, K):
     full_check(g, dev, p)
 
 
+@pytest.mark.parametrize("am,bm", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("K", [16, 17, 1000, 1024])
+@pytest.mark.parametrize("grid", [0, 7])
+@pytest.mark.parametrize("tile", [64, 128])
+def test_simt_interior_and_ragged_k(g, dev, am, bm, K, grid, tile):
+    """fp32, every tile inside M and N: the unchecked interior loop (direct
+    global-to-shared copies for operands stored m/n-contiguous) runs all
+    whole k-blocks, the checked loop only a ragged last one; with a forced
+    grid the k ranges of the split start and end inside tiles."""
+    set_opts(g, tile_n=tile)
+    if grid:
+        set_opts(g, grid=grid)
+    p = problem(256, 384, K, am, bm, F32, F32, True, 300 + K + 2 * am + bm)
+    full_check(g, dev, p)
+
+
 @pytest.mark.parametrize("tile", [64, 128])
 @pytest.mark.parametrize("grid", [1, 5, 37, 304])
 def test_simt_split_grid_sizes(g, dev, tile, grid):

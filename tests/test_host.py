@@ -182,7 +182,7 @@ def test_picker_fp32_and_degenerate():
     # over 304 CTAs (a whole-tile launch would leave 48 SMs with one tile)
     rc, p = plan(2048, 2048, 2048, 0, 0, F32, F32)
     assert rc == 0 and p.kernel == B.GEMM_KERNEL_SIMT and p.tile_m == 128
-    assert (p.grid, p.dp_tiles, p.sk_tiles, p.k_iters) == (304, 0, 256, 256)
+    assert (p.grid, p.dp_tiles, p.sk_tiles, p.k_iters, p.tile_k) == (304, 0, 256, 128, 16)
     assert p.workspace_bytes == 2 * 304 * 128 * 128 * 4 and p.group_m == 16
     # whole waves of resident CTAs stay whole: 608 tiles, 2 waves
     rc, p = plan(128 * 16, 128 * 38, 512, 0, 0, F32, F32)
@@ -196,9 +196,13 @@ def test_picker_fp32_and_degenerate():
     # shallow K: at least 8 k-blocks per split CTA -> 160 tiles x 2 k-blocks stay whole
     rc, p = plan(128 * 10, 128 * 16, 16, 0, 0, F32, F32)
     assert (p.grid, p.dp_tiles, p.sk_tiles) == (160, 160, 0)
-    # fewer 128-tiles than SMs: 64x64 tiles spread the work over more SMs
+    # fewer 128-tiles than SMs: their k-blocks split over more CTAs (16 tiles x
+    # 32 k-blocks in runs of at least 8 -> 64 CTAs)
     rc, p = plan(512, 512, 512, 0, 0, F32, F32)
-    assert rc == 0 and (p.tile_m, p.grid) == (64, 64)
+    assert rc == 0 and (p.tile_m, p.grid, p.dp_tiles, p.sk_tiles) == (128, 64, 0, 16)
+    # ... unless even that split runs fewer than 8 CTAs: 64x64 tiles
+    rc, p = plan(128, 128, 128, 0, 0, F32, F32)
+    assert rc == 0 and (p.tile_m, p.grid, p.sk_tiles) == (64, 4, 0)
     assert plan(64, 64, 64, 0, 0, F32, F16)[0] == B.GEMM_ERR_UNSUPPORTED
     assert plan(10, 10, 0)[1].kernel == B.GEMM_KERNEL_FILL
     assert plan(0, 10, 10)[1].kernel == B.GEMM_KERNEL_NONE
