@@ -10,7 +10,7 @@ int simt_b_stride() { return simt_detail::aligned_stride(kSimtBN, 32, 4); }
 int simt_ctas_per_sm() {
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-          &n, simt_detail::simt_sgemm_kernel<float, float, kSimtBM, kSimtBN, false, false>,
+          &n, simt_detail::simt_sgemm_kernel<float, float, kSimtBM, kSimtBN, false, false, true>,
           kSimtThreads, 0) != cudaSuccess)
     return -1;
   return n;

@@ -10,10 +10,16 @@
 //   Step 3 shared memory, cooperative fetch-> all threads stage a BM x 16 A block
 //                                             and a 16 x BN B block per k-step
 //   Step 4 vectorisation + register caching-> float4 global and shared loads;
-//                                             accumulators live in registers
+//                                             accumulators live in registers, and
+//                                             the FMAs are packed two lanes wide
+//                                             (fma.rn.f32x2: a pair of A rows times
+//                                             one B column per instruction)
 //   Step 5 software pipelining             -> two shared-memory buffers; the next
-//                                             block is fetched into registers
-//                                             while the current one is consumed
+//                                             block is fetched (into registers, or
+//                                             by direct global-to-shared copies
+//                                             for aligned fp32 operands stored
+//                                             m/n-contiguous) while the current
+//                                             one is consumed
 //   Step 6 unrolling                       -> the k-step and the 8x8 FMA nest are
 //                                             fully unrolled
 // The staging rows are padded as storage_align(factor 32, offset 4) pads them
@@ -35,11 +41,15 @@
 // order and stores the tile.  No CTA ever waits for another.
 //
 // fp16 inputs are widened to fp32 as they are staged (8-byte loads of four
-// halves where aligned), so products and sums are the fp32 FFMAs of the fp32
-// path; an fp16 output is rounded once, after the bias add.
+// halves where aligned), so products and sums are the fp32 FMAs of the fp32
+// path; an fp16 output is rounded once, after the bias add.  Each packed FMA
+// lane is an IEEE fused multiply-add rounded to nearest, exactly fmaf, so the
+// packing changes no result.
 #pragma once
 
 #include <cuda_fp16.h>
+
+#include <type_traits>
 
 #include "internal.h"
 #include "work.cuh"
@@ -93,6 +103,34 @@ __device__ __forceinline__ void load4(float (&r)[4], const __half* p, bool vec, 
   }
 }
 
+// d = a * b + d on two packed fp32 lanes ({low, high} halves of each 64-bit
+// operand), each lane one IEEE fused multiply-add rounded to nearest: the
+// results of two fmaf calls in one instruction, which halves the issue slots
+// the FMAs take (the FMA pipe itself does the same 128 lanes per SM per clock).
+__device__ __forceinline__ void fma2(uint64_t& d, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+// {x, x} as one packed operand.
+__device__ __forceinline__ uint64_t dup2(float x) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(x));
+  return r;
+}
+
+// 16 bytes global -> shared without passing through registers, cached in L2
+// only; with inside == false nothing is read (src may be any valid address)
+// and the 16 bytes are zero-filled.  Both addresses 16-byte aligned.  Awaited
+// by cp_async_wait_all before the barrier that publishes the buffer.
+__device__ __forceinline__ void cp_async16(float* smem_dst, const float* gsrc, bool inside) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n"
+               ::"r"(d), "l"(gsrc), "r"(inside ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async16(float*, const __half*, bool) {}  // fp16: not used
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;\n" ::: "memory");
+}
+
 // Four consecutive outputs of one row (n + j < N checked per element when the
 // vector store is not allowed); one rounding to TOut.
 __device__ __forceinline__ void store4(float* dst, const float (&o)[4], bool vec, int64_t n,
@@ -125,9 +163,10 @@ __device__ __forceinline__ void store4(__half* dst, const float (&o)[4], bool ve
 // of two 4-row groups BM/2 apart and two 4-column groups BN/2 apart.  A 1-D
 // grid of a.work.grid CTAs walks the units that WorkIter hands it.  Residency
 // asked of the compiler: 2 CTAs per SM for 128-tiles; 4 for 64-tiles, which the
-// picker uses only while 128-tiles are fewer than the SMs (so fewer than 4 x
-// SMs 64-tiles).
-template <typename TIn, typename TOut, int BM, int BN, bool A_COL, bool B_COL>
+// picker uses only for products too small to give 128-tiles 8 CTAs.  ASYNC
+// (fp32 only): the operands stored m/n-contiguous have 16-byte aligned rows
+// and are copied global -> shared directly, holding no staging registers.
+template <typename TIn, typename TOut, int BM, int BN, bool A_COL, bool B_COL, bool ASYNC>
 __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
     simt_sgemm_kernel(const SimtArgs a) {
   constexpr int BK = kSimtBK;
@@ -137,6 +176,9 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
   constexpr int AV = BM * BK / 4 / NT;  // float4 pieces of A per thread per k-block
   constexpr int BV = BN * BK / 4 / NT;
   static_assert(AV >= 1 && BV >= 1 && AV * NT * 4 == BM * BK && BV * NT * 4 == BN * BK, "");
+  static_assert(!ASYNC || std::is_same<TIn, float>::value, "direct copies are fp32 only");
+  constexpr bool kAsyncA = ASYNC && A_COL;   // column-major A: m-contiguous
+  constexpr bool kAsyncB = ASYNC && !B_COL;  // row-major B: n-contiguous
   __shared__ __align__(16) float As[2][BK][AS];
   __shared__ __align__(16) float Bs[2][BK][BS];
   __shared__ int last_flag;
@@ -150,6 +192,9 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
 
   float ra[AV][4], rb[BV][4];
   float acc[8][8];
+  // The main loop accumulates row pairs, P[i][j] = {acc[2i][j], acc[2i+1][j]},
+  // with packed two-wide FMAs: a pair of A rows times one B column, {b, b}.
+  uint64_t P[4][8];
 
   // Piece v of this thread for an operand stored k-contiguous (row-major A,
   // column-major B): pairs of threads cover 8 consecutive k of one row (a
@@ -163,8 +208,9 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
   auto kc_row = [&](int v, int rows) { return (t >> 1) + (v % (rows / RP)) * RP; };
   auto kc_kq = [&](int v, int rows) { return 2 * (v / (rows / RP)) + (t & 1); };
 
-  // Global -> registers for the k-block starting at k0 of the tile at (m0, n0).
-  auto fetch = [&](int64_t m0, int64_t n0, int64_t k0) {
+  // Global -> registers (or, for ASYNC operands, straight into shared buffer
+  // `buf`) for the k-block starting at k0 of the tile at (m0, n0).
+  auto fetch = [&](int64_t m0, int64_t n0, int64_t k0, int buf) {
 #pragma unroll
     for (int v = 0; v < AV; ++v) {
       const int f = t + v * NT;
@@ -172,16 +218,29 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
         const int64_t m = m0 + kc_row(v, BM), k = k0 + kc_kq(v, BM) * 4;
         load4(ra[v], Ap + m * K + k, a.vec_a, m < M, k, K);
       } else {
-        const int64_t k = k0 + f / (BM / 4), m = m0 + (f % (BM / 4)) * 4;
-        load4(ra[v], Ap + k * M + m, a.vec_a, k < K, m, M);
+        const int kr = f / (BM / 4), mr = (f % (BM / 4)) * 4;
+        const int64_t k = k0 + kr, m = m0 + mr;
+        if constexpr (kAsyncA) {
+          // rows are whole vectors: a run is inside or outside as a whole
+          const bool in = k < K && m < M;
+          cp_async16(&As[buf][kr][mr], in ? Ap + k * M + m : Ap, in);
+        } else {
+          load4(ra[v], Ap + k * M + m, a.vec_a, k < K, m, M);
+        }
       }
     }
 #pragma unroll
     for (int v = 0; v < BV; ++v) {
       const int f = t + v * NT;
       if (!B_COL) {
-        const int64_t k = k0 + f / (BN / 4), n = n0 + (f % (BN / 4)) * 4;
-        load4(rb[v], Bp + k * N + n, a.vec_b, k < K, n, N);
+        const int kr = f / (BN / 4), nr = (f % (BN / 4)) * 4;
+        const int64_t k = k0 + kr, n = n0 + nr;
+        if constexpr (kAsyncB) {
+          const bool in = k < K && n < N;
+          cp_async16(&Bs[buf][kr][nr], in ? Bp + k * N + n : Bp, in);
+        } else {
+          load4(rb[v], Bp + k * N + n, a.vec_b, k < K, n, N);
+        }
       } else {
         const int64_t n = n0 + kc_row(v, BN), k = k0 + kc_kq(v, BN) * 4;
         load4(rb[v], Bp + n * K + k, a.vec_b, n < N, k, K);
@@ -189,10 +248,11 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
     }
   };
 
-  // Registers -> shared buffer `buf`, as As[k][m] and Bs[k][n].
+  // Registers -> shared buffer `buf`, as As[k][m] and Bs[k][n] (operands that
+  // were copied directly are already there).
   auto stage = [&](int buf) {
 #pragma unroll
-    for (int v = 0; v < AV; ++v) {
+    for (int v = 0; v < AV && !kAsyncA; ++v) {
       const int f = t + v * NT;
       if (!A_COL) {
         const int m = kc_row(v, BM), k = kc_kq(v, BM) * 4;
@@ -205,7 +265,7 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
       }
     }
 #pragma unroll
-    for (int v = 0; v < BV; ++v) {
+    for (int v = 0; v < BV && !kAsyncB; ++v) {
       const int f = t + v * NT;
       if (!B_COL) {
         const int k = f / (BN / 4), n = (f % (BN / 4)) * 4;
@@ -217,6 +277,7 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
         for (int i = 0; i < 4; ++i) Bs[buf][k + i][n] = rb[v][i];
       }
     }
+    if constexpr (kAsyncA || kAsyncB) cp_async_wait_all();
   };
 
   // Epilogue: + bias[n]; rows ty*4+i (+BM/2), columns tx*4+j (+BN/2).
@@ -253,34 +314,46 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
     tile_coords(W, u.tile, tm, tn);
     const int64_t m0 = int64_t(tm) * BM, n0 = int64_t(tn) * BN;
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+      for (int j = 0; j < 8; ++j) P[i][j] = 0;  // two +0.0f
 
     // The previous unit ended with a barrier after its last shared reads, so
     // buffer 0 is free.
-    fetch(m0, n0, int64_t(u.kb0) * BK);
+    fetch(m0, n0, int64_t(u.kb0) * BK, 0);
     stage(0);
     __syncthreads();
     for (int32_t kt = u.kb0; kt < u.kb1; ++kt) {
       const int buf = (kt - u.kb0) & 1;
-      if (kt + 1 < u.kb1) fetch(m0, n0, int64_t(kt + 1) * BK);
+      // buffer buf^1 was last read before the barrier that ended the step before
+      if (kt + 1 < u.kb1) fetch(m0, n0, int64_t(kt + 1) * BK, buf ^ 1);
 #pragma unroll
       for (int kk = 0; kk < BK; ++kk) {
-        const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
-        const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][BM / 2 + ty * 4]);
+        // rows (ty*4 + {0,1}), (ty*4 + {2,3}), and the same BM/2 further on
+        const ulonglong2 a0 = *reinterpret_cast<const ulonglong2*>(&As[buf][kk][ty * 4]);
+        const ulonglong2 a1 =
+            *reinterpret_cast<const ulonglong2*>(&As[buf][kk][BM / 2 + ty * 4]);
+        // columns tx*4 + {0..3} and BN/2 + tx*4 + {0..3}, each as {b, b}
         const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
         const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][BN / 2 + tx * 4]);
-        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        const uint64_t av[4] = {a0.x, a0.y, a1.x, a1.y};
+        const uint64_t bv[8] = {dup2(b0.x), dup2(b0.y), dup2(b0.z), dup2(b0.w),
+                                dup2(b1.x), dup2(b1.y), dup2(b1.z), dup2(b1.w)};
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
-          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+          for (int j = 0; j < 8; ++j) fma2(P[i][j], av[i], bv[j]);
       }
       if (kt + 1 < u.kb1) stage(buf ^ 1);
       __syncthreads();
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        acc[2 * i][j] = __uint_as_float(uint32_t(P[i][j]));
+        acc[2 * i + 1][j] = __uint_as_float(uint32_t(P[i][j] >> 32));
+      }
 
     if (!unit_is_partial(W, u)) {
       store_tile(m0, n0);
@@ -340,20 +413,30 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
   }
 }
 
+template <typename TIn, typename TOut, int BM, int BN, bool A_COL, bool B_COL>
+cudaError_t launch_simt_layout(const SimtArgs& a, cudaStream_t s) {
+  constexpr int NT = (BM / 8) * (BN / 8);
+  const dim3 grid{unsigned(a.work.grid), 1u, 1u};
+  // direct copies for the 128-tile fp32 kernel when its m/n-contiguous
+  // operands have aligned rows (the 64-tile kernel has registers to spare)
+  constexpr bool kCanAsync = BM == 128 && std::is_same<TIn, float>::value && (A_COL || !B_COL);
+  if constexpr (kCanAsync) {
+    if ((!A_COL || a.vec_a) && (B_COL || a.vec_b)) {
+      simt_sgemm_kernel<TIn, TOut, BM, BN, A_COL, B_COL, true><<<grid, NT, 0, s>>>(a);
+      return cudaGetLastError();
+    }
+  }
+  simt_sgemm_kernel<TIn, TOut, BM, BN, A_COL, B_COL, false><<<grid, NT, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
 template <typename TIn, typename TOut, int BM, int BN>
 cudaError_t launch_simt_tile(const SimtArgs& a, int a_major, int b_major, cudaStream_t s) {
-  constexpr int NT = (BM / 8) * (BN / 8);
   if (a.work.grid <= 0) return cudaErrorInvalidConfiguration;
-  const dim3 grid{unsigned(a.work.grid), 1u, 1u};
-  if (a_major == 0 && b_major == 0)
-    simt_sgemm_kernel<TIn, TOut, BM, BN, false, false><<<grid, NT, 0, s>>>(a);
-  else if (a_major == 0)
-    simt_sgemm_kernel<TIn, TOut, BM, BN, false, true><<<grid, NT, 0, s>>>(a);
-  else if (b_major == 0)
-    simt_sgemm_kernel<TIn, TOut, BM, BN, true, false><<<grid, NT, 0, s>>>(a);
-  else
-    simt_sgemm_kernel<TIn, TOut, BM, BN, true, true><<<grid, NT, 0, s>>>(a);
-  return cudaGetLastError();
+  if (a_major == 0 && b_major == 0) return launch_simt_layout<TIn, TOut, BM, BN, false, false>(a, s);
+  if (a_major == 0) return launch_simt_layout<TIn, TOut, BM, BN, false, true>(a, s);
+  if (b_major == 0) return launch_simt_layout<TIn, TOut, BM, BN, true, false>(a, s);
+  return launch_simt_layout<TIn, TOut, BM, BN, true, true>(a, s);
 }
 
 inline bool aligned_to(const void* p, uintptr_t n) {
