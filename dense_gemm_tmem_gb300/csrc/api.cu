@@ -866,9 +866,19 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, co
   a.wait_limit_ns = h->opt.wait_limit_ns;
   a.a_mn = plan.a_mn_major;
   a.b_mn = plan.b_mn_major;
-  // row-major output chunks of 32 columns leave by TMA store when C allows it
+  // Row-major output chunks of 32 columns leave by TMA store when C allows it.
+  // By default only for fp16 output or launches with more output tiles than
+  // CTAs: an fp32 single-wave launch measured faster with staged plain stores
+  // (graph replay, cold inputs, us per launch: 512^3 6.64 vs 6.92, 256^3 5.55
+  // vs 5.91, one 128 x 128 tile 4.04 vs 4.41; fp16 output even).
   std::memset(&L.tmC, 0, sizeof(L.tmC));
-  a.c_tma = (h->opt.tma_store && !swap && plan.tile_n >= 32 &&
+  const int64_t out_tiles = int64_t(plan.tiles_m) * plan.tiles_n;
+  const bool tma_wanted =
+      h->opt.tma_store > 0 ||
+      (h->opt.tma_store < 0 &&
+       (layout.out_dtype == GEMM_F16 ||
+        out_tiles * (plan.kernel == GEMM_KERNEL_TC2 ? 2 : 1) > plan.grid));
+  a.c_tma = (tma_wanted && !swap && plan.tile_n >= 32 &&
              plan.kernel != GEMM_KERNEL_SPLITC &&
              dg::encode_output(h, &L.tmC, C, M, N, layout.out_dtype == GEMM_F16))
                 ? 1

@@ -25,7 +25,8 @@ struct Options {
   int csplit = -1;         // cluster split: -1 picker's rule, 0 never, 2/4/8 forced
   int pdl = 1;             // programmatic dependent launch of the tensor-core kernels
   int pair_split = -1;     // two-SM kernel k-split: -1/0 none, 1 all tiles, 2 the tail
-  int tma_store = 1;       // epilogue output by TMA store where C allows it
+  int tma_store = -1;      // epilogue output by TMA store where C allows it: -1 for fp16
+                           // output or more output tiles than CTAs, 1 always, 0 never
   int bias_init = 0;       // seed the accumulators with the bias
   int csplit_clusters[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};  // clusters of s resident (0: SMs/s)
   int simt_per_sm = 0;     // 128 x 128 CUDA-core CTAs resident per SM (0: 2); set per device

@@ -106,6 +106,16 @@ def test_plain_store_path(g, dev, kernel, odt):
     full_check(g, dev, p)
 
 
+@pytest.mark.parametrize("kernel", [TC, SK, TC2])
+@pytest.mark.parametrize("odt", [F16, F32])
+def test_tma_store_path_forced(g, dev, kernel, odt):
+    """GEMM_OPT_TMA_STORE = 1: TMA stores even where the default takes plain
+    stores (fp32 output on a single wave of tiles)."""
+    set_opts(g, kernel=kernel, tma_store=1)
+    p = problem(296, 520, 200, 0, 1, F16, odt, True, 162 + (odt == F32))
+    full_check(g, dev, p)
+
+
 @pytest.mark.parametrize("kernel", [TC, TC2])
 @pytest.mark.parametrize("odt", [F16, F32])
 def test_output_pitch_not_16_bytes(g, dev, kernel, odt):
