@@ -25,6 +25,7 @@ from .gemm import Gemm
 
 L2_BYTES = 129 * 10**6
 SHAPES = [(8192, True, True), (16384, False, False)]  # (n, B column-major, bias)
+LAYOUT_SHAPES = [(8192, True, False), (8192, False, False), (16384, True, False)]
 
 
 def _operands(n, bcol, copies, dev):
@@ -66,9 +67,9 @@ def _graph(fn, launches, dev):
     return gr
 
 
-def compare(dev) -> None:
+def compare(dev, shapes=SHAPES) -> None:
     g = Gemm(dev)
-    for n, bcol, bias in SHAPES:
+    for n, bcol, bias in shapes:
         copies = max(2, -(-3 * L2_BYTES // (3 * n * n * 2)))
         sets = _operands(n, bcol, copies, dev)
         b32 = torch.randn(n, device=dev) if bias else None
@@ -91,7 +92,8 @@ def compare(dev) -> None:
                     us = e0.elapsed_time(e1) * 1e3 / k
                     res.setdefault("%s_%s" % (w, r), []).append(round(flops / us / 1e6, 1))
         g.status()
-        print("%d^3" % n, json.dumps(res), "launches: %s" % json.dumps(runs), flush=True)
+        print("%d^3 B %s%s" % (n, "col" if bcol else "row", " +bias" if bias else ""), json.dumps(res),
+              "launches: %s" % json.dumps(runs), flush=True)
         del sets, graphs
         torch.cuda.empty_cache()
     g.close()
@@ -116,12 +118,14 @@ def main():
     ap.add_argument("--only", choices=["ours", "cublas"])
     ap.add_argument("--launches", type=int, default=4)
     ap.add_argument("--n", type=int, default=8192)
+    ap.add_argument("--layouts", action="store_true",
+                    help="B row- vs column-major without bias (8192^3, and 16384^3 column-major)")
     a = ap.parse_args()
     dev = torch.device("cuda", 0)
     if a.only:
         plain(dev, a.only, a.launches, a.n)
     else:
-        compare(dev)
+        compare(dev, LAYOUT_SHAPES if a.layouts else SHAPES)
 
 
 if __name__ == "__main__":
