@@ -117,7 +117,8 @@ template <int S>
 __device__ __forceinline__ void tc2_producer(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                              const TcArgs& args, uint8_t* sA, uint8_t* sB,
                                              uint64_t* full, uint64_t* empty, const WaitCtl& wc,
-                                             uint32_t rank, int32_t cluster_id) {
+                                             uint32_t rank, int32_t cluster_id,
+                                             uint64_t t_entry) {
   using Cfg = Tc2Config;
   const WorkSpec& W = args.work;
   WorkIter it;
@@ -126,6 +127,15 @@ __device__ __forceinline__ void tc2_producer(const CUtensorMap& tmA, const CUten
   int s = 0;
   uint32_t ph = 0, issued = 0, issued_par = 0;
   bool ok = true;
+  bool waited = false;
+  auto prerequisites_done = [&]() {  // thread 0 of the CTA
+    pdl_wait_prerequisites();
+    waited = true;
+    if (args.trace) {
+      args.trace[size_t(blockIdx.x) * kTraceSlots + kTraceEntry] = t_entry;
+      trace_mark(args, blockIdx.x, kTraceStart);
+    }
+  };
   const int32_t row_off = int32_t(rank) * kBM;      // this CTA's rows of the A tile
   const int32_t col_off = int32_t(rank) * kHalfBN;  // this CTA's columns of the B tile
   int32_t nunit = 0;
@@ -145,6 +155,7 @@ __device__ __forceinline__ void tc2_producer(const CUtensorMap& tmA, const CUten
         ok = false;
         break;
       }
+      if (!waited) prerequisites_done();  // the first load: the operands are now final
       const uint32_t fb_local = smem_u32(&full[s]);
       if (rank == 0) mbar_arrive_expect_tx(fb_local, 2 * Cfg::kStageBytes);
       const uint32_t fb = map_to_rank(fb_local, 0);
@@ -172,6 +183,7 @@ __device__ __forceinline__ void tc2_producer(const CUtensorMap& tmA, const CUten
       }
     }
   }
+  if (!waited) prerequisites_done();  // no load at all
   if (!ok) {
     if (rank == 0) {
       for (int t = 0; t < S; ++t)
@@ -357,6 +369,7 @@ __device__ __forceinline__ void tc2_epilogue(const TcArgs& args, uint64_t* acc_f
   WorkIter it, ahead;
   it.init_tc(W, cluster_id);
   ahead.init_tc(W, cluster_id);
+  pdl_wait_prerequisites();  // the bias (seeding), C and the workspace are global
   Unit u, un;
   auto release = [&](int buf, bool have_next) {
     if (have_next && args.bias_init && un.kb0 == 0) {
@@ -471,18 +484,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   cluster_sync_all();  // both CTAs' barriers initialised and TMEM allocated
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // global memory only after the kernels before this one have completed
+  // Global memory only after the kernels before this one have completed; the
+  // producer first prepares its first load (work iterator, coordinates, free
+  // stage), which with a programmatic launch overlaps the previous kernel.
   pdl_launch_dependents();
-  pdl_wait_prerequisites();
   const WaitCtl wc{args.wait_limit_ns, args.status, abort_flag};
-  if (threadIdx.x == 0 && args.trace) {
-    args.trace[size_t(blockIdx.x) * kTraceSlots + kTraceEntry] = t_entry;
-    trace_mark(args, blockIdx.x, kTraceStart);
-  }
 
   if (warp == 0) {
-    if (lane == 0) tc2_producer<S>(tmA, tmB, args, sA, sB, full, empty, wc, rank, cluster_id);
+    if (lane == 0)
+      tc2_producer<S>(tmA, tmB, args, sA, sB, full, empty, wc, rank, cluster_id, t_entry);
+    else
+      pdl_wait_prerequisites();
   } else if (warp == 1) {
+    pdl_wait_prerequisites();
     if (lane == 0 && rank == 0)
       tc2_mma<S>(args, sA, sB, full, empty, acc_full, acc_empty, drain, wc, tmem_base,
                  cluster_id);

@@ -573,17 +573,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // Up to here only this CTA's own resources were touched.  Let the next
-  // kernel of the stream start its prologue, and touch global memory
-  // (operands, C, workspace, counters, status, trace) only once the kernels
-  // before this one have completed.
+  // kernel of the stream start its prologue.  Each role then does what needs
+  // only this CTA's own resources (work iterators, the first unit's
+  // coordinates, the first free stage) and waits for the kernels before this
+  // one to complete before it touches global memory (operands, C, workspace,
+  // counters, status, trace): with a programmatic launch that preparation
+  // overlaps the previous kernel instead of following it.
   pdl_launch_dependents();
-  pdl_wait_prerequisites();
   const WaitCtl wc{args.wait_limit_ns, args.status, abort_flag};
   const WorkSpec& W = args.work;
-  if (threadIdx.x == 0 && args.trace) {
-    args.trace[size_t(blockIdx.x) * kTraceSlots + kTraceEntry] = t_entry;
-    trace_mark(args, blockIdx.x, kTraceStart);
-  }
+  auto prerequisites_done = [&]() {
+    pdl_wait_prerequisites();
+    if (threadIdx.x == 0 && args.trace) {
+      args.trace[size_t(blockIdx.x) * kTraceSlots + kTraceEntry] = t_entry;
+      trace_mark(args, blockIdx.x, kTraceStart);
+    }
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
@@ -595,6 +600,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t ph = 0, issued = 0, issued_par = 0;
       bool ok = true;
       bool first = true;
+      bool waited = false;
       while (ok && it.next(W, u)) {
         int32_t tm, tn;
         tile_coords(W, u.tile, tm, tn);
@@ -602,6 +608,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (!wait_bounded(smem_u32(&empty[s]), ph ^ 1, wc, kSiteProducer)) {
             ok = false;
             break;
+          }
+          if (!waited) {  // the first load: the operands are now final
+            prerequisites_done();
+            waited = true;
           }
           const uint32_t fb = smem_u32(&full[s]);
           mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
@@ -635,13 +645,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       }
+      if (!waited) prerequisites_done();  // no load at all
       if (!ok) {  // let the copies still in flight land before the CTA exits
         for (int t = 0; t < S; ++t)
           if ((issued >> t) & 1) wait_drain(smem_u32(&full[t]), (issued_par >> t) & 1, wc);
       }
+    } else {
+      pdl_wait_prerequisites();
     }
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer --
+    pdl_wait_prerequisites();
     if (lane == 0) {
       WorkIter it;
       it.init_tc(W, blockIdx.x);
@@ -708,6 +722,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     WorkIter it, ahead;
     it.init_tc(W, blockIdx.x);
     ahead.init_tc(W, blockIdx.x);
+    pdl_wait_prerequisites();  // the bias (seeding), C and the workspace are global
     Unit u, un;
     auto release = [&](int buf, bool have_next) {
       if (have_next && args.bias_init && un.kb0 == 0) {
