@@ -137,9 +137,13 @@ int plan_simt(int64_t M, int64_t N, int64_t K, int num_sms, const Options& o, ge
 //  * fp16 inputs whose leading dimensions (or, in gemm_run, base addresses)
 //    break the TMA rules -> the same CUDA-core kernel, fp16 widened to fp32.
 //  * fp16 inputs -> tcgen05 kernels.  Shapes with at least half as many
-//    256x256 tiles as CTA pairs -> the two-SM kernel.  Skinny M (M <= 128,
+//    256x256 tiles as CTA pairs -> the two-SM kernel.  Skinny M (M <= 64,
 //    N >= 2M, A row-major) swaps the operands so N fills the 128-row MMA side
-//    and M becomes the MMA N side (16/32/64/128 columns).  Otherwise the tile
+//    and M becomes the MMA N side (16/32/64 columns).  Measured (N = K =
+//    4096, graph replay, cold inputs, us per launch, swapped vs not): M = 32
+//    10.3 vs 12.8, 64 10.9 vs 12.9, but 80 13.0 vs 12.9, 128 13.6 vs 13.1 --
+//    beyond 64 the swapped tile is 128 wide either way and its partials no
+//    longer fit the push path.  Otherwise the tile
 //    is 128x256 (128x128 when N <= 128 or when 256-wide tiles would fill fewer
 //    than half the SMs).
 //  * Decomposition of the one-SM kernel (the k-split the leiblog.wang
@@ -185,7 +189,7 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
   const bool forced_pair = o.force_kernel == GEMM_KERNEL_TC2;
   const bool swap = o.force_swap >= 0 ? (o.force_swap != 0)
                     : forced_pair     ? false
-                                      : (L.a_major == GEMM_ROW_MAJOR && M <= 128 && N >= 2 * M);
+                                      : (L.a_major == GEMM_ROW_MAJOR && M <= 64 && N >= 2 * M);
   const int64_t Mm = swap ? N : M;
   const int64_t Nm = swap ? M : N;
   const int a_mn = swap ? (L.b_major == GEMM_ROW_MAJOR) : (L.a_major == GEMM_COL_MAJOR);

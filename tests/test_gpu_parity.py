@@ -150,7 +150,10 @@ def test_tc_tile_widths(g, dev, tile_n, kernel):
 @pytest.mark.parametrize("bm", [0, 1])
 @pytest.mark.parametrize("odt", [F16, F32])
 def test_swapped_skinny(g, dev, M, bm, odt):
-    """Skinny M runs with swapped operands (Cᵀ = Bᵀ·Aᵀ) and a transposed store."""
+    """Skinny M runs with swapped operands (Cᵀ = Bᵀ·Aᵀ) and a transposed store:
+    by the picker's choice up to M = 64, forced beyond."""
+    if M > 64:
+        set_opts(g, swap=1)
     p = problem(M, 1000, 520, 0, bm, F16, odt, True, 30 + M)
     pl = g.plan(M, 1000, 520, 0, bm, B.GEMM_F16, B.GEMM_F16 if odt == F16 else B.GEMM_F32)
     assert pl["swap_ab"] == 1

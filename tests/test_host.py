@@ -163,7 +163,16 @@ def test_split_granularity_per_tile_width(bn, iters):
     assert iters == -(-4 * 128 * bn * 4 // ((128 + bn) * 64 * 2))
 
 
-@pytest.mark.parametrize("M,bn", [(1, 16), (16, 16), (64, 64), (128, 128)])
+def test_picker_m128_keeps_operands():
+    """M = 128 fills the MMA's 128 rows: no swap (measured faster than the
+    swapped 128-wide tile); 32 tiles of 128 x 128 in clusters of 4."""
+    rc, p = plan(128, 4096, 4096)
+    assert rc == 0 and p.swap_ab == 0 and p.tile_n == 128
+    assert p.kernel == B.GEMM_KERNEL_SPLITC and p.cluster_split == 4
+    assert (p.tiles_m, p.tiles_n, p.grid) == (1, 32, 128)
+
+
+@pytest.mark.parametrize("M,bn", [(1, 16), (16, 16), (64, 64)])
 def test_picker_skinny_swaps_operands(M, bn):
     rc, p = plan(M, 4096, 4096)
     assert rc == 0 and p.swap_ab == 1 and p.tile_n == bn
