@@ -511,7 +511,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
-    if (lane == 0) trace_mark(args, blockIdx.x, kTraceExit);
+  }
+  if (args.trace) {  // the exit stamp after the TMEM is freed, by the end's thread
+    __syncthreads();
+    if (threadIdx.x == kStampThread) trace_mark(args, blockIdx.x, kTraceExit);
   }
 }
 

@@ -101,9 +101,13 @@ enum TracePhase : int {
   kTraceEntry = 8,      // kernel entry (taken first, written after the prerequisite wait)
   kTraceExit = 9,       // TMEM freed, about to return
   kTraceClusterParked = 10,   // cluster split: every CTA of the cluster parked its partial
-  kTraceClusterReduced = 11,  // cluster split: thread 0's share of the reduction stored
+  kTraceClusterReduced = 11,  // cluster split: the stamping thread's share of the reduction stored
   kTraceSlots = 12
 };
+
+// The thread that stamps the end of the epilogue and everything after it
+// (the first epilogue thread).
+constexpr int kStampThread = 64;
 
 __device__ __forceinline__ void trace_mark(const TcArgs& a, uint32_t cta, int phase) {
   if (a.trace) a.trace[size_t(cta) * kTraceSlots + phase] = globaltimer_ns();
@@ -903,24 +907,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // Every thread of every CTA of the cluster reaches the barriers, aborted
     // or not, so none can wait forever.
     cluster_sync_all();  // all partials parked (or pushed to their owners)
-    if (threadIdx.x == 0) trace_mark(args, blockIdx.x, kTraceClusterParked);
+    // the tail's stamps come from the thread that stamped the epilogue's end,
+    // so they are ordered however the timer reads are scheduled
+    if (threadIdx.x == kStampThread) trace_mark(args, blockIdx.x, kTraceClusterParked);
     if constexpr (TRANS && kPushReduce<BN>) {
       csplit_reduce_pushed<BN, OUT_F16>(args, stage, threadIdx.x, kTcThreads);
-      if (threadIdx.x == 0) {
+      if (threadIdx.x == kStampThread) {
         trace_mark(args, blockIdx.x, kTraceClusterReduced);
         trace_mark(args, blockIdx.x, kTraceClusterDone);
       }
     } else {
       csplit_reduce<BN, OUT_F16, TRANS>(args, smem, threadIdx.x, kTcThreads);
-      if (threadIdx.x == 0) trace_mark(args, blockIdx.x, kTraceClusterReduced);
+      if (threadIdx.x == kStampThread) trace_mark(args, blockIdx.x, kTraceClusterReduced);
       cluster_sync_all();  // no CTA still reads another's shared memory
-      if (threadIdx.x == 0) trace_mark(args, blockIdx.x, kTraceClusterDone);
+      if (threadIdx.x == kStampThread) trace_mark(args, blockIdx.x, kTraceClusterDone);
     }
   }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::kTmemCols);
-    if (lane == 0) trace_mark(args, blockIdx.x, kTraceExit);
+  }
+  if (args.trace) {  // the exit stamp after the TMEM is freed
+    __syncthreads();
+    if (threadIdx.x == kStampThread) trace_mark(args, blockIdx.x, kTraceExit);
   }
 }
 

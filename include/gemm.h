@@ -181,7 +181,7 @@ int gemm_status_detail(gemm_handle_t h);
  * accumulator committed, 4 last accumulator received by the epilogue,
  * 5 epilogue done, 10 cluster split: every CTA of the cluster parked its
  * partial, 11 cluster split: this CTA's share of the reduction stored (by
- * thread 0), 7 cluster split: the whole cluster done, 9 TMEM freed (about to
+ * thread 64), 7 cluster split: the whole cluster done, 9 TMEM freed (about to
  * return); slot 6 holds the CTA's work-unit count.  Slots a CTA
  * never reaches (e.g. the MMA slots of the second CTA of a pair) are not
  * written.  Launches with more CTAs than `ctas` are not traced.
