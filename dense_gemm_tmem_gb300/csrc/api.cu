@@ -288,8 +288,8 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
   if (!bn_ok || (b_mn && bn % 64 != 0)) return GEMM_ERR_UNSUPPORTED;
 
   const int64_t tiles_m = ceil_div(Mm, kBM);
-  const int64_t tiles_n = ceil_div(Nm, bn);
-  const int64_t T = tiles_m * tiles_n;
+  int64_t tiles_n = ceil_div(Nm, bn);
+  int64_t T = tiles_m * tiles_n;
   const int64_t I = ceil_div(K, kBK);
   if (T > INT32_MAX / 2 || I > INT32_MAX / 2 || T * I > (int64_t(1) << 40))
     return GEMM_ERR_UNSUPPORTED;
@@ -298,30 +298,59 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
   const int64_t max_grid = o.force_grid > 0 ? std::min<int64_t>(o.force_grid, G) : G;
 
   // Cluster split: when the tiles fill few SMs, each tile's k-blocks are split
-  // over a cluster of s CTAs (8, 4 or 2: the largest whose clusters all fit at
-  // once and leave every CTA >= 2 k-blocks).  The CTAs of a cluster add their
-  // fp32 partials through distributed shared memory: no global workspace, and
-  // the hardware co-schedules the cluster, so its barrier always completes.
+  // over a cluster of s CTAs (8, 4 or 2, whose clusters all fit at once and
+  // leave every CTA >= 2 k-blocks).  The CTAs of a cluster add their fp32
+  // partials through distributed shared memory: no global workspace, and the
+  // hardware co-schedules the cluster, so its barrier always completes.
   {
     const bool forced = o.force_kernel == GEMM_KERNEL_SPLITC;
     int64_t cs = 0;
-    auto fits = [&](int s) {
+    auto fits = [&](int64_t tiles, int s) {
       // capacity: measured clusters resident at once; 0 = unknown (SMs / s); < 0 = none
       const int64_t cap = o.csplit_clusters[s] != 0 ? o.csplit_clusters[s] : G / s;
-      return cap > 0 && T <= cap && T * s <= G;
+      return cap > 0 && tiles <= cap && tiles * s <= G;
     };
     if (forced) {
       cs = o.csplit >= 2 ? o.csplit : 4;
       if (I < cs) return GEMM_ERR_UNSUPPORTED;
     } else if (o.force_kernel < 0 && o.csplit != 0 && o.force_grid <= 0 && T < G && !narrow) {
       if (o.csplit >= 2) {
-        if (fits(o.csplit) && I >= 2 * o.csplit) cs = o.csplit;
+        if (fits(T, o.csplit) && I >= 2 * o.csplit) cs = o.csplit;
       } else {
-        for (int s : {8, 4, 2})
-          if (fits(s) && I >= 2 * s) {
-            cs = s;
-            break;
+        // Tile width and cluster size by the per-CTA cost: the operand bytes
+        // it loads, (128 + w) x 128 B per k-block over ceil(I / s) k-blocks,
+        // plus the fp32 partial bytes it exchanges, 128 x w x 4 B x (s-1)/s,
+        // weighted 3x (distributed shared memory moves them about that much
+        // slower per SM than TMA loads operands).  Widths: the picker's, and
+        // 64 for unswapped tiles wider than that.  Measured best on all of
+        // (graph replay, cold inputs, us per launch, picked vs the old rule's
+        // widest tile with the largest fitting split): 512x512x1024 7.3 vs 8.0,
+        // 512x512x2048 8.4 vs 9.2, 384x384x2048 7.6 vs 8.2, 512x512x8192 15.2
+        // vs 16.4, 256x256x1024 6.1 vs 7.2; unchanged where 128-wide tiles
+        // were best (512x1024x2048, 768x768x1536, 1024x1024x2048/8192,
+        // 256x512x4096).
+        int best_w = 0;
+        double best_cost = 0;
+        for (int w : {bn, (!swap && o.force_tile_n <= 0 && bn > 64) ? 64 : 0}) {
+          if (w == 0) continue;
+          const int64_t tw = tiles_m * ceil_div(Nm, w);
+          if (tw >= G) continue;
+          for (int sz : {8, 4, 2}) {
+            if (!fits(tw, sz) || I < 2 * sz) continue;
+            const double cost = double(kBM + w) * kBK * 2 * double(ceil_div(I, sz)) +
+                                3.0 * kBM * w * 4 * double(sz - 1) / sz;
+            if (cs == 0 || cost < best_cost) {
+              best_w = w;
+              cs = sz;
+              best_cost = cost;
+            }
           }
+        }
+        if (cs > 1 && best_w != bn) {
+          bn = best_w;
+          tiles_n = ceil_div(Nm, bn);
+          T = tiles_m * tiles_n;
+        }
       }
     }
     if (cs > 1) {

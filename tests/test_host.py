@@ -139,11 +139,16 @@ def test_picker_small_shapes():
     assert (p.grid, p.dp_tiles, p.sk_tiles, p.workspace_bytes) == (32, 32, 0, 0)
     rc, p = plan(1024, 1024, 768)  # 12 k-blocks: still narrow whole tiles
     assert (p.kernel, p.tile_n, p.grid) == (B.GEMM_KERNEL_TC, 64, 128)
-    # 16 k-blocks: 16 tiles of 128, clusters of 8 CTAs split every tile (2 k-blocks each)
+    # 16 k-blocks: 32 tiles 64 columns wide in clusters of 4 (4 k-blocks each)
+    # cost less per CTA than 16 tiles of 128 in clusters of 8: fewer operand
+    # bytes (192 x 4 vs 256 x 2 rows of k-blocks) and far fewer partial bytes
     rc, p = plan(512, 512, 1024)
     assert rc == 0 and p.kernel == B.GEMM_KERNEL_SPLITC
-    assert (p.tile_n, p.tiles_m, p.tiles_n, p.k_iters) == (128, 4, 4, 16)
-    assert (p.cluster_split, p.grid, p.sk_tiles, p.workspace_bytes) == (8, 128, 16, 0)
+    assert (p.tile_n, p.tiles_m, p.tiles_n, p.k_iters) == (64, 4, 8, 16)
+    assert (p.cluster_split, p.grid, p.sk_tiles, p.workspace_bytes) == (4, 128, 32, 0)
+    # the cost rule keeps 128-wide tiles where they load less per CTA
+    rc, p = plan(512, 1024, 2048)
+    assert (p.kernel, p.tile_n, p.cluster_split, p.grid) == (B.GEMM_KERNEL_SPLITC, 128, 4, 128)
     # deep K: 16 tiles in clusters of 8
     rc, p = plan(512, 512, 8192)
     assert rc == 0 and p.kernel == B.GEMM_KERNEL_SPLITC
