@@ -242,6 +242,29 @@ def test_cluster_split_layouts(g, dev, csplit, am, bm, odt):
     full_check(g, dev, p)
 
 
+@pytest.mark.parametrize("csplit", [2, 4, 8])
+@pytest.mark.parametrize("am,bm", [(0, 0), (1, 1)])
+@pytest.mark.parametrize("odt", [F16, F32])
+def test_cluster_split_narrow_unswapped(g, dev, csplit, am, bm, odt):
+    """64-column unswapped tiles split over clusters (the parked partials of a
+    64-wide tile, rows of 68 floats), with ragged M, N and K."""
+    set_opts(g, kernel=SPLITC, csplit=csplit, tile_n=64)
+    p = problem(296, 200, 1032, am, bm, F16, odt, True, 170 + csplit + am)
+    pl = g.plan(296, 200, 1032, am, bm, B.GEMM_F16, B.GEMM_F16 if odt == F16 else B.GEMM_F32)
+    assert pl["kernel"] == SPLITC and pl["cluster_split"] == csplit and pl["tile_n"] == 64
+    full_check(g, dev, p)
+
+
+@pytest.mark.parametrize("M,N,K,w", [(512, 512, 1024, 64), (384, 384, 2048, 64),
+                                     (256, 256, 1024, 64), (512, 1024, 2048, 128)])
+def test_cluster_split_picker_widths(g, dev, M, N, K, w):
+    """The picker's own cluster splits (width and size by per-CTA cost)."""
+    p = problem(M, N, K, 0, 1, F16, F32, True, 180 + M + K)
+    pl = g.plan(M, N, K, 0, 1, B.GEMM_F16, B.GEMM_F32)
+    assert pl["kernel"] == SPLITC and pl["tile_n"] == w and pl["swap_ab"] == 0
+    full_check(g, dev, p)
+
+
 @pytest.mark.parametrize("tile_n", [16, 32, 64, 128])
 @pytest.mark.parametrize("csplit", [2, 4, 8])
 @pytest.mark.parametrize("odt", [F16, F32])
