@@ -1,4 +1,4 @@
-// Instantiations with a 128-column MMA tile (mid shapes; swapped M <= 128).
+// Instantiations with a 128-column MMA tile (mid shapes; swapped skinny M up to 128 when forced).
 #include "tc_launch.cuh"
 
 namespace dg {
