@@ -500,12 +500,17 @@ __device__ __forceinline__ void csplit_reduce_pushed(const TcArgs& a, const uint
   for (int g = tid; g < groups; g += nthreads) {
     const int col = g / (R / 4);
     const int r4 = (g % (R / 4)) * 4;
-    float4 acc = *reinterpret_cast<const float4*>(slot + (0 * BN + col) * R + r4);
-#pragma unroll 1
-    for (int src = 1; src < s; ++src) {
-      const float4 v = *reinterpret_cast<const float4*>(slot + (src * BN + col) * R + r4);
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-    }
+    // all s slots' loads in flight at once, added in source order
+    float4 part[8];
+#pragma unroll
+    for (int src = 0; src < 8; ++src)
+      if (src < s) part[src] = *reinterpret_cast<const float4*>(slot + (src * BN + col) * R + r4);
+    float4 acc = part[0];
+#pragma unroll
+    for (int src = 1; src < 8; ++src)
+      if (src < s) {
+        acc.x += part[src].x; acc.y += part[src].y; acc.z += part[src].z; acc.w += part[src].w;
+      }
     const int32_t mm = tm * kBM + rank * R + r4;  // MMA-view row: C column
     const int32_t nn = tn * BN + col;             // MMA-view column: C row
     if (mm >= a.Mm || nn >= a.Nm) continue;
