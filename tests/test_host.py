@@ -168,6 +168,15 @@ def test_split_granularity_per_tile_width(bn, iters):
     assert iters == -(-4 * 128 * bn * 4 // ((128 + bn) * 64 * 2))
 
 
+@pytest.mark.parametrize("M,swapped", [(1, 1), (64, 1), (65, 0), (96, 0)])
+def test_picker_swap_boundary(M, swapped):
+    """Operands swap for skinny M up to 64 only (row-major A, N >= 2M)."""
+    rc, p = plan(M, 4096, 4096)
+    assert rc == 0 and p.swap_ab == swapped
+    rc, p = plan(M, 4096, 4096, 1, 0)  # column-major A: never swapped
+    assert rc == 0 and p.swap_ab == 0
+
+
 def test_picker_m128_keeps_operands():
     """M = 128 fills the MMA's 128 rows: no swap (measured faster than the
     swapped 128-wide tile); 32 tiles of 128 x 128 in clusters of 4."""
