@@ -20,6 +20,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -111,8 +112,8 @@ class ClockSampler:
 
     def start(self):
         try:
-            out_dir = os.path.join(ROOT, "gpurun_out") if os.path.isdir(
-                os.path.join(ROOT, "gpurun_out")) else "/tmp"
+            # the raw samples (the JSON line carries their summary)
+            out_dir = os.environ.get("BENCH_CLOCKS_DIR") or tempfile.gettempdir()
             self.path = os.path.join(out_dir, "clocks_%d_%d.csv" % (os.getpid(), self.gpu))
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
