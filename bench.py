@@ -61,6 +61,22 @@ def flops_of(M, N, K):
     return 2.0 * M * N * K
 
 
+def slowest_rank_ms(elapsed_ms, device, dist=None):
+    """The timed region's length on the slowest rank (all ranks get it): the
+    whole job is done when the last replica is."""
+    import torch
+    t = torch.tensor([float(elapsed_ms)], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world, steps, step_flops, elapsed_ms):
+    """Every rank's steps over the slowest rank's time (weak scaling: each
+    replica runs the same workload)."""
+    return world * steps * step_flops / (elapsed_ms * 1e-3) / 1e12
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -345,12 +361,9 @@ def run_ours(args):
         per_launch_ms = [elapsed_ms / args.steps]  # back-to-back launches inside the replay
     else:
         per_launch_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
-    elapsed = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(elapsed, op=dist.ReduceOp.MAX)
-    elapsed_ms = float(elapsed.item())
+    elapsed_ms = slowest_rank_ms(elapsed_ms, dev, dist)
     step_flops = flops_of(p.M, p.N, p.K)
-    value = world * args.steps * step_flops / (elapsed_ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, args.steps, step_flops, elapsed_ms)
 
     # roofline of the one kernel per step
     avg_launch_s = statistics.mean(per_launch_ms) * 1e-3
@@ -434,11 +447,9 @@ def run_ours(args):
         for i in range(e_steps):
             e2e_step(i)
         barrier()
-        e_dt = torch.tensor([time.perf_counter() - t0], dtype=torch.float64, device=dev)
-        if dist is not None:
-            dist.all_reduce(e_dt, op=dist.ReduceOp.MAX)
+        e_ms = slowest_rank_ms((time.perf_counter() - t0) * 1e3, dev, dist)
         g.status(stream)
-        e2e = {"value": world * e_steps * step_flops / float(e_dt.item()) / 1e12,
+        e2e = {"value": whole_job_tflops(world, e_steps, step_flops, e_ms),
                "unit": "TFLOP/s", "h2d_bytes_per_step": bytes_a + bytes_b + bytes_bias,
                "d2h_bytes_per_step": bytes_c, "steps": e_steps,
                "pipelining": "two device slots; copy-in, compute and copy-out streams"}
