@@ -398,61 +398,43 @@ def run_ours(args):
     roof["traffic"] = traffic
     roof["algorithmic_bytes"] = step_bytes
 
-    # end to end through the public API: every step copies its inputs from
-    # pinned host memory, runs, and copies its result back to pinned host
-    # memory.  Steps are pipelined over two device slots and three streams
-    # (copy in, compute, copy out), so step i+1's inputs travel while step i
-    # computes and step i-1's result comes back.
+    # end to end through the C ABI with host buffers: every step is one
+    # gemm_run_host call, which copies A, B and bias in from pinned host
+    # memory, runs, and copies C back, all on its stream.  Steps alternate
+    # between two handles on two streams, so step i+1's inputs travel while
+    # step i computes and its result comes back.
     e2e = None
     if not args.no_e2e:
-        slots = [sets[0]]
-        if copies >= 2:
-            slots.append(sets[1])
-        else:
-            slots.append((torch.empty_like(sets[0][0]), torch.empty_like(sets[0][1]),
-                          None if sets[0][2] is None else torch.empty_like(sets[0][2]),
-                          torch.empty_like(sets[0][3])))
+        hs = [g, Gemm(dev)]
+        ss = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
         hCs = [torch.empty((p.M, p.N), dtype=out_t).pin_memory() for _ in range(2)]
-        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        in_done = [torch.cuda.Event() for _ in range(2)]
-        run_done = [torch.cuda.Event() for _ in range(2)]
-        out_done = [torch.cuda.Event() for _ in range(2)]
-        for e in run_done + out_done:
-            e.record(stream)
 
         def e2e_step(i):
             k = i % 2
-            A, Bd, bias, C = slots[k]
-            s_in.wait_event(run_done[k])  # slot's operands no longer read
-            with torch.cuda.stream(s_in):
-                A.copy_(hA, non_blocking=True)
-                Bd.copy_(hB, non_blocking=True)
-                if bias is not None:
-                    bias.copy_(hbias, non_blocking=True)
-            in_done[k].record(s_in)
-            stream.wait_event(in_done[k])
-            stream.wait_event(out_done[k])  # slot's previous result read out
-            g.run(A, Bd, C, bias, p.a_major, p.b_major, stream=stream)
-            run_done[k].record(stream)
-            s_out.wait_event(run_done[k])
-            with torch.cuda.stream(s_out):
-                hCs[k].copy_(C, non_blocking=True)
-            out_done[k].record(s_out)
+            hs[k].run_host(hA, hB, hCs[k], hbias, p.a_major, p.b_major, stream=ss[k])
 
         e_steps = max(3, min(args.steps, 50))
         for i in range(2):
             e2e_step(i)
+        for s in ss:
+            s.synchronize()
         barrier()
         t0 = time.perf_counter()
         for i in range(e_steps):
             e2e_step(i)
+        for s in ss:
+            s.synchronize()
         barrier()
         e_ms = slowest_rank_ms((time.perf_counter() - t0) * 1e3, dev, dist)
-        g.status(stream)
+        for h, s in zip(hs, ss):
+            h.status(s)
+        for h in hs[1:]:
+            h.close()
         e2e = {"value": whole_job_tflops(world, e_steps, step_flops, e_ms),
                "unit": "TFLOP/s", "h2d_bytes_per_step": bytes_a + bytes_b + bytes_bias,
                "d2h_bytes_per_step": bytes_c, "steps": e_steps,
-               "pipelining": "two device slots; copy-in, compute and copy-out streams"}
+               "api": "gemm_run_host (pinned host buffers)",
+               "pipelining": "two handles on two streams, alternating steps"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:

@@ -75,6 +75,8 @@ def load(build_if_missing: bool = True):
         "gemm_destroy": (c_int, [c_void_p]),
         "gemm_run": (c_int, [c_void_p, c_int64, c_int64, c_int64, c_void_p, c_void_p,
                              c_void_p, c_void_p, gemm_layout_t, c_void_p]),
+        "gemm_run_host": (c_int, [c_void_p, c_int64, c_int64, c_int64, c_void_p, c_void_p,
+                                  c_void_p, c_void_p, gemm_layout_t, c_void_p]),
         "gemm_status": (c_int, [c_void_p, c_void_p]),
         "gemm_status_detail": (c_int, [c_void_p]),
         "gemm_set_option": (c_int, [c_void_p, c_int, c_int64]),
@@ -124,6 +126,13 @@ def gemm_run(h, M, N, K, A_ptr, B_ptr, bias_ptr, C_ptr, lay: gemm_layout_t, stre
     return load().gemm_run(c_void_p(h), int(M), int(N), int(K), c_void_p(A_ptr),
                            c_void_p(B_ptr), c_void_p(bias_ptr), c_void_p(C_ptr), lay,
                            c_void_p(stream_ptr))
+
+
+def gemm_run_host(h, M, N, K, A_ptr, B_ptr, bias_ptr, C_ptr, lay: gemm_layout_t,
+                  stream_ptr) -> int:
+    return load().gemm_run_host(c_void_p(h), int(M), int(N), int(K), c_void_p(A_ptr),
+                                c_void_p(B_ptr), c_void_p(bias_ptr), c_void_p(C_ptr), lay,
+                                c_void_p(stream_ptr))
 
 
 def gemm_status(h, stream_ptr) -> int:

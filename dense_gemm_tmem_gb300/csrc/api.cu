@@ -474,6 +474,8 @@ struct gemm_ctx {
   uint64_t* trace = nullptr;  // caller's device buffer for phase stamps, or NULL
   int64_t trace_ctas = 0;     // CTA rows it holds (kTraceSlots stamps each)
   dg::Options opt;
+  void* host_stage = nullptr;   // gemm_run_host: device copies of A, B, bias and C
+  size_t host_stage_bytes = 0;  // grow-only
   std::mutex mu;  // guards the tensor-map cache
   dg::TmapEntry cache[dg::kTmapCacheSize];
   int cache_next = 0;
@@ -741,6 +743,7 @@ int gemm_destroy(gemm_handle_t h) {
     if (h->workspace) cudaFree(h->workspace);
     if (h->tickets) cudaFree(h->tickets);
     if (h->status) cudaFree(h->status);
+    if (h->host_stage) cudaFree(h->host_stage);
     return GEMM_OK;
   });
   delete h;
@@ -923,6 +926,52 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, co
                                plan.b_mn_major);
   return dg::on_device(h->device, [&]() -> int {
     return dg::launch_tc(L) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+  });
+}
+
+int gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A,
+                  const void* B, const float* bias, void* C, gemm_layout_t layout,
+                  void* stream_ptr) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || layout.in_dtype > 1 || layout.out_dtype > 1)
+    return GEMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (!C || (K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;
+  const size_t in_sz = layout.in_dtype == GEMM_F16 ? 2 : 4;
+  const size_t out_sz = layout.out_dtype == GEMM_F16 ? 2 : 4;
+  auto up = [](size_t b) { return (b + 255) & ~size_t(255); };  // 256-byte aligned parts
+  const size_t a_bytes = size_t(M) * size_t(K) * in_sz, b_bytes = size_t(K) * size_t(N) * in_sz;
+  const size_t bias_bytes = bias ? size_t(N) * 4 : 0, c_bytes = size_t(M) * size_t(N) * out_sz;
+  const size_t need = up(a_bytes) + up(b_bytes) + up(bias_bytes) + up(c_bytes);
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
+  return dg::on_device(h->device, [&]() -> int {
+    if (need > h->host_stage_bytes) {
+      // earlier calls on this stream may still read the old buffers
+      if (cudaStreamSynchronize(stream) != cudaSuccess) return GEMM_ERR_CUDA;
+      if (h->host_stage) cudaFree(h->host_stage);
+      h->host_stage = nullptr;
+      h->host_stage_bytes = 0;
+      if (cudaMalloc(&h->host_stage, need) != cudaSuccess) {
+        h->host_stage = nullptr;
+        return GEMM_ERR_ALLOC;
+      }
+      h->host_stage_bytes = need;
+    }
+    uint8_t* base = static_cast<uint8_t*>(h->host_stage);
+    void* dA = base;
+    void* dB = base + up(a_bytes);
+    float* dbias = bias ? reinterpret_cast<float*>(base + up(a_bytes) + up(b_bytes)) : nullptr;
+    void* dC = base + up(a_bytes) + up(b_bytes) + up(bias_bytes);
+    if ((a_bytes && cudaMemcpyAsync(dA, A, a_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) ||
+        (b_bytes && cudaMemcpyAsync(dB, B, b_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) ||
+        (bias_bytes &&
+         cudaMemcpyAsync(dbias, bias, bias_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess))
+      return GEMM_ERR_CUDA;
+    const int rc = gemm_run(h, M, N, K, dA, dB, dbias, dC, layout, stream_ptr);
+    if (rc != GEMM_OK) return rc;
+    if (cudaMemcpyAsync(C, dC, c_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    return GEMM_OK;
   });
 }
 

@@ -87,6 +87,30 @@ class Gemm:
         if rc != B.GEMM_OK:
             raise B.GemmError(rc, "gemm_run")
 
+    def run_host(self, A, Bm, C, bias=None, a_major=ROW, b_major=ROW, stream=None) -> None:
+        """Enqueues C = A·B (+bias) on host (CPU) tensors through gemm_run_host:
+        copies in, the GEMM and the copy out all on the stream.  Pinned tensors
+        (`.pin_memory()`) make the copies asynchronous; C is ready once the
+        stream has reached this point (e.g. after `status()`)."""
+        M, N, K = problem_dims(A, Bm, a_major, b_major)
+        for t in (A, Bm, C) + ((bias,) if bias is not None else ()):
+            if t.device.type != "cpu":
+                raise ValueError("run_host takes host tensors; got one on %s" % t.device)
+            if not t.is_contiguous():
+                raise ValueError("tensors must be contiguous")
+        in_code, out_code = _DT.get(A.dtype), _DT.get(C.dtype)
+        if A.dtype != Bm.dtype or in_code is None or out_code is None:
+            raise TypeError("A, B: both float16 or both float32; C: float16 or float32")
+        if C.dim() != 2 or C.shape[0] != M or C.shape[1] != N:
+            raise ValueError("C has shape %s, expected (%d, %d)" % (tuple(C.shape), M, N))
+        if bias is not None and (bias.dtype != torch.float32 or tuple(bias.shape) != (N,)):
+            raise ValueError("bias must be float32 of shape (N,)")
+        rc = B.gemm_run_host(self.handle, M, N, K, A.data_ptr(), Bm.data_ptr(),
+                             bias.data_ptr() if bias is not None else None, C.data_ptr(),
+                             _layout(a_major, b_major, in_code, out_code), self._stream(stream))
+        if rc != B.GEMM_OK:
+            raise B.GemmError(rc, "gemm_run_host")
+
     def __call__(self, A, Bm, bias=None, a_major=ROW, b_major=ROW, out_dtype=torch.float32,
                  stream=None) -> torch.Tensor:
         M, N, _ = problem_dims(A, Bm, a_major, b_major)

@@ -159,6 +159,23 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A,
              const void *B, const float *bias, void *C, gemm_layout_t layout,
              void *stream);
 
+/* gemm_run for operands and output in HOST memory.  A, B, bias (NULL or N
+ * fp32) and C are host pointers owned by the caller, laid out as for
+ * gemm_run.  Enqueued on `stream`, in this order: A, B and bias copied to
+ * device buffers the handle owns, gemm_run on them, C copied back.  The call
+ * returns once the work is enqueued; C holds the result when the stream has
+ * reached that point (gemm_status, or a stream synchronisation).  With
+ * page-locked host memory (cudaHostAlloc, or pinned torch tensors) the
+ * copies are asynchronous; pageable memory works, but each copy then
+ * completes before the call returns.  The device buffers grow to the largest
+ * problem seen on the handle (a call that grows them first synchronises
+ * `stream`, so nothing still reads the old ones) and are freed by
+ * gemm_destroy.  For one step's copies to overlap another's compute, use two
+ * handles on two streams.  Errors: gemm_run's, and ALLOC. */
+int gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A,
+                  const void *B, const float *bias, void *C, gemm_layout_t layout,
+                  void *stream);
+
 /* Synchronises `stream`, then reads and clears the device status word.
  * Returns GEMM_OK, GEMM_ERR_DEVICE_TIMEOUT (a bounded wait inside a kernel
  * expired; the kernel stopped early and C is unspecified; the handle's

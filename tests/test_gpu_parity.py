@@ -618,3 +618,34 @@ def test_workload_large_sampled_rows(g, dev, name, kind):
         assert np.array_equal(got, ref)
     else:
         check(got, ref, p, rows)
+
+
+# ------------------------------------------------------------- host buffers --
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("odt", [F16, F32])
+def test_run_host_matches_oracle(g, dev, pinned, odt):
+    """gemm_run_host: host operands copied in, the GEMM, the result copied out,
+    all on one stream; pinned and pageable host memory."""
+    p = problem(300, 520, 1000, 0, 1, F16, odt, True, 200 + pinned + 2 * (odt == F32))
+    hA = torch.from_numpy(p.A)
+    hB = torch.from_numpy(p.B)
+    hbias = torch.from_numpy(p.bias)
+    hC = torch.empty((p.M, p.N), dtype=TDT[odt])
+    if pinned:
+        hA, hB, hbias, hC = hA.pin_memory(), hB.pin_memory(), hbias.pin_memory(), hC.pin_memory()
+    g.run_host(hA, hB, hC, hbias, p.a_major, p.b_major)
+    g.status()
+    check(as_f64(hC), oracle.gemm(p.A, p.B, p.bias, a_major=p.a_major, b_major=p.b_major), p)
+
+
+def test_run_host_buffers_grow_and_fp32(g, dev):
+    """The handle's device buffers grow to the largest problem and stay valid
+    for smaller ones; the fp32 path runs through the same call."""
+    for (M, N, K, idt) in [(64, 96, 40, F16), (700, 300, 900, F32), (64, 96, 40, F32)]:
+        odt = F32
+        p = problem(M, N, K, 0, 0, idt, odt, True, 210 + M)
+        hC = torch.empty((M, N), dtype=torch.float32).pin_memory()
+        g.run_host(torch.from_numpy(p.A).pin_memory(), torch.from_numpy(p.B).pin_memory(), hC,
+                   torch.from_numpy(p.bias).pin_memory(), 0, 0)
+        g.status()
+        check(as_f64(hC), oracle.gemm(p.A, p.B, p.bias), p)
