@@ -6,6 +6,7 @@ import numpy as np
 import pytest
 import torch
 
+import golden_values
 import oracle
 from dense_gemm_tmem_gb300 import binding as B
 from dense_gemm_tmem_gb300 import inputs
@@ -350,6 +351,25 @@ def test_all_ones_gives_k(g, dev):
     p = inputs.Problem("ones", M, N, K, np.ones((M, K), np.float16), np.ones((K, N), np.float16),
                        None, 0, 0, F16, F32)
     assert np.array_equal(as_f64(run(g, p, dev)), np.full((M, N), float(K)))
+
+
+@pytest.mark.parametrize("M,N,idt,opts", [
+    (1, 1, F16, {}), (1, 1, F32, {}), (300, 264, F16, {"kernel": TC}),
+    (520, 776, F16, {"kernel": TC2}), (384, 512, F16, {"kernel": SK, "grid": 23}),
+    (16, 2048, F16, {"kernel": SPLITC, "csplit": 2}), (200, 300, F32, {}),
+    (300, 420, F16, {"kernel": SIMT, "grid": 23})])
+@pytest.mark.parametrize("odt", [F16, F32])
+def test_golden_block_sum(g, dev, M, N, idt, opts, odt):
+    """Every output is the pages' worked reduction 0 + 1 + ... + 255 = 32640
+    (tests/golden/block_sum_arange256.txt): each row of A is the ramp
+    0..K-1 and B (column-major) is all ones; exact in any summation order."""
+    gv = golden_values.load("block_sum_arange256.txt")
+    K = int(gv["K"])
+    set_opts(g, **opts)
+    npdt = np.float16 if idt == F16 else np.float32
+    A = np.tile(np.arange(K, dtype=npdt), (M, 1))
+    p = inputs.Problem("golden", M, N, K, A, np.ones((N, K), npdt), None, 0, 1, idt, odt)
+    assert np.array_equal(as_f64(run(g, p, dev)), np.full((M, N), gv["C"]))
 
 
 # ------------------------------------------------------------ edge cases --

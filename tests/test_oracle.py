@@ -6,6 +6,7 @@ from fractions import Fraction
 import numpy as np
 import pytest
 
+import golden_values
 import oracle
 from dense_gemm_tmem_gb300 import inputs
 
@@ -199,3 +200,24 @@ def test_bad_arguments():
                          rows=[3])
     with pytest.raises(TypeError):
         oracle.gemm(np.zeros((3, 5), np.float64), np.zeros((5, 2), np.float64))
+
+
+@pytest.mark.parametrize("dt", [np.float16, np.float32])
+@pytest.mark.parametrize("b_major", [0, 1])
+def test_golden_block_sum(dt, b_major):
+    """The pages' worked reduction (0 + 1 + ... + 255 = 32640, printed in
+    tests/golden/block_sum_arange256.txt) as a 1 x K by K x 1 product, in
+    both operand orders and both storage orders of B."""
+    gv = golden_values.load("block_sum_arange256.txt")
+    K, want = int(gv["K"]), gv["C"]
+    row = np.arange(K, dtype=dt).reshape(1, K)
+    ones = np.ones((K, 1), dtype=dt)
+    Bs = ones.T.copy() if b_major else ones  # column-major B is stored (N, K)
+    assert oracle.gemm(row, Bs, b_major=b_major)[0, 0] == want
+    # the same sum with the ramp in B and the ones in A
+    ramp = row.T.copy()
+    Bs = ramp.T.copy() if b_major else ramp
+    assert oracle.gemm(ones.T.copy(), Bs, b_major=b_major)[0, 0] == want
+    # a bias of -want cancels it exactly; a dropped bias would not
+    got = oracle.gemm(row, ones, bias=np.array([-want], dtype=np.float32))
+    assert got[0, 0] == 0.0
