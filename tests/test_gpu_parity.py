@@ -353,12 +353,16 @@ def test_all_ones_gives_k(g, dev):
     assert np.array_equal(as_f64(run(g, p, dev)), np.full((M, N), float(K)))
 
 
-@pytest.mark.parametrize("M,N,idt,opts", [
+_GOLDEN_CASES = [
     (1, 1, F16, {}), (1, 1, F32, {}), (300, 264, F16, {"kernel": TC}),
     (520, 776, F16, {"kernel": TC2}), (384, 512, F16, {"kernel": SK, "grid": 23}),
     (16, 2048, F16, {"kernel": SPLITC, "csplit": 2}), (200, 300, F32, {}),
-    (300, 420, F16, {"kernel": SIMT, "grid": 23})])
-@pytest.mark.parametrize("odt", [F16, F32])
+    (300, 420, F16, {"kernel": SIMT, "grid": 23})]
+
+
+# fp32 operands give fp32 output only
+@pytest.mark.parametrize("M,N,idt,opts,odt", [
+    c + (odt,) for c in _GOLDEN_CASES for odt in (F16, F32) if c[2] == F16 or odt == F32])
 def test_golden_block_sum(g, dev, M, N, idt, opts, odt):
     """Every output is the pages' worked reduction 0 + 1 + ... + 255 = 32640
     (tests/golden/block_sum_arange256.txt): each row of A is the ramp
