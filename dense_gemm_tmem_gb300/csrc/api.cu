@@ -476,6 +476,9 @@ struct gemm_ctx {
   dg::Options opt;
   void* host_stage = nullptr;   // gemm_run_host: device copies of A, B, bias and C
   size_t host_stage_bytes = 0;  // grow-only
+  std::mutex host_mu;           // serialises gemm_run_host's enqueueing
+  cudaEvent_t host_done = nullptr;  // recorded after each gemm_run_host call's work
+  bool host_done_recorded = false;
   std::mutex mu;  // guards the tensor-map cache
   dg::TmapEntry cache[dg::kTmapCacheSize];
   int cache_next = 0;
@@ -744,6 +747,7 @@ int gemm_destroy(gemm_handle_t h) {
     if (h->tickets) cudaFree(h->tickets);
     if (h->status) cudaFree(h->status);
     if (h->host_stage) cudaFree(h->host_stage);
+    if (h->host_done) cudaEventDestroy(h->host_done);
     return GEMM_OK;
   });
   delete h;
@@ -944,10 +948,16 @@ int gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* 
   const size_t bias_bytes = bias ? size_t(N) * 4 : 0, c_bytes = size_t(M) * size_t(N) * out_sz;
   const size_t need = up(a_bytes) + up(b_bytes) + up(bias_bytes) + up(c_bytes);
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
+  std::lock_guard<std::mutex> lock(h->host_mu);
   return dg::on_device(h->device, [&]() -> int {
+    if (!h->host_done && cudaEventCreateWithFlags(&h->host_done, cudaEventDisableTiming) != cudaSuccess) {
+      h->host_done = nullptr;
+      return GEMM_ERR_CUDA;
+    }
     if (need > h->host_stage_bytes) {
-      // earlier calls on this stream may still read the old buffers
-      if (cudaStreamSynchronize(stream) != cudaSuccess) return GEMM_ERR_CUDA;
+      // the previous call (on any stream) may still use the old buffers
+      if (h->host_done_recorded && cudaEventSynchronize(h->host_done) != cudaSuccess)
+        return GEMM_ERR_CUDA;
       if (h->host_stage) cudaFree(h->host_stage);
       h->host_stage = nullptr;
       h->host_stage_bytes = 0;
@@ -956,22 +966,32 @@ int gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* 
         return GEMM_ERR_ALLOC;
       }
       h->host_stage_bytes = need;
+    } else if (h->host_done_recorded && cudaStreamWaitEvent(stream, h->host_done, 0) != cudaSuccess) {
+      // same buffers: this call's copies start after the previous call's work
+      return GEMM_ERR_CUDA;
     }
     uint8_t* base = static_cast<uint8_t*>(h->host_stage);
     void* dA = base;
     void* dB = base + up(a_bytes);
     float* dbias = bias ? reinterpret_cast<float*>(base + up(a_bytes) + up(b_bytes)) : nullptr;
     void* dC = base + up(a_bytes) + up(b_bytes) + up(bias_bytes);
+    int rc = GEMM_OK;
     if ((a_bytes && cudaMemcpyAsync(dA, A, a_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) ||
         (b_bytes && cudaMemcpyAsync(dB, B, b_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) ||
         (bias_bytes &&
-         cudaMemcpyAsync(dbias, bias, bias_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess))
-      return GEMM_ERR_CUDA;
-    const int rc = gemm_run(h, M, N, K, dA, dB, dbias, dC, layout, stream_ptr);
-    if (rc != GEMM_OK) return rc;
-    if (cudaMemcpyAsync(C, dC, c_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
-      return GEMM_ERR_CUDA;
-    return GEMM_OK;
+         cudaMemcpyAsync(dbias, bias, bias_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)) {
+      rc = GEMM_ERR_CUDA;
+    } else {
+      rc = gemm_run(h, M, N, K, dA, dB, dbias, dC, layout, stream_ptr);
+      if (rc == GEMM_OK && cudaMemcpyAsync(C, dC, c_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        rc = GEMM_ERR_CUDA;
+    }
+    // whatever was enqueued, the next call waits for it
+    if (cudaEventRecord(h->host_done, stream) == cudaSuccess)
+      h->host_done_recorded = true;
+    else if (rc == GEMM_OK)
+      rc = GEMM_ERR_CUDA;
+    return rc;
   });
 }
 

@@ -91,7 +91,8 @@ class Gemm:
         """Enqueues C = A·B (+bias) on host (CPU) tensors through gemm_run_host:
         copies in, the GEMM and the copy out all on the stream.  Pinned tensors
         (`.pin_memory()`) make the copies asynchronous; C is ready once the
-        stream has reached this point (e.g. after `status()`)."""
+        stream has reached this point (e.g. after `status()`), and every
+        tensor passed must stay alive until then."""
         M, N, K = problem_dims(A, Bm, a_major, b_major)
         for t in (A, Bm, C) + ((bias,) if bias is not None else ()):
             if t.device.type != "cpu":

@@ -168,10 +168,14 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A,
  * page-locked host memory (cudaHostAlloc, or pinned torch tensors) the
  * copies are asynchronous; pageable memory works, but each copy then
  * completes before the call returns.  The device buffers grow to the largest
- * problem seen on the handle (a call that grows them first synchronises
- * `stream`, so nothing still reads the old ones) and are freed by
- * gemm_destroy.  For one step's copies to overlap another's compute, use two
- * handles on two streams.  Errors: gemm_run's, and ALLOC. */
+ * problem seen on the handle (a call that grows them first waits for the
+ * handle's previous gemm_run_host call to finish) and are freed by
+ * gemm_destroy.  Calls on one handle run in call order whatever their
+ * streams: each call's copies wait (on the device) for the previous call's
+ * work, so they never overwrite buffers still in use.  For one step's copies
+ * to overlap another's compute, use two handles on two streams.  Not for
+ * stream capture.  Errors: gemm_run's, ALLOC, and CUDA (a copy, event or
+ * stream call failed). */
 int gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A,
                   const void *B, const float *bias, void *C, gemm_layout_t layout,
                   void *stream);

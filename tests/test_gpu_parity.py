@@ -669,7 +669,25 @@ def test_run_host_buffers_grow_and_fp32(g, dev):
         odt = F32
         p = problem(M, N, K, 0, 0, idt, odt, True, 210 + M)
         hC = torch.empty((M, N), dtype=torch.float32).pin_memory()
-        g.run_host(torch.from_numpy(p.A).pin_memory(), torch.from_numpy(p.B).pin_memory(), hC,
-                   torch.from_numpy(p.bias).pin_memory(), 0, 0)
-        g.status()
+        hA, hB, hbias = (torch.from_numpy(x).pin_memory() for x in (p.A, p.B, p.bias))
+        g.run_host(hA, hB, hC, hbias, 0, 0)
+        g.status()  # the copies read hA, hB, hbias until here
         check(as_f64(hC), oracle.gemm(p.A, p.B, p.bias), p)
+
+
+def test_run_host_one_handle_two_streams(g, dev):
+    """Two calls on one handle from two streams share its device buffers:
+    the second call's copies wait for the first call's work, so both
+    results are right."""
+    ps = [problem(520, 392, 1032, 0, 1, F16, F32, True, 230 + i) for i in range(2)]
+    ss = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+    hCs = [torch.empty((p.M, p.N), dtype=torch.float32).pin_memory() for p in ps]
+    # every host buffer stays referenced until both streams are done: the
+    # copies run after the calls return
+    hins = [[torch.from_numpy(x).pin_memory() for x in (p.A, p.B, p.bias)] for p in ps]
+    for (hA, hB, hbias), s, hC in zip(hins, ss, hCs):
+        g.run_host(hA, hB, hC, hbias, 0, 1, stream=s)
+    for s in ss:
+        g.status(s)
+    for p, hC in zip(ps, hCs):
+        check(as_f64(hC), oracle.gemm(p.A, p.B, p.bias, b_major=1), p)
