@@ -298,3 +298,13 @@ def test_simt_staging_strides_follow_storage_align():
     a, b = B.gemm_simt_smem_strides()
     assert a == schedule.storage_align_strides([8, 128], [(32, 4), None])[0]
     assert b == schedule.storage_align_strides([8, 128], [(32, 4), None])[0]
+
+
+def test_run_entry_points_check_handle_and_sizes(lib):
+    """gemm_run and gemm_run_host reject a NULL handle before any CUDA call,
+    so this runs without a GPU; the status and destroy calls do the same."""
+    lay = B.layout(0, 0, B.GEMM_F16, B.GEMM_F32)
+    for fn in (B.gemm_run, B.gemm_run_host):
+        assert fn(None, 8, 8, 8, 1, 1, None, 1, lay, None) == B.GEMM_ERR_INVALID_ARG
+        assert fn(None, -1, 8, 8, 1, 1, None, 1, lay, None) == B.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_status(None, None) == B.GEMM_ERR_INVALID_ARG
