@@ -88,6 +88,7 @@ def load(build_if_missing: bool = True):
         "gemm_work_units": (c_int, [P(gemm_plan_t), c_int, P(c_int32), c_int]),
         "gemm_split_contributors": (c_int, [P(gemm_plan_t), c_int, P(c_int32), P(c_int32)]),
         "gemm_simt_smem_strides": (c_int, [P(c_int32), P(c_int32)]),
+        "gemm_drain_limit_ns": (c_int64, [c_int64]),
         "gemm_selftest_wait_timeout": (c_int, [c_void_p, c_int64, c_void_p]),
         "gemm_set_trace": (c_int, [c_void_p, c_void_p, c_int64]),
         "gemm_run_noalloc": (c_int, [c_int64, c_int64, c_int64, c_void_p, c_void_p, c_void_p,
@@ -184,6 +185,10 @@ def gemm_simt_smem_strides():
     if rc != GEMM_OK:
         raise GemmError(rc, "gemm_simt_smem_strides")
     return a.value, b.value
+
+
+def gemm_drain_limit_ns(wait_limit_ns: int) -> int:
+    return load().gemm_drain_limit_ns(int(wait_limit_ns))
 
 
 def gemm_selftest_wait_timeout(h, limit_ns: int, stream_ptr) -> int:

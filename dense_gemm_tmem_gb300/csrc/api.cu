@@ -690,6 +690,11 @@ int gemm_split_contributors(const gemm_plan_t* plan, int sk_tile, int32_t* first
   return GEMM_OK;
 }
 
+int64_t gemm_drain_limit_ns(int64_t wait_limit_ns) {
+  const uint64_t w = wait_limit_ns > 0 ? uint64_t(wait_limit_ns) : dg::Options().wait_limit_ns;
+  return int64_t(dg::drain_limit_ns(w));
+}
+
 int gemm_simt_smem_strides(int32_t* a_stride, int32_t* b_stride) {
   if (!a_stride || !b_stride) return GEMM_ERR_INVALID_ARG;
   *a_stride = dg::simt_a_stride();

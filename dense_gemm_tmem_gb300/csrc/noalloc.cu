@@ -151,17 +151,24 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
     rc = plan_for(M, N, K, layout, sc.num_sms, opt, &plan);
     if (rc != GEMM_OK) return rc;
   }
-  if (plan.workspace_bytes > int64_t(kNaPartialBytes) || plan.sk_tiles > kNaCounters)
+  // Only the Stream-K split counts arrivals per tile; the cluster split adds
+  // its partials on chip and the whole-tile plans need no counters.
+  if (plan.workspace_bytes > int64_t(kNaPartialBytes) ||
+      (plan.kernel == GEMM_KERNEL_STREAMK && plan.sk_tiles > kNaCounters))
     return GEMM_ERR_UNSUPPORTED;
 
   float* partials = reinterpret_cast<float*>(sc.base);
   int* counters = reinterpret_cast<int*>(sc.base + kNaCounterOff);
-  int* status = dev_status ? dev_status : reinterpret_cast<int*>(sc.base + kNaStatusOff);
+  int* own_status = reinterpret_cast<int*>(sc.base + kNaStatusOff);
+  int* status = dev_status ? dev_status : own_status;
 
-  // The counters must start at zero; the array keeps whatever the last call
-  // (possibly an aborted one) left there.
+  // The counters must start at zero, and so must the array's own status word
+  // when it stands in for the caller's: the array keeps whatever the last
+  // call (possibly an aborted one) left there.
   if (plan.kernel == GEMM_KERNEL_STREAMK &&
       cudaMemsetAsync(counters, 0, sizeof(int) * size_t(plan.sk_tiles), stream) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  if (!dev_status && cudaMemsetAsync(own_status, 0, sizeof(int), stream) != cudaSuccess)
     return GEMM_ERR_CUDA;
 
   const bool swap = plan.swap_ab != 0;

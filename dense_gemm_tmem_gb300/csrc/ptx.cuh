@@ -52,6 +52,15 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Counts `bytes` of transactions as done on the barrier without any copy
+// (used after an abort, for bytes a copy that was never issued would have
+// brought).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+
 // True once the phase with parity `parity` has completed.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -99,12 +108,24 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
   return true;
 }
 
-// Clean-up wait used after an abort: ignores the abort flag, still bounded.
+// Bound on a clean-up wait after an abort: the caller's wait limit, but never
+// less than one second.  The copies and MMAs a CTA has issued land within
+// microseconds, so a wait limit short enough to abort a launch on purpose
+// must not also cut the clean-up short: the CTA would free its TMEM and exit
+// while those operations still target its shared memory and TMEM.
+constexpr uint64_t kDrainFloorNs = 1000000000ull;
+__host__ __device__ constexpr uint64_t drain_limit_ns(uint64_t wait_limit_ns) {
+  return wait_limit_ns > kDrainFloorNs ? wait_limit_ns : kDrainFloorNs;
+}
+
+// Clean-up wait used after an abort: ignores the abort flag, bounded by
+// drain_limit_ns.
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity,
                                            const WaitCtl& wc) {
+  const uint64_t limit = drain_limit_ns(wc.limit_ns);
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > wc.limit_ns) {
+    if (globaltimer_ns() - t0 > limit) {
       atomicCAS(wc.status, 0, 1 + kSiteDrain);
       return false;
     }
@@ -155,6 +176,11 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
 // fp32 store into a cluster CTA's shared memory (distributed shared memory).
 __device__ __forceinline__ void st_dsmem_f32(uint32_t cluster_addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
+}
+
+// 32-bit store into a cluster CTA's shared memory.
+__device__ __forceinline__ void st_dsmem_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
 // 16-byte load from another CTA's shared memory (address 16-byte aligned).

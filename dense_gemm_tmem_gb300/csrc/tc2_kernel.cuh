@@ -103,18 +103,14 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
                : "memory");
 }
 
-// Busy-waits about `ns` nanoseconds (only on the abort path, to let this CTA's
-// copies that signal the leader's barrier land before the CTA exits).
-__device__ __forceinline__ void spin_ns(uint64_t ns) {
-  const uint64_t t0 = globaltimer_ns();
-  while (globaltimer_ns() - t0 < ns) {
-  }
-}
-
 // TMA producer (one thread in each CTA): this CTA's A rows and B half per
-// k-block; the leader's arrive.expect_tx covers both CTAs' bytes.
+// k-block; the leader's arrive.expect_tx covers both CTAs' bytes.  Both
+// producers walk the same sequence of (stage, phase) slots; the return value is
+// how many of them this one filled (issued loads for), which is all of them
+// unless a wait gave up.  Loads still in flight after an abort are waited for
+// by tc2_drain_loads once both producers have stopped.
 template <int S>
-__device__ __forceinline__ void tc2_producer(const CUtensorMap& tmA, const CUtensorMap& tmB,
+__device__ __forceinline__ uint32_t tc2_producer(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                              const TcArgs& args, uint8_t* sA, uint8_t* sB,
                                              uint64_t* full, uint64_t* empty, const WaitCtl& wc,
                                              uint32_t rank, int32_t cluster_id,
@@ -125,7 +121,7 @@ __device__ __forceinline__ void tc2_producer(const CUtensorMap& tmA, const CUten
   it.init_tc(W, cluster_id);
   Unit u;
   int s = 0;
-  uint32_t ph = 0, issued = 0, issued_par = 0;
+  uint32_t ph = 0, filled = 0;
   bool ok = true;
   bool waited = false;
   auto prerequisites_done = [&]() {  // thread 0 of the CTA
@@ -174,9 +170,7 @@ __device__ __forceinline__ void tc2_producer(const CUtensorMap& tmA, const CUten
         tma_load_2d_pair(b_dst, &tmB, fb, b_row, k0);
         tma_load_2d_pair(b_dst + 8192, &tmB, fb, b_row + 64, k0);
       }
-      if (!issued) trace_mark(args, blockIdx.x, kTraceFirstLoad);
-      issued |= 1u << s;
-      issued_par = (issued_par & ~(1u << s)) | (ph << s);
+      if (filled++ == 0) trace_mark(args, blockIdx.x, kTraceFirstLoad);
       if (++s == S) {
         s = 0;
         ph ^= 1;
@@ -184,13 +178,32 @@ __device__ __forceinline__ void tc2_producer(const CUtensorMap& tmA, const CUten
     }
   }
   if (!waited) prerequisites_done();  // no load at all
-  if (!ok) {
-    if (rank == 0) {
-      for (int t = 0; t < S; ++t)
-        if ((issued >> t) & 1) wait_drain(smem_u32(&full[t]), (issued_par >> t) & 1, wc);
-    } else if (issued) {
-      spin_ns(200000);  // the peer's copies complete on the leader's barrier
-    }
+  return filled;
+}
+
+// After both producers of the pair have stopped (leader's thread 0, between
+// the two closing cluster barriers): waits until every load either producer
+// issued has landed, so that neither CTA exits while a copy still writes its
+// shared memory.  n0 and n1 count the slots the leader and the peer filled;
+// a slot's `full` phase completes once the leader armed it and both halves
+// landed.  They differ only after an abort, by less than one ring (a producer
+// refills a stage only after the MMA consumed the previous load into it, which
+// needed both halves), so for each stage only its last slot can be one-sided:
+// filled by the peer alone, the leader arms it for the peer's half; filled by
+// the leader alone, the peer's half that will never come is counted as done.
+template <int S>
+__device__ __forceinline__ void tc2_drain_loads(uint64_t* full, uint32_t n0, uint32_t n1,
+                                                const WaitCtl& wc) {
+  const uint32_t n = n0 > n1 ? n0 : n1;
+#pragma unroll 1
+  for (uint32_t s = 0; s < uint32_t(S) && s < n; ++s) {
+    const uint32_t q = s + ((n - 1 - s) / S) * S;  // the stage's last filled slot
+    const uint32_t bar = smem_u32(&full[s]);
+    if (q >= n0)
+      mbar_arrive_expect_tx(bar, Tc2Config::kStageBytes);  // the peer's half only
+    else if (q >= n1)
+      mbar_complete_tx(bar, Tc2Config::kStageBytes);       // the peer's half never comes
+    wait_drain(bar, (q / S) & 1, wc);
   }
 }
 
@@ -451,6 +464,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  uint32_t* peer_filled = tmem_slot + 3;  // leader: load slots the peer's producer filled
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -490,11 +504,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   pdl_launch_dependents();
   const WaitCtl wc{args.wait_limit_ns, args.status, abort_flag};
 
+  uint32_t filled = 0;  // thread 0: load slots this CTA's producer filled
   if (warp == 0) {
-    if (lane == 0)
-      tc2_producer<S>(tmA, tmB, args, sA, sB, full, empty, wc, rank, cluster_id, t_entry);
-    else
+    if (lane == 0) {
+      filled = tc2_producer<S>(tmA, tmB, args, sA, sB, full, empty, wc, rank, cluster_id,
+                               t_entry);
+      if (rank != 0) st_dsmem_u32(map_to_rank(smem_u32(peer_filled), 0), filled);
+    } else {
       pdl_wait_prerequisites();
+    }
   } else if (warp == 1) {
     pdl_wait_prerequisites();
     if (lane == 0 && rank == 0)
@@ -507,7 +525,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
 
   __syncthreads();
   tc_fence_before();
-  cluster_sync_all();  // no MMA or remote arrive is still aimed at either CTA
+  // Both CTAs' roles are done: no MMA or remote arrive is still aimed at
+  // either CTA, no load will be issued, and the peer's fill count is in.
+  cluster_sync_all();
+  if (rank == 0 && threadIdx.x == 0) tc2_drain_loads<S>(full, filled, *peer_filled, wc);
+  cluster_sync_all();  // no copy still lands in either CTA's shared memory
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);

@@ -103,7 +103,9 @@ enum {
   GEMM_OPT_FORCE_KERNEL = 0,     /* GEMM_KERNEL_TC / _STREAMK / _SIMT / _TC2 / _SPLITC, or -1 */
   GEMM_OPT_FORCE_TILE_N = 1,     /* 16, 32, 64, 128, 256 (tensor-core path), or -1 */
   GEMM_OPT_FORCE_GRID = 2,       /* CTA count for the split path, or -1 */
-  GEMM_OPT_WAIT_LIMIT_NS = 3,    /* bound on each device-side wait (default 2e9 ns) */
+  GEMM_OPT_WAIT_LIMIT_NS = 3,    /* bound on each device-side wait (default 2e9 ns); the
+                                    clean-up waits after one gave up are bounded by
+                                    gemm_drain_limit_ns of it */
   GEMM_OPT_MIN_SPLIT_ITERS = 4,  /* fewest k-blocks per CTA when splitting (default: enough
                                     that a CTA reads 4x its fp32 partial tile in operands) */
   GEMM_OPT_FORCE_SWAP_AB = 5,    /* 0 or 1, or -1 for the picker's choice */
@@ -233,7 +235,10 @@ int gemm_selftest_wait_timeout(gemm_handle_t h, int64_t limit_ns, void *stream);
  * on the CURRENT device, owned by the caller; stream belongs to that device.
  * dev_status: NULL, or a device int the caller owns that the kernel sets to a
  * nonzero site code (as gemm_status_detail reports) if a bounded device-side
- * wait expires; with NULL such an expiry is recorded only in the array.
+ * wait expires; the caller clears it.  With NULL a timeout CANNOT be detected:
+ * the kernel stops early, C is incomplete, and nothing reports it (the expiry
+ * goes to a word inside the array, which each such call clears before its
+ * kernel and nothing reads).  Pass a status word wherever a wrong C matters.
  *
  * The first call on a device looks up the array's device address with that
  * device current (cudaGetSymbolAddress) and caches it; make that first call
@@ -246,9 +251,10 @@ int gemm_selftest_wait_timeout(gemm_handle_t h, int64_t limit_ns, void *stream);
  * ordering between them) race on the array and give wrong results: order them.
  *
  * Limits: fp16 inputs only (fp32 inputs return GEMM_ERR_UNSUPPORTED; use
- * gemm_run).  A split whose partial tiles exceed 16 MiB runs on fewer CTAs
- * so that they fit; a split over more than 4096 output tiles is refused with
- * GEMM_ERR_UNSUPPORTED (the counters would not fit).  Other errors as gemm_run:
+ * gemm_run).  A Stream-K split whose partial tiles exceed 16 MiB runs on fewer
+ * CTAs so that they fit; a Stream-K split over more than 4096 output tiles is
+ * refused with GEMM_ERR_UNSUPPORTED (the counters would not fit).  Cluster
+ * splits and whole-tile plans use neither.  Other errors as gemm_run:
  * INVALID_ARG, UNSUPPORTED (alignment, device not compute capability 10.3),
  * CUDA. */
 int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, const void *B,
@@ -281,6 +287,13 @@ int gemm_work_units(const gemm_plan_t *plan, int cta, int32_t *out, int max_unit
  * last contributing CTA, in ascending k order.  Returns 0 or INVALID_ARG. */
 int gemm_split_contributors(const gemm_plan_t *plan, int sk_tile, int32_t *first,
                             int32_t *last);
+
+/* The bound on the clean-up waits of a kernel whose device-side wait gave up
+ * (its TMA copies and MMAs still in flight must land before it frees its TMEM
+ * and exits), for a GEMM_OPT_WAIT_LIMIT_NS of wait_limit_ns (<= 0: the
+ * default): the limit itself, but never less than one second, so that a limit
+ * short enough to stop a launch early cannot also cut its clean-up short. */
+int64_t gemm_drain_limit_ns(int64_t wait_limit_ns);
 
 /* Shared-memory row strides (in floats) of the fp32 CUDA-core kernel's A and B
  * staging tiles, padded as storage_align(factor 32, offset 4) pads them. */

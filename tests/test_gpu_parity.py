@@ -598,6 +598,36 @@ def test_wait_timeout_selftest(g, dev):
     full_check(g, dev, p)
 
 
+@pytest.mark.parametrize("kernel,shape", [
+    (TC, (1024, 1024, 8192)),     # one-SM kernel, whole tiles
+    (SK, (512, 512, 8192)),       # one-SM kernel, Stream-K partials through the workspace
+    (SPLITC, (512, 512, 8192)),   # one-SM kernel, cluster split (partials on chip)
+    (TC2, (2048, 2048, 8192)),    # two-SM kernel (CTA pairs)
+])
+def test_real_kernel_wait_timeout(g, dev, kernel, shape):
+    """A wait limit of 1 us, far shorter than a launch, makes the kernels' own
+    bounded waits give up mid-launch: gemm_status reports
+    GEMM_ERR_DEVICE_TIMEOUT with the role whose wait expired first (TMA
+    producer, MMA issuer or epilogue; never the clean-up, whose waits keep at
+    least gemm_drain_limit_ns), and the next launch on the same handle, with
+    the default limit, matches the oracle."""
+    M, N, K = shape
+    p = problem(M, N, K, 0, 1, F16, F32, True, 150 + kernel)
+    set_opts(g, kernel=kernel)
+    assert g.plan(M, N, K, 0, 1, B.GEMM_F16, B.GEMM_F32)["kernel"] == kernel
+    A, Bt, bias = to_dev(p, dev)
+    s = torch.cuda.current_stream(dev).cuda_stream
+    g.set_option(B.GEMM_OPT_WAIT_LIMIT_NS, 1000)
+    g(A, Bt, bias, 0, 1, out_dtype=torch.float32)
+    assert B.gemm_status(g.handle, s) == B.GEMM_ERR_DEVICE_TIMEOUT
+    assert B.gemm_status_detail(g.handle) in (1, 2, 3, 4)
+    g.set_option(B.GEMM_OPT_WAIT_LIMIT_NS, -1)
+    C = g(A, Bt, bias, 0, 1, out_dtype=torch.float32)
+    g.status()
+    rows = sample_rows(M, 9)
+    check(as_f64(C, rows), oracle.gemm_rows(p.A, p.B, p.bias, b_major=1, rows=rows), p, rows)
+
+
 # ------------------------------------------------- the named workloads --
 def test_workload_512_full(g, dev):
     p = inputs.WORKLOADS["gemm512_f16_f32out"].make()
@@ -691,3 +721,27 @@ def test_run_host_one_handle_two_streams(g, dev):
         g.status(s)
     for p, hC in zip(ps, hCs):
         check(as_f64(hC), oracle.gemm(p.A, p.B, p.bias, b_major=1), p)
+
+
+def test_run_host_two_streams_regrow(g, dev):
+    """A call on a second stream that needs larger device buffers than the
+    handle holds: the host waits for the previous call's work before freeing
+    the old buffers, so the first call (still running on its own stream) and
+    the second both come out right."""
+    ps = [problem(256, 384, 2048, 0, 1, F16, F32, True, 240),
+          problem(1536, 1280, 2056, 0, 1, F16, F32, True, 241)]
+    h = Gemm(dev)  # a fresh handle: no buffers yet
+    try:
+        ss = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+        hCs = [torch.empty((p.M, p.N), dtype=torch.float32).pin_memory() for p in ps]
+        hins = [[torch.from_numpy(x).pin_memory() for x in (p.A, p.B, p.bias)] for p in ps]
+        for (hA, hB, hbias), s, hC in zip(hins, ss, hCs):
+            h.run_host(hA, hB, hC, hbias, 0, 1, stream=s)
+        for s in ss:
+            h.status(s)
+        for i, (p, hC) in enumerate(zip(ps, hCs)):
+            rows = None if i == 0 else sample_rows(p.M, 11)
+            got = as_f64(hC) if rows is None else hC.double().numpy()[rows]
+            check(got, oracle.gemm_rows(p.A, p.B, p.bias, b_major=1, rows=rows), p, rows)
+    finally:
+        h.close()

@@ -25,13 +25,13 @@ def declared_functions():
     for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
         if fn.endswith(".h"):
             txt = open(os.path.join(ROOT, "include", fn)).read()
-            names += re.findall(r"^(?:int|const char \*)\s*(gemm_\w+)\(", txt, re.M)
+            names += re.findall(r"^(?:int|int64_t|const char \*)\s*(gemm_\w+)\(", txt, re.M)
     return names
 
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) >= 12
+    assert len(names) >= 12 and "gemm_drain_limit_ns" in names
     for n in names:
         assert hasattr(lib, n), n
 
@@ -308,3 +308,15 @@ def test_run_entry_points_check_handle_and_sizes(lib):
         assert fn(None, 8, 8, 8, 1, 1, None, 1, lay, None) == B.GEMM_ERR_INVALID_ARG
         assert fn(None, -1, 8, 8, 1, 1, None, 1, lay, None) == B.GEMM_ERR_INVALID_ARG
     assert lib.gemm_status(None, None) == B.GEMM_ERR_INVALID_ARG
+
+
+def test_drain_limit_has_a_floor():
+    """The clean-up waits after an aborted wait (for the copies and MMAs a CTA
+    issued to land before it frees TMEM and exits) keep at least one second
+    whatever the wait limit, so a limit short enough to abort a launch cannot
+    cut the clean-up short; longer limits carry over, and <= 0 means the
+    default limit (2 s)."""
+    for limit in (1, 1000, 250_000, 999_999_999):
+        assert B.gemm_drain_limit_ns(limit) == 1_000_000_000
+    assert B.gemm_drain_limit_ns(5_000_000_000) == 5_000_000_000
+    assert B.gemm_drain_limit_ns(0) == B.gemm_drain_limit_ns(-1) == 2_000_000_000

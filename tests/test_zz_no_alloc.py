@@ -5,9 +5,10 @@ application whose allocator owns the GPU's memory, or a latency-critical path
 that must not synchronise on cudaMalloc/cudaFree).  gemm_run_noalloc serves
 them with scratch compiled into the library.  Each case calls it twice in a
 row (the second call finds the first call's partial tiles and counters still
-in the shared array) and compares both results with gemm_run's, within the
-tolerance the other GPU tests use; where both entry points run the same plan
-the results must be bit-identical.
+in the shared array) and checks both results against the CPU oracle at the
+gates every other GPU test uses, and against gemm_run's result within the same
+tolerance; where both entry points run the same plan the results must be
+bit-identical.
 
 This file is collected last on purpose, and builds everything it needs itself
 so it also passes alone in a fresh process."""
@@ -15,20 +16,23 @@ import numpy as np
 import pytest
 import torch
 
-import oracle  # noqa: F401  (same test infrastructure as the other GPU tests)
+import oracle
 from dense_gemm_tmem_gb300 import binding as B
 from dense_gemm_tmem_gb300 import inputs
 from dense_gemm_tmem_gb300.gemm import Gemm
 
-from gpu_helpers import TDT, check, to_dev
+from gpu_helpers import TDT, check, sample_rows, to_dev
 
 pytestmark = pytest.mark.gpu
 
 CASES = [
     # (M, N, K, a_major, b_major, out, bias)
-    (16, 4096, 4096, 0, 0, inputs.F32, False),    # skinny: swapped operands, 16-wide split
-    (512, 512, 512, 0, 0, inputs.F32, False),     # all tiles split, fits the scratch as is
-    (1280, 5120, 1024, 0, 1, inputs.F16, True),   # hybrid split that needs fewer CTAs to fit
+    (16, 4096, 192, 0, 0, inputs.F32, True),      # Stream-K split: partial tiles and tile
+                                                  # counters in the shared array
+    (16, 2048, 192, 0, 1, inputs.F16, True),      # the same, column-major B, fp16 output
+    (16, 4096, 4096, 0, 0, inputs.F32, False),    # skinny: swapped operands, cluster split
+    (512, 512, 512, 0, 0, inputs.F32, False),     # whole 128 x 64 tiles
+    (1280, 5120, 1024, 0, 1, inputs.F16, True),   # CTA pairs, whole 256 x 256 tiles
     (296, 520, 200, 1, 0, inputs.F16, True),      # ragged tiles, MN-major A
     (8, 8, 0, 0, 0, inputs.F32, True),            # K = 0: bias only
 ]
@@ -53,6 +57,8 @@ def test_noalloc_matches_gemm_run_twice(dev, case):
     g.status()
     ref_plan = g.plan(M, N, K, am, bm, B.GEMM_F16,
                       B.GEMM_F16 if odt == inputs.F16 else B.GEMM_F32)
+    if K == 192:  # these shapes run the split that keeps its partials in the array
+        assert ref_plan["kernel"] == B.GEMM_KERNEL_STREAMK and ref_plan["workspace_bytes"] > 0
     lay = B.layout(am, bm, B.GEMM_F16, B.GEMM_F16 if odt == inputs.F16 else B.GEMM_F32)
     stream = torch.cuda.current_stream(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -66,13 +72,20 @@ def test_noalloc_matches_gemm_run_twice(dev, case):
         outs.append(C)
     torch.cuda.synchronize(dev)
     assert int(status.item()) == 0
-    want = ref.double().cpu().numpy()
+    # the oracle on every row of the smaller cases, on one row per 128-row
+    # tile (plus the edges) of the larger ones
+    rows = None if M * N * K <= (1 << 31) else sample_rows(M, 17)
+    exact = oracle.gemm_rows(p.A, p.B, p.bias, a_major=am, b_major=bm, rows=rows)
+    pick = (lambda X: X) if rows is None else (lambda X: X[rows])
+    want = pick(ref.double().cpu().numpy())
+    check(want, exact, p, rows)  # gemm_run itself passes the gates here
     same_plan = ref_plan["workspace_bytes"] <= (16 << 20)
     for C in outs:
         got = C.double().cpu().numpy()
         assert not np.isnan(got).any()
-        # within the tolerance of the other GPU tests, taking gemm_run as reference
-        check(got, want, p)
+        check(pick(got), exact, p, rows)
+        # and within the same tolerance of gemm_run's result
+        check(pick(got), want, p, rows)
         if same_plan:
             assert torch.equal(C, ref)
     g.close()
