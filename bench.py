@@ -211,6 +211,57 @@ def cpu_baseline(p, seconds, threads):
                       "fp64 accumulation, %.1f s" % (reps, len(rows), p.M, p.N, p.K, p.N, total_t)}
 
 
+def host_link(dev, hA, hB, hbias, hC, dev_set, step_flops, per_launch_s, reps=3):
+    """The host link the end-to-end steps travel over, measured with the same
+    pinned buffers: one step's inputs host -> device, its output device ->
+    host, and both directions at once on two streams (CUDA events, best of
+    `reps`).  The bound is the step rate the link (or the kernel, if slower)
+    allows when one step's copies overlap the previous step's compute, as
+    the pipelined end-to-end steps do."""
+    import torch
+    A, Bd, bias, C = dev_set
+    ins = [(A, hA), (Bd, hB)] + ([(bias, hbias)] if hbias is not None else [])
+    bytes_in = sum(h.numel() * h.element_size() for _, h in ins)
+    bytes_out = hC.numel() * hC.element_size()
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(streams_work):
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            cur = torch.cuda.current_stream(dev)
+            e0.record(cur)
+            for st, work in streams_work:
+                st.wait_stream(cur)
+                with torch.cuda.stream(st):
+                    work()
+            for st, _ in streams_work:
+                cur.wait_stream(st)
+            e1.record(cur)
+            torch.cuda.synchronize(dev)
+            best = min(best, e0.elapsed_time(e1) * 1e-3)
+        return best
+
+    def copy_in():
+        for d, h in ins:
+            d.copy_(h, non_blocking=True)
+
+    def copy_out():
+        hC.copy_(C, non_blocking=True)
+
+    t_in = timed([(s_in, copy_in)])
+    t_out = timed([(s_out, copy_out)])
+    t_both = timed([(s_in, copy_in), (s_out, copy_out)])
+    step_s = max(t_both, per_launch_s)
+    return {"h2d_gbs": bytes_in / t_in / 1e9, "d2h_gbs": bytes_out / t_out / 1e9,
+            "both_gbs": (bytes_in + bytes_out) / t_both / 1e9,
+            "bound_tflops": step_flops / step_s / 1e12,
+            "bound_basis": "one step's copies in both directions at once, overlapping the "
+                           "previous step's kernel (or the kernel, if slower)"}
+
+
 # ------------------------------------------------------------ reference arm --
 def run_reference(args):
     import numpy as np
@@ -434,7 +485,10 @@ def run_ours(args):
                "unit": "TFLOP/s", "h2d_bytes_per_step": bytes_a + bytes_b + bytes_bias,
                "d2h_bytes_per_step": bytes_c, "steps": e_steps,
                "api": "gemm_run_host (pinned host buffers)",
-               "pipelining": "two handles on two streams, alternating steps"}
+               "pipelining": "two handles on two streams, alternating steps",
+               "link": host_link(dev, hA, hB, hbias, hCs[0], sets[0], step_flops,
+                                 per_launch_s=avg_launch_s)}
+        e2e["link"]["frac"] = e2e["value"] / e2e["link"]["bound_tflops"]
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:

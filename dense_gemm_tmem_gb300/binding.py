@@ -27,7 +27,7 @@ GEMM_ROW_MAJOR, GEMM_COL_MAJOR = 0, 1
 (GEMM_OPT_FORCE_KERNEL, GEMM_OPT_FORCE_TILE_N, GEMM_OPT_FORCE_GRID, GEMM_OPT_WAIT_LIMIT_NS,
  GEMM_OPT_MIN_SPLIT_ITERS, GEMM_OPT_FORCE_SWAP_AB, GEMM_OPT_GROUP_M, GEMM_OPT_PAIR,
  GEMM_OPT_CLUSTER_SPLIT, GEMM_OPT_PDL, GEMM_OPT_PAIR_SPLIT, GEMM_OPT_TMA_STORE,
- GEMM_OPT_BIAS_INIT) = range(13)
+ GEMM_OPT_BIAS_INIT, GEMM_OPT_DYNAMIC_TILES) = range(14)
 
 
 class gemm_layout_t(ctypes.Structure):
@@ -89,6 +89,7 @@ def load(build_if_missing: bool = True):
         "gemm_split_contributors": (c_int, [P(gemm_plan_t), c_int, P(c_int32), P(c_int32)]),
         "gemm_simt_smem_strides": (c_int, [P(c_int32), P(c_int32)]),
         "gemm_drain_limit_ns": (c_int64, [c_int64]),
+        "gemm_inject_alloc_failure": (c_int, [c_int64]),
         "gemm_selftest_wait_timeout": (c_int, [c_void_p, c_int64, c_void_p]),
         "gemm_set_trace": (c_int, [c_void_p, c_void_p, c_int64]),
         "gemm_run_noalloc": (c_int, [c_int64, c_int64, c_int64, c_void_p, c_void_p, c_void_p,
@@ -185,6 +186,10 @@ def gemm_simt_smem_strides():
     if rc != GEMM_OK:
         raise GemmError(rc, "gemm_simt_smem_strides")
     return a.value, b.value
+
+
+def gemm_inject_alloc_failure(n: int) -> int:
+    return load().gemm_inject_alloc_failure(int(n))
 
 
 def gemm_drain_limit_ns(wait_limit_ns: int) -> int:

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -19,6 +20,8 @@ namespace dg {
 constexpr int kMaxTileN = 256;
 constexpr int kNarrowIters = 12;  // deepest K (in k-blocks) for which narrow whole tiles win
 constexpr int kTicketCap = 16384;     // split tiles one launch may have
+// after the tickets: the two-SM kernel's tile counter and finished-pair count
+constexpr int kCounterInts = kTicketCap + 2;
 constexpr int kTmapCacheSize = 32;
 constexpr int64_t kMaxCoord = (int64_t(1) << 31) - 1024;  // TMA coordinates are int32
 
@@ -50,6 +53,21 @@ bool log_enabled() {
 }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Allocation-failure injection (gemm_inject_alloc_failure): when armed with n,
+// the n-th device allocation from now fails as if the device were full.
+std::atomic<int64_t> g_fail_alloc_in{0};
+
+cudaError_t dev_malloc(void** p, size_t bytes) {
+  int64_t n = g_fail_alloc_in.load();
+  while (n > 0 && !g_fail_alloc_in.compare_exchange_weak(n, n - 1)) {
+  }
+  if (n == 1) {
+    *p = nullptr;
+    return cudaErrorMemoryAllocation;
+  }
+  return cudaMalloc(p, bytes);
+}
 
 }  // namespace
 
@@ -727,11 +745,15 @@ int gemm_create(gemm_handle_t* out, int device) {
     const int simt = dg::simt_ctas_per_sm();
     h->opt.simt_per_sm = simt > 0 ? simt : 2;
     h->workspace_bytes = size_t(2) * h->num_sms * dg::kBM * dg::kMaxTileN * sizeof(float);
-    if (cudaMalloc(&h->workspace, h->workspace_bytes) != cudaSuccess) return GEMM_ERR_ALLOC;
-    if (cudaMalloc(&h->tickets, sizeof(int) * dg::kTicketCap) != cudaSuccess)
+    if (dg::dev_malloc(reinterpret_cast<void**>(&h->workspace), h->workspace_bytes) !=
+        cudaSuccess)
       return GEMM_ERR_ALLOC;
-    if (cudaMalloc(&h->status, sizeof(int)) != cudaSuccess) return GEMM_ERR_ALLOC;
-    if (cudaMemset(h->tickets, 0, sizeof(int) * dg::kTicketCap) != cudaSuccess ||
+    if (dg::dev_malloc(reinterpret_cast<void**>(&h->tickets), sizeof(int) * dg::kCounterInts) !=
+        cudaSuccess)
+      return GEMM_ERR_ALLOC;
+    if (dg::dev_malloc(reinterpret_cast<void**>(&h->status), sizeof(int)) != cudaSuccess)
+      return GEMM_ERR_ALLOC;
+    if (cudaMemset(h->tickets, 0, sizeof(int) * dg::kCounterInts) != cudaSuccess ||
         cudaMemset(h->status, 0, sizeof(int)) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess)
       return GEMM_ERR_CUDA;
@@ -815,6 +837,10 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value) {
     case GEMM_OPT_BIAS_INIT:
       if (value > 1) return GEMM_ERR_INVALID_ARG;
       o.bias_init = value < 0 ? d.bias_init : int(value);
+      return GEMM_OK;
+    case GEMM_OPT_DYNAMIC_TILES:
+      if (value > 1) return GEMM_ERR_INVALID_ARG;
+      o.dyn_sched = value < 0 ? d.dyn_sched : int(value);
       return GEMM_OK;
     default:
       return GEMM_ERR_INVALID_ARG;
@@ -928,7 +954,16 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, co
              dg::encode_output(h, &L.tmC, C, M, N, layout.out_dtype == GEMM_F16))
                 ? 1
                 : 0;
+  // whole, aligned 4-column groups for the plain stores of row-major output
+  const int64_t c_pitch = N * (layout.out_dtype == GEMM_F16 ? 2 : 4);
+  a.c_vec = (!swap && (reinterpret_cast<uintptr_t>(C) & 15) == 0 && c_pitch % 16 == 0) ? 1 : 0;
   a.bias_init = (h->opt.bias_init && bias) ? 1 : 0;
+  // Whole pair tiles are handed out at run time in tile order (a counter the
+  // pairs draw from), so the tiles in flight stay one compact block of the
+  // raster however the pairs drift apart; the split tail and the bias seeding
+  // keep the static schedule.
+  if (pair && plan.sk_tiles == 0 && !a.bias_init && h->opt.dyn_sched != 0)
+    a.sched = h->tickets + dg::kTicketCap;
   // phase stamps only if the caller's buffer holds one row per CTA
   a.trace = (h->trace && h->trace_ctas >= plan.grid) ? h->trace : nullptr;
   a.idesc = dg::make_idesc_f16(pair ? dg::kPairBM : dg::kBM, plan.tile_n, plan.a_mn_major,
@@ -966,7 +1001,7 @@ int gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* 
       if (h->host_stage) cudaFree(h->host_stage);
       h->host_stage = nullptr;
       h->host_stage_bytes = 0;
-      if (cudaMalloc(&h->host_stage, need) != cudaSuccess) {
+      if (dg::dev_malloc(&h->host_stage, need) != cudaSuccess) {
         h->host_stage = nullptr;
         return GEMM_ERR_ALLOC;
       }
@@ -1013,7 +1048,7 @@ int gemm_status(gemm_handle_t h, void* stream_ptr) {
     // a kernel stopped early: clear the word and the split counters it may
     // have left behind, so the handle is usable again
     if (cudaMemset(h->status, 0, sizeof(int)) != cudaSuccess ||
-        cudaMemset(h->tickets, 0, sizeof(int) * dg::kTicketCap) != cudaSuccess ||
+        cudaMemset(h->tickets, 0, sizeof(int) * dg::kCounterInts) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess)
       return GEMM_ERR_CUDA;
     return GEMM_ERR_DEVICE_TIMEOUT;
@@ -1021,6 +1056,12 @@ int gemm_status(gemm_handle_t h, void* stream_ptr) {
 }
 
 int gemm_status_detail(gemm_handle_t h) { return h ? h->last_detail : 0; }
+
+int gemm_inject_alloc_failure(int64_t n) {
+  if (n < 0) return GEMM_ERR_INVALID_ARG;
+  dg::g_fail_alloc_in.store(n);
+  return GEMM_OK;
+}
 
 int gemm_set_trace(gemm_handle_t h, uint64_t* dev_buf, int64_t ctas) {
   if (!h || ctas < 0 || (ctas > 0 && !dev_buf)) return GEMM_ERR_INVALID_ARG;

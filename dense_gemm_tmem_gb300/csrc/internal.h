@@ -28,6 +28,7 @@ struct Options {
   int tma_store = -1;      // epilogue output by TMA store where C allows it: -1 for fp16
                            // output or more output tiles than CTAs, 1 always, 0 never
   int bias_init = 0;       // seed the accumulators with the bias
+  int dyn_sched = 1;       // two-SM kernel, whole tiles: tiles handed out at run time
   int csplit_clusters[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};  // clusters of s resident (0: SMs/s)
   int simt_per_sm = 0;     // 128 x 128 CUDA-core CTAs resident per SM (0: 2); set per device
   uint64_t wait_limit_ns = 2000000000ull;
@@ -98,7 +99,8 @@ struct SimtLaunch {
 };
 cudaError_t launch_simt(const SimtLaunch& L);
 cudaError_t launch_simt_f16(const SimtLaunch& L);
-constexpr int kSimtBM = 128, kSimtBN = 128, kSimtBK = 16, kSimtThreads = 256;
+constexpr int kSimtBM = 128, kSimtBN = 128, kSimtBK = 16;
+constexpr int kSimtThreads = 128;  // 128 x 128 tile: 16 x 8 outputs per thread
 constexpr int kSimtSmallTile = 64;  // 64 x 64 tiles, 64 threads
 constexpr int kSimtMinSplitIters = 8;  // fewest k-blocks a split CTA gets
 // CTAs of the 128 x 128 kernel resident on one SM (-1 if the query fails).

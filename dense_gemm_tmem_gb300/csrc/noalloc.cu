@@ -204,6 +204,8 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
   a.trace = nullptr;
   std::memset(&L.tmC, 0, sizeof(L.tmC));
   a.c_tma = 0;  // plain stores: no output tensor map to encode and keep
+  const int64_t c_pitch = N * (layout.out_dtype == GEMM_F16 ? 2 : 4);
+  a.c_vec = (!swap && (reinterpret_cast<uintptr_t>(C) & 15) == 0 && c_pitch % 16 == 0) ? 1 : 0;
   a.bias_init = 0;
   return launch_tc(L) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }

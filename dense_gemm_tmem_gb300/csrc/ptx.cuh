@@ -74,6 +74,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same, with acquire semantics at cluster scope: the phase was completed
+// by arrivals (release, cluster scope) of threads in another CTA of the
+// cluster, whose earlier stores this thread then sees.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Where a bounded wait gave up (the device status word holds 1 + this).
 enum WaitSite : int {
   kSiteProducer = 0,   // TMA producer waiting for a free stage
@@ -116,6 +131,22 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
 constexpr uint64_t kDrainFloorNs = 1000000000ull;
 __host__ __device__ constexpr uint64_t drain_limit_ns(uint64_t wait_limit_ns) {
   return wait_limit_ns > kDrainFloorNs ? wait_limit_ns : kDrainFloorNs;
+}
+
+// wait_bounded at cluster scope (mbar_try_wait_cluster).
+__device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity,
+                                                     const WaitCtl& wc, int site) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait_cluster(bar, parity)) {
+    if (*wc.abort) return false;
+    if (globaltimer_ns() - t0 > wc.limit_ns) {
+      *wc.abort = 1;
+      atomicCAS(wc.status, 0, 1 + site);
+      return false;
+    }
+  }
+  return true;
 }
 
 // Clean-up wait used after an abort: ignores the abort flag, bounded by

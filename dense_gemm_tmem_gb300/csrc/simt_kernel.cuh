@@ -159,18 +159,27 @@ __device__ __forceinline__ void store4(__half* dst, const float (&o)[4], bool ve
   }
 }
 
-// BM x BN tile, NT = (BM/8) x (BN/8) threads, each an 8x8 register tile made
-// of two 4-row groups BM/2 apart and two 4-column groups BN/2 apart.  A 1-D
-// grid of a.work.grid CTAs walks the units that WorkIter hands it.  Residency
-// asked of the compiler: 2 CTAs per SM for 128-tiles; 4 for 64-tiles, which the
-// picker uses only for products too small to give 128-tiles 8 CTAs.  ASYNC
-// (fp32 only): the operands stored m/n-contiguous have 16-byte aligned rows
-// and are copied global -> shared directly, holding no staging registers.
+// Rows of the register tile each thread of a BM-row tile owns: 16 for the
+// 128-row tiles (128 threads), 8 for the 64-row tiles (64 threads).
+template <int BM>
+constexpr int kSimtTM = BM == 128 ? 16 : 8;
+
+// BM x BN tile, NT = (BM/TM) x (BN/8) threads, each a TM x 8 register tile
+// made of TM/4 groups of 4 rows, BM/(TM/4) apart, and two 4-column groups
+// BN/2 apart.  A 1-D grid of a.work.grid CTAs walks the units that WorkIter
+// hands it.  Residency asked of the compiler: 2 CTAs per SM for 128-tiles; 4
+// for 64-tiles, which the picker uses only for products too small to give
+// 128-tiles 8 CTAs.  ASYNC (fp32 only): the operands stored m/n-contiguous
+// have 16-byte aligned rows and are copied global -> shared directly, holding
+// no staging registers.
 template <typename TIn, typename TOut, int BM, int BN, bool A_COL, bool B_COL, bool ASYNC>
-__global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
+__global__ void __launch_bounds__((BM / kSimtTM<BM>) * (BN / 8), BM == 128 ? 2 : 4)
     simt_sgemm_kernel(const SimtArgs a) {
   constexpr int BK = kSimtBK;
-  constexpr int NT = (BM / 8) * (BN / 8);
+  constexpr int TM = kSimtTM<BM>;   // rows per thread
+  constexpr int RG = TM / 4;        // groups of 4 rows per thread
+  constexpr int RS = BM / RG;       // row distance between a thread's groups
+  constexpr int NT = (BM / TM) * (BN / 8);
   constexpr int AS = aligned_stride(BM, 32, 4);
   constexpr int BS = aligned_stride(BN, 32, 4);
   constexpr int AV = BM * BK / 4 / NT;  // float4 pieces of A per thread per k-block
@@ -191,10 +200,10 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
   const TIn* const Bp = static_cast<const TIn*>(a.B);
 
   float ra[AV][4], rb[BV][4];
-  float acc[8][8];
+  float acc[TM][8];
   // The main loop accumulates row pairs, P[i][j] = {acc[2i][j], acc[2i+1][j]},
   // with packed two-wide FMAs: a pair of A rows times one B column, {b, b}.
-  uint64_t P[4][8];
+  uint64_t P[TM / 2][8];
 
   // Piece v of this thread for an operand stored k-contiguous (row-major A,
   // column-major B): pairs of threads cover 8 consecutive k of one row (a
@@ -280,11 +289,11 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
     if constexpr (kAsyncA || kAsyncB) cp_async_wait_all();
   };
 
-  // Epilogue: + bias[n]; rows ty*4+i (+BM/2), columns tx*4+j (+BN/2).
+  // Epilogue: + bias[n]; rows (i/4)*RS + ty*4 + i%4, columns tx*4+j (+BN/2).
   auto store_tile = [&](int64_t m0, int64_t n0) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int64_t m = m0 + (i < 4 ? ty * 4 + i : BM / 2 + ty * 4 + (i - 4));
+    for (int i = 0; i < TM; ++i) {
+      const int64_t m = m0 + (i / 4) * RS + ty * 4 + (i % 4);
       if (m >= M) continue;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -314,7 +323,7 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
     tile_coords(W, u.tile, tm, tn);
     const int64_t m0 = int64_t(tm) * BM, n0 = int64_t(tn) * BN;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < TM / 2; ++i)
 #pragma unroll
       for (int j = 0; j < 8; ++j) P[i][j] = 0;  // two +0.0f
 
@@ -329,18 +338,22 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
       if (kt + 1 < u.kb1) fetch(m0, n0, int64_t(kt + 1) * BK, buf ^ 1);
 #pragma unroll
       for (int kk = 0; kk < BK; ++kk) {
-        // rows (ty*4 + {0,1}), (ty*4 + {2,3}), and the same BM/2 further on
-        const ulonglong2 a0 = *reinterpret_cast<const ulonglong2*>(&As[buf][kk][ty * 4]);
-        const ulonglong2 a1 =
-            *reinterpret_cast<const ulonglong2*>(&As[buf][kk][BM / 2 + ty * 4]);
+        // row pairs (ty*4 + {0,1}) and (ty*4 + {2,3}) of each row group
+        uint64_t av[TM / 2];
+#pragma unroll
+        for (int g = 0; g < RG; ++g) {
+          const ulonglong2 ag =
+              *reinterpret_cast<const ulonglong2*>(&As[buf][kk][g * RS + ty * 4]);
+          av[2 * g] = ag.x;
+          av[2 * g + 1] = ag.y;
+        }
         // columns tx*4 + {0..3} and BN/2 + tx*4 + {0..3}, each as {b, b}
         const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
         const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][BN / 2 + tx * 4]);
-        const uint64_t av[4] = {a0.x, a0.y, a1.x, a1.y};
         const uint64_t bv[8] = {dup2(b0.x), dup2(b0.y), dup2(b0.z), dup2(b0.w),
                                 dup2(b1.x), dup2(b1.y), dup2(b1.z), dup2(b1.w)};
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < TM / 2; ++i)
 #pragma unroll
           for (int j = 0; j < 8; ++j) fma2(P[i][j], av[i], bv[j]);
       }
@@ -348,7 +361,7 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
       __syncthreads();
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < TM / 2; ++i)
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         acc[2 * i][j] = __uint_as_float(uint32_t(P[i][j]));
@@ -362,13 +375,14 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
     // Split unit.  Publish the fp32 partial: float4 j of thread t (row j/2 of
     // its register tile, column half j%2) at float4 index j*NT + t of the slot,
     // so each warp's stores are contiguous.
+    constexpr int kQuads = TM * 2;  // float4 per thread
     const int32_t st = u.tile - W.dp_tiles;
     const int32_t me = int32_t(blockIdx.x);
     const size_t slot_elems = size_t(BM) * BN;
     float4* mine = reinterpret_cast<float4*>(a.workspace +
                                              size_t(split_slot(W, me, st)) * slot_elems);
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
+    for (int j = 0; j < kQuads; ++j)
       __stcg(mine + j * NT + t, make_float4(acc[j >> 1][(j & 1) * 4], acc[j >> 1][(j & 1) * 4 + 1],
                                             acc[j >> 1][(j & 1) * 4 + 2],
                                             acc[j >> 1][(j & 1) * 4 + 3]));
@@ -391,7 +405,7 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
     const int32_t first_slot = split_slot(W, first, st);
     // four float4 (one register-tile row pair) of every contributor at a time
 #pragma unroll
-    for (int jc = 0; jc < 4; ++jc) {
+    for (int jc = 0; jc < kQuads / 4; ++jc) {
       for (int32_t r = first; r <= last; ++r) {
         const float4* src = reinterpret_cast<const float4*>(
             a.workspace + size_t(r == first ? first_slot : 2 * r) * slot_elems);
@@ -415,7 +429,7 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 4)
 
 template <typename TIn, typename TOut, int BM, int BN, bool A_COL, bool B_COL>
 cudaError_t launch_simt_layout(const SimtArgs& a, cudaStream_t s) {
-  constexpr int NT = (BM / 8) * (BN / 8);
+  constexpr int NT = (BM / kSimtTM<BM>) * (BN / 8);
   const dim3 grid{unsigned(a.work.grid), 1u, 1u};
   // direct copies for the 128-tile fp32 kernel when its m/n-contiguous
   // operands have aligned rows (the 64-tile kernel has registers to spare)

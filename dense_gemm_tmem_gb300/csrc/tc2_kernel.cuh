@@ -36,13 +36,15 @@ struct Tc2Config {
   static constexpr int kBBytes = kHalfBN * kBK * 2;  // 16 KiB: this CTA's 128 columns
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 512;  // two 256-column accumulators
+  static constexpr int kSchedDepth = 4;  // tile ring of the dynamic schedule
   static constexpr int kBarBytes = 256;
   // epilogue staging (after the stages, so 1024-byte aligned), 4 warps: padded
   // rows of 36 floats, or a 4 KiB swizzled TMA store box each
   static constexpr int kEpiStageBytes = 4 * 32 * (32 + 4) * 4;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes + kEpiStageBytes;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-  static_assert((2 * kStages + 5) * 8 + 16 <= kBarBytes, "barrier area");
+  static_assert((2 * kStages + 5 + 2 * kSchedDepth) * 8 + 16 + 4 * kSchedDepth <= kBarBytes,
+                "barrier area");
 };
 
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
@@ -103,6 +105,50 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
                : "memory");
 }
 
+// Consumers of one slot of the tile ring: the leader's MMA issuer and four
+// epilogue warps, the peer's producer and four epilogue warps.
+constexpr int kSchedConsumers = 10;
+
+// The tile ring of the dynamic schedule.  The leader's producer takes tiles
+// from a global counter (the first one is the pair's index) and writes each
+// into slot d of both CTAs' rings, -1 once the tiles are all taken; every
+// other role reads its CTA's copy and reports the slot read on the leader's
+// `empty`.  Waits and arrivals are at cluster scope: the two CTAs hand the
+// slots to each other.
+struct TileRing {
+  uint64_t* full;   // this CTA's: one arrival per published tile
+  uint64_t* empty;  // the leader's: kSchedConsumers arrivals per slot read
+  volatile int32_t* slot;
+  uint32_t d = 0, ph = 0;
+
+  __device__ __forceinline__ void advance() {
+    if (++d == uint32_t(Tc2Config::kSchedDepth)) {
+      d = 0;
+      ph ^= 1;
+    }
+  }
+  // Consumer: waits for slot d (bounded), then reads it; false if the wait
+  // gave up.  Call done() once every thread that needs the value has it.
+  __device__ __forceinline__ bool wait(const WaitCtl& wc, int site) {
+    return wait_bounded_cluster(smem_u32(&full[d]), ph, wc, site);
+  }
+  __device__ __forceinline__ int32_t read() const { return slot[d]; }
+  __device__ __forceinline__ void done() {
+    mbar_arrive_cluster(map_to_rank(smem_u32(&empty[d]), 0));
+    advance();
+  }
+  // Leader's producer: publishes `tile` in slot d of both CTAs' rings.
+  __device__ __forceinline__ bool publish(int32_t tile, const WaitCtl& wc) {
+    if (!wait_bounded_cluster(smem_u32(&empty[d]), ph ^ 1, wc, kSiteProducer)) return false;
+    const uint32_t sl = smem_u32(const_cast<int32_t*>(&slot[d]));
+    const uint32_t fl = smem_u32(&full[d]);
+    for (uint32_t r = 0; r < 2; ++r) st_dsmem_u32(map_to_rank(sl, r), uint32_t(tile));
+    for (uint32_t r = 0; r < 2; ++r) mbar_arrive_cluster(map_to_rank(fl, r));
+    advance();
+    return true;
+  }
+};
+
 // TMA producer (one thread in each CTA): this CTA's A rows and B half per
 // k-block; the leader's arrive.expect_tx covers both CTAs' bytes.  Both
 // producers walk the same sequence of (stage, phase) slots; the return value is
@@ -114,12 +160,14 @@ __device__ __forceinline__ uint32_t tc2_producer(const CUtensorMap& tmA, const C
                                              const TcArgs& args, uint8_t* sA, uint8_t* sB,
                                              uint64_t* full, uint64_t* empty, const WaitCtl& wc,
                                              uint32_t rank, int32_t cluster_id,
-                                             uint64_t t_entry) {
+                                             uint64_t t_entry, TileRing& ring) {
   using Cfg = Tc2Config;
   const WorkSpec& W = args.work;
   WorkIter it;
   it.init_tc(W, cluster_id);
   Unit u;
+  const int32_t tiles = W.dp_tiles;
+  int32_t dyn_next = cluster_id;  // leader, dynamic schedule: the tile to publish next
   int s = 0;
   uint32_t ph = 0, filled = 0;
   bool ok = true;
@@ -132,19 +180,48 @@ __device__ __forceinline__ uint32_t tc2_producer(const CUtensorMap& tmA, const C
       trace_mark(args, blockIdx.x, kTraceStart);
     }
   };
+  // The next unit: the static schedule's, or the next tile of the ring (the
+  // leader takes it from the global counter and publishes it first).
+  auto next_unit = [&]() -> bool {
+    if (!args.sched) return it.next(W, u);
+    int32_t t;
+    if (rank == 0) {
+      t = dyn_next < tiles ? dyn_next : -1;
+      if (!ring.publish(t, wc)) return ok = false;
+      if (!waited) prerequisites_done();  // the counter is global memory
+      if (t >= 0) {
+        dyn_next = atomicAdd(args.sched, 1) + W.grid;  // the tile after this one
+      } else if (atomicAdd(args.sched + 1, 1) == W.grid - 1) {
+        // every pair has taken its last tile: ready for the next launch
+        atomicExch(args.sched, 0);
+        atomicExch(args.sched + 1, 0);
+      }
+    } else {
+      if (!ring.wait(wc, kSiteProducer)) return ok = false;
+      t = ring.read();
+      ring.done();
+    }
+    if (t < 0) return false;
+    u.tile = t;
+    u.kb0 = 0;
+    u.kb1 = W.k_iters;
+    return true;
+  };
   const int32_t row_off = int32_t(rank) * kBM;      // this CTA's rows of the A tile
   const int32_t col_off = int32_t(rank) * kHalfBN;  // this CTA's columns of the B tile
-  int32_t nunit = 0;
-  while (ok && it.next(W, u)) {
+  while (ok && next_unit()) {
     int32_t tm, tn;
     tile_coords(W, u.tile, tm, tn);
     const int32_t a_row = tm * kPairBM + row_off;
     const int32_t b_row = tn * kPairBN + col_off;
-    // Every other unit walks k from the last block to the first: the pairs'
-    // next wave of tiles shares the raster group's A row panels with the wave
-    // before, and starting from the k-panels that wave loaded last finds them
-    // still in L2.  tc2_mma follows the same order.
-    const bool rev = (nunit++ & 1) != 0;
+    // Every other wave of tiles walks k from the last block to the first: a
+    // wave shares the raster group's A row panels with the wave before, and
+    // starting from the k-panels that wave loaded last finds them still in
+    // L2.  The wave is counted by tile (tiles are taken in order, a wave of
+    // `pairs` at a time), not by this pair's units, so that a tile's k order,
+    // and with it its fp32 sum, is the same whichever pair computes it.  The
+    // MMA issuer consumes the stages in the order they are loaded.
+    const bool rev = ((u.tile / W.grid) & 1) != 0;
     for (int32_t i = 0; i < u.kb1 - u.kb0; ++i) {
       const int32_t kb = rev ? u.kb1 - 1 - i : u.kb0 + i;
       if (!wait_bounded(smem_u32(&empty[s]), ph ^ 1, wc, kSiteProducer)) {
@@ -212,7 +289,7 @@ template <int S>
 __device__ __forceinline__ void tc2_mma(const TcArgs& args, uint8_t* sA, uint8_t* sB,
                                         uint64_t* full, uint64_t* empty, uint64_t* acc_full,
                                         uint64_t* acc_empty, uint64_t* drain, const WaitCtl& wc,
-                                        uint32_t tmem_base, int32_t cluster_id) {
+                                        uint32_t tmem_base, int32_t cluster_id, TileRing& ring) {
   using Cfg = Tc2Config;
   const WorkSpec& W = args.work;
   WorkIter it;
@@ -221,11 +298,22 @@ __device__ __forceinline__ void tc2_mma(const TcArgs& args, uint8_t* sA, uint8_t
   int s = 0, b = 0;
   uint32_t ph = 0, aph = 0;
   bool ok = true, any = false;
+  auto next_unit = [&]() -> bool {
+    if (!args.sched) return it.next(W, u);
+    if (!ring.wait(wc, kSiteMmaFull)) return ok = false;
+    const int32_t t = ring.read();
+    ring.done();
+    if (t < 0) return false;
+    u.tile = t;
+    u.kb0 = 0;
+    u.kb1 = W.k_iters;
+    return true;
+  };
   const uint32_t a_lbo = args.a_mn ? 8192u : 16u;
   const uint32_t b_lbo = args.b_mn ? 8192u : 16u;
   const uint32_t a_step = args.a_mn ? (2048u >> 4) : (32u >> 4);
   const uint32_t b_step = args.b_mn ? (2048u >> 4) : (32u >> 4);
-  while (ok && it.next(W, u)) {
+  while (ok && next_unit()) {
     // both CTAs' epilogues release each buffer once before its first use
     // (after seeding it, if asked) and once after each drain
     if (!wait_bounded(smem_u32(&acc_empty[b]), aph, wc, kSiteMmaAccum)) {
@@ -369,7 +457,8 @@ __device__ __forceinline__ void tc2_epilogue(const TcArgs& args, uint64_t* acc_f
                                              uint64_t* acc_empty, const WaitCtl& wc,
                                              uint32_t tmem_base, uint32_t rank,
                                              int32_t cluster_id, volatile int* last_flag,
-                                             uint8_t* stage, const CUtensorMap* tmC) {
+                                             uint8_t* stage, const CUtensorMap* tmC,
+                                             TileRing& ring) {
   const WorkSpec& W = args.work;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -396,19 +485,36 @@ __device__ __forceinline__ void tc2_epilogue(const TcArgs& args, uint64_t* acc_f
     __syncwarp();
     if (lane == 0) mbar_arrive_cluster(buf == 0 ? leader_empty0 : leader_empty1);
   };
-  release(0, ahead.next(W, un));
-  release(1, ahead.next(W, un));
+  // (the dynamic schedule runs without the bias seeding, which needs the
+  // unit two ahead)
+  release(0, !args.sched && ahead.next(W, un));
+  release(1, !args.sched && ahead.next(W, un));
   int b = 0;
   uint32_t aph = 0;
   int units = 0;
-  while (it.next(W, u)) {
+  // The next unit: the static schedule's, or the next tile of the ring (all
+  // four warps read the same slot, so they stop together).
+  auto next_unit = [&]() -> bool {
+    if (!args.sched) return it.next(W, u);
+    if (!epi_all(ring.wait(wc, kSiteEpilogue))) return false;
+    const int32_t t = ring.read();
+    __syncwarp();
+    if (lane == 0) ring.done();
+    else ring.advance();
+    if (t < 0) return false;
+    u.tile = t;
+    u.kb0 = 0;
+    u.kb1 = W.k_iters;
+    return true;
+  };
+  while (next_unit()) {
+    int32_t tm, tn;
+    tile_coords(W, u.tile, tm, tn);  // while the MMAs still run
     const bool got = wait_bounded(smem_u32(&acc_full[b]), aph, wc, kSiteEpilogue);
     if (!epi_all(got)) break;
     tc_fence_after();
     if (threadIdx.x == 64) trace_mark(args, blockIdx.x, kTraceLastAccum);
     ++units;
-    int32_t tm, tn;
-    tile_coords(W, u.tile, tm, tn);
     const int32_t mm = tm * kPairBM + int32_t(rank) * kBM + row;
     const int32_t nbase = tn * kPairBN;
     const uint32_t taddr = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(b * kPairBN);
@@ -424,7 +530,7 @@ __device__ __forceinline__ void tc2_epilogue(const TcArgs& args, uint64_t* acc_f
       tc2_split_half<OUT_F16>(args, tmC, stage, taddr, row, mm, nbase, u, rank, cluster_id,
                               last_flag);
     }
-    release(b, ahead.next(W, un));
+    release(b, !args.sched && ahead.next(W, un));
     if (++b == 2) {
       b = 0;
       aph ^= 1;
@@ -461,10 +567,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   uint64_t* acc_full = bars + 2 * S;   // one multicast commit per unit, in both CTAs
   uint64_t* acc_empty = acc_full + 2;  // leader's: 4 epilogue warps x 2 CTAs
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* sched_full = drain + 1;                    // tile ring (dynamic schedule)
+  uint64_t* sched_empty = sched_full + Cfg::kSchedDepth;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sched_empty + Cfg::kSchedDepth);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
   uint32_t* peer_filled = tmem_slot + 3;  // leader: load slots the peer's producer filled
+  int32_t* sched_slot = reinterpret_cast<int32_t*>(tmem_slot + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -481,6 +590,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
       mbar_init(smem_u32(&acc_empty[b]), 2 * (kEpiThreads / 32));
     }
     mbar_init(smem_u32(drain), 1);
+    for (int d = 0; d < Cfg::kSchedDepth; ++d) {
+      mbar_init(smem_u32(&sched_full[d]), 1);
+      mbar_init(smem_u32(&sched_empty[d]), kSchedConsumers);
+    }
     *abort_flag = 0;
     *last_flag = 0;
     fence_barrier_init();
@@ -503,12 +616,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   // stage), which with a programmatic launch overlaps the previous kernel.
   pdl_launch_dependents();
   const WaitCtl wc{args.wait_limit_ns, args.status, abort_flag};
+  TileRing ring{sched_full, sched_empty, sched_slot};
 
   uint32_t filled = 0;  // thread 0: load slots this CTA's producer filled
   if (warp == 0) {
     if (lane == 0) {
       filled = tc2_producer<S>(tmA, tmB, args, sA, sB, full, empty, wc, rank, cluster_id,
-                               t_entry);
+                               t_entry, ring);
       if (rank != 0) st_dsmem_u32(map_to_rank(smem_u32(peer_filled), 0), filled);
     } else {
       pdl_wait_prerequisites();
@@ -517,10 +631,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     pdl_wait_prerequisites();
     if (lane == 0 && rank == 0)
       tc2_mma<S>(args, sA, sB, full, empty, acc_full, acc_empty, drain, wc, tmem_base,
-                 cluster_id);
+                 cluster_id, ring);
   } else {
     tc2_epilogue<OUT_F16>(args, acc_full, acc_empty, wc, tmem_base, rank, cluster_id,
-                          last_flag, stage, &tmC);
+                          last_flag, stage, &tmC, ring);
   }
 
   __syncthreads();

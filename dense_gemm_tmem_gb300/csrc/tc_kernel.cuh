@@ -83,9 +83,13 @@ struct TcArgs {
   uint64_t wait_limit_ns;
   int32_t a_mn, b_mn;     // operand majors in the MMA view (1 = MN-major)
   int32_t c_tma = 0;      // 1: row-major C chunks leave by TMA store (tmC is valid)
+  int32_t c_vec = 0;      // 1: C's base is 16-byte aligned and its row pitch a multiple of
+                          // 16 bytes, so every 4-column group is whole and aligned
   int32_t bias_init = 0;  // 1: each tile's k-block-0 accumulator is seeded with the bias
   uint32_t idesc;         // tcgen05 instruction descriptor
   uint64_t* trace = nullptr;  // NULL, or kTraceSlots %globaltimer stamps per CTA
+  int* sched = nullptr;       // two-SM kernel, whole tiles: NULL for the static schedule,
+                              // else {next-tile counter, finished pairs}, both 0 at launch
 };
 
 // Phase stamps a traced launch writes per CTA (trace[cta * kTraceSlots + i]).
@@ -308,6 +312,62 @@ __device__ __forceinline__ void store_rows_staged(const TcArgs& a, float* sw, in
   }
 }
 
+// The same store when C takes whole, aligned 4-column groups (TcArgs::c_vec):
+// the bounds and alignment are settled once per chunk and the row pointer
+// advances by a fixed step, so the stores of all passes issue back to back
+// instead of one guarded store after another.
+template <int CW, bool OUT_F16>
+__device__ __forceinline__ void store_rows_vec(const TcArgs& a, float* sw, int32_t mrow0,
+                                               int lane, int32_t nn0, const float (&v)[CW]) {
+  constexpr int LD = CW + 4;
+  constexpr int Q = CW / 4;    // float4 per row
+  constexpr int RPI = 32 / Q;  // rows per pass
+  constexpr int kPasses = 32 / RPI;
+  __syncwarp();                // the previous chunk's reads of sw are done
+  float4* mine = reinterpret_cast<float4*>(sw + lane * LD);
+#pragma unroll
+  for (int j = 0; j < Q; ++j)
+    mine[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+  __syncwarp();
+  const int c4 = lane % Q;
+  const int rsub = lane / Q;
+  float4 x[kPasses];
+#pragma unroll
+  for (int it = 0; it < kPasses; ++it)
+    x[it] = *reinterpret_cast<const float4*>(sw + (it * RPI + rsub) * LD + 4 * c4);
+  const int32_t nn = nn0 + 4 * c4;
+  const int32_t r0 = mrow0 + rsub;
+  if (nn >= a.Nm || r0 >= a.Mm) return;  // no warp-wide step follows
+  const float* ob = out_bias(a);
+  if (ob) {
+    const float4 b4 = make_float4(__ldg(ob + nn), __ldg(ob + nn + 1), __ldg(ob + nn + 2),
+                                  __ldg(ob + nn + 3));
+#pragma unroll
+    for (int it = 0; it < kPasses; ++it) {
+      x[it].x += b4.x; x[it].y += b4.y; x[it].z += b4.z; x[it].w += b4.w;
+    }
+  }
+  const int32_t rows = a.Mm - r0;  // > 0: rows of this lane's group left in C
+  const int64_t step = int64_t(RPI) * a.ldc;
+  if constexpr (OUT_F16) {
+    __half* p = reinterpret_cast<__half*>(a.C) + int64_t(r0) * a.ldc + nn;
+#pragma unroll
+    for (int it = 0; it < kPasses; ++it, p += step) {
+      const __half2 h0 = __floats2half2_rn(x[it].x, x[it].y);
+      const __half2 h1 = __floats2half2_rn(x[it].z, x[it].w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<const uint32_t*>(&h0);
+      pk.y = *reinterpret_cast<const uint32_t*>(&h1);
+      if (it * RPI < rows) *reinterpret_cast<uint2*>(p) = pk;
+    }
+  } else {
+    float* p = reinterpret_cast<float*>(a.C) + int64_t(r0) * a.ldc + nn;
+#pragma unroll
+    for (int it = 0; it < kPasses; ++it, p += step)
+      if (it * RPI < rows) *reinterpret_cast<float4*>(p) = x[it];
+  }
+}
+
 // Row-major store of one epilogue warp's 32 rows x 32 columns by TMA: lane i
 // writes row mrow0 + i (bias added, rounded once to the output type) into the
 // warp's 4 KiB box in shared memory, in the layout the tensor map's swizzle
@@ -368,22 +428,26 @@ __device__ __forceinline__ void store_rows_tma(const CUtensorMap* tmC, const TcA
 
 // Any store of an epilogue chunk: transposed stores are already coalesced
 // (lanes are consecutive columns of C); row-major ones leave by TMA store when
-// the launch set one up (32-column chunks), else through the padded staging.
+// the launch set one up (32-column chunks), else through the padded staging
+// (with whole aligned 4-column groups where C allows them).
 template <int CW, bool OUT_F16, bool TRANS>
 __device__ __forceinline__ void store_out(const TcArgs& a, const CUtensorMap* tmC,
                                           uint8_t* stage, int q, int32_t mm, int lane,
                                           int32_t nn0, const float (&v)[CW]) {
   if constexpr (TRANS) {
     store_chunk_trans<CW, OUT_F16>(a, mm, nn0, v);
-  } else if constexpr (CW == 32) {
-    if (a.c_tma)
-      store_rows_tma<OUT_F16>(tmC, a, stage + q * 4096, mm - lane, lane, nn0, v);
-    else
-      store_rows_staged<CW, OUT_F16>(a, reinterpret_cast<float*>(stage) + q * 32 * (CW + 4),
-                                     mm - lane, lane, nn0, v);
   } else {
-    store_rows_staged<CW, OUT_F16>(a, reinterpret_cast<float*>(stage) + q * 32 * (CW + 4),
-                                   mm - lane, lane, nn0, v);
+    if constexpr (CW == 32) {
+      if (a.c_tma) {
+        store_rows_tma<OUT_F16>(tmC, a, stage + q * 4096, mm - lane, lane, nn0, v);
+        return;
+      }
+    }
+    float* sw = reinterpret_cast<float*>(stage) + q * 32 * (CW + 4);
+    if (a.c_vec)
+      store_rows_vec<CW, OUT_F16>(a, sw, mm - lane, lane, nn0, v);
+    else
+      store_rows_staged<CW, OUT_F16>(a, sw, mm - lane, lane, nn0, v);
   }
 }
 
@@ -523,6 +587,67 @@ __device__ __forceinline__ void csplit_reduce_pushed(const TcArgs& a, const uint
     }
     put4<OUT_F16>(a, int64_t(nn) * a.ldc + mm, acc, valid);
   }
+}
+
+// The same exchange for tiles 32 or 64 columns wide with operands in place
+// (row-major output): rank j adds rows [j*R, (j+1)*R) of the tile, and each
+// CTA pushes those rows of its partial into rank j's staging area as
+// slot[src][row][column], 16 bytes at a time.  A row's float4 c4 sits at
+// c4 ^ (row % 8), so the 32 rows a warp pushes at once, and the column groups a
+// warp reads back, fall on different banks although rows are a whole number
+// of 128-byte lines long.
+__device__ __forceinline__ uint32_t push_row_offset(int src, int R, int BN, int r, int c4) {
+  return 4u * uint32_t((src * R + r) * BN + 4 * (c4 ^ (r & 7)));
+}
+
+template <int BN, bool OUT_F16>
+__device__ __forceinline__ void csplit_reduce_pushed_rows(const TcArgs& a, const uint8_t* stage,
+                                                          int tid, int nthreads) {
+  static_assert(BN == 32 || BN == 64, "row pushes: 8 or 16 float4 per row");
+  const WorkSpec& W = a.work;
+  const int s = W.csplit;
+  const int rank = int(blockIdx.x) % s;
+  const int R = kBM / s;
+  int32_t tm, tn;
+  tile_coords(W, int32_t(blockIdx.x) / s, tm, tn);
+  const float* ob = out_bias(a);
+  constexpr int G = BN / 4;  // float4 per row
+  const int groups = R * G;
+#pragma unroll 1
+  for (int g = tid; g < groups; g += nthreads) {
+    const int r = g / G;
+    const int c4 = g % G;
+    float4 part[8];
+#pragma unroll
+    for (int src = 0; src < 8; ++src)
+      if (src < s)
+        part[src] = *reinterpret_cast<const float4*>(stage + push_row_offset(src, R, BN, r, c4));
+    float4 acc = part[0];
+#pragma unroll
+    for (int src = 1; src < 8; ++src)
+      if (src < s) {
+        acc.x += part[src].x; acc.y += part[src].y; acc.z += part[src].z; acc.w += part[src].w;
+      }
+    const int32_t mm = tm * kBM + rank * R + r;
+    const int32_t nn = tn * BN + 4 * c4;
+    if (mm >= a.Mm || nn >= a.Nm) continue;
+    const int valid = min(4, a.Nm - nn);
+    if (ob) {
+      acc.x += __ldg(ob + nn);
+      if (valid > 1) acc.y += __ldg(ob + nn + 1);
+      if (valid > 2) acc.z += __ldg(ob + nn + 2);
+      if (valid > 3) acc.w += __ldg(ob + nn + 3);
+    }
+    put4<OUT_F16>(a, int64_t(mm) * a.ldc + nn, acc, valid);
+  }
+}
+
+// 16-byte store into a cluster CTA's shared memory.
+__device__ __forceinline__ void st_dsmem_f32x4(uint32_t cluster_addr, float x, float y, float z,
+                                               float w) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(x),
+               "f"(y), "f"(z), "f"(w)
+               : "memory");
 }
 
 template <int BN, bool OUT_F16, bool TRANS>
@@ -749,13 +874,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t aph = 0;
     int units = 0;
     while (it.next(W, u)) {
+      int32_t tm, tn;
+      tile_coords(W, u.tile, tm, tn);  // while the MMAs still run
       const bool got = wait_bounded(smem_u32(&acc_full[b]), aph, wc, kSiteEpilogue);
       if (!epi_all(got)) break;
       tc_fence_after();
       if (et == 0) trace_mark(args, blockIdx.x, kTraceLastAccum);
       ++units;
-      int32_t tm, tn;
-      tile_coords(W, u.tile, tm, tn);
       const int32_t mm = tm * kBM + row;
       const int32_t nbase = tn * BN;
       const uint32_t taddr = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(b * BN);
@@ -778,6 +903,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int j = 0; j < CW; ++j)
             st_dsmem_f32(dst + 4u * uint32_t((src * BN + c * CW + j) * R + r_in), v[j]);
+        }
+      } else if (!TRANS && kPushReduce<BN> && W.csplit > 1) {
+        // Cluster split, narrow tile in place: push each row of the partial
+        // to the rank that adds it (csplit_reduce_pushed_rows).
+        const int s = W.csplit;
+        const int R = kBM / s;
+        const int owner = row / R;
+        const int r_in = row - owner * R;
+        const int src = int(blockIdx.x) % s;
+        const uint32_t dst = map_to_rank(smem_u32(stage), uint32_t(owner));
+#pragma unroll 1
+        for (int c = 0; c < BN / CW; ++c) {
+          float v[CW];
+          __syncwarp();
+          tmem_load_chunk<CW>(taddr + c * CW, v);
+#pragma unroll
+          for (int j = 0; j < CW / 4; ++j)
+            st_dsmem_f32x4(dst + push_row_offset(src, R, BN, r_in, c * (CW / 4) + j), v[4 * j],
+                           v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
         }
       } else if (W.csplit > 1) {
         // Cluster split: park this CTA's fp32 partial in its own (now idle)
@@ -915,8 +1059,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // the tail's stamps come from the thread that stamped the epilogue's end,
     // so they are ordered however the timer reads are scheduled
     if (threadIdx.x == kStampThread) trace_mark(args, blockIdx.x, kTraceClusterParked);
-    if constexpr (TRANS && kPushReduce<BN>) {
-      csplit_reduce_pushed<BN, OUT_F16>(args, stage, threadIdx.x, kTcThreads);
+    if constexpr (kPushReduce<BN>) {
+      if constexpr (TRANS)
+        csplit_reduce_pushed<BN, OUT_F16>(args, stage, threadIdx.x, kTcThreads);
+      else
+        csplit_reduce_pushed_rows<BN, OUT_F16>(args, stage, threadIdx.x, kTcThreads);
       if (threadIdx.x == kStampThread) {
         trace_mark(args, blockIdx.x, kTraceClusterReduced);
         trace_mark(args, blockIdx.x, kTraceClusterDone);

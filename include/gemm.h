@@ -127,10 +127,16 @@ enum {
                                     is a multiple of 16 bytes: -1 (default) for fp16 output or
                                     launches with more output tiles than CTAs, 1 always,
                                     0 never (plain stores) */
-  GEMM_OPT_BIAS_INIT = 12        /* 1: the tensor-core kernels start each tile's fp32
+  GEMM_OPT_BIAS_INIT = 12,       /* 1: the tensor-core kernels start each tile's fp32
                                     reduction from the bias (seeded into the accumulator
                                     before the first MMA) instead of adding it to the sum;
                                     0 (default): added to the finished fp32 sum */
+  GEMM_OPT_DYNAMIC_TILES = 13    /* two-SM kernel with whole tiles: 1 (default) each pair
+                                    takes its next tile from a counter in the handle at run
+                                    time, so the tiles in flight stay in raster order; 0 the
+                                    static schedule gemm_work_units reports (pair c takes
+                                    tiles c, c + pairs, ...).  The split tail and the bias
+                                    seeding always use the static schedule. */
 };
 
 /* Creates a handle on CUDA device `device`.  Allocates, on that device, the
@@ -194,6 +200,17 @@ int gemm_status(gemm_handle_t h, void *stream);
  * waiting for data, 3 MMA issuer waiting for an accumulator, 4 epilogue,
  * 5 drain, 6 the self-test below). */
 int gemm_status_detail(gemm_handle_t h);
+
+/* Failure injection for tests of the error paths: with n > 0, the n-th
+ * device allocation this library makes from now on (1 = the next one; in any
+ * thread, on any handle) fails as if the device memory were exhausted, so the
+ * call that makes it returns GEMM_ERR_ALLOC.  gemm_create makes three (the
+ * workspace, the tile counters, the status word) and frees whatever it made
+ * before the failure; gemm_run_host makes one when its buffers grow, and the
+ * handle stays usable (its buffers are then empty and grow on the next call).
+ * n == 0 disarms.  gemm_run_noalloc makes no allocation and is not affected.
+ * Errors: INVALID_ARG (n < 0). */
+int gemm_inject_alloc_failure(int64_t n);
 
 /* Phase tracing for the tensor-core kernels.  dev_buf: NULL (tracing off) or a
  * caller-owned DEVICE buffer of ctas x 12 uint64 values; while set, every

@@ -200,6 +200,27 @@ def test_pair_grid_sizes(g, dev, grid):
     full_check(g, dev, p)
 
 
+@pytest.mark.parametrize("odt", [F16, F32])
+def test_pair_dynamic_matches_static(g, dev, odt):
+    """Two-SM kernel over several waves of whole tiles (9 x 17 pair tiles,
+    ragged on both sides): by default the pairs take tiles from a counter at
+    run time; with GEMM_OPT_DYNAMIC_TILES = 0, in the static order.  A tile's
+    k order depends on the tile alone, so both give the same bits, which
+    match the oracle; the counter resets itself at the end of a launch, so a
+    second launch gives them again."""
+    p = problem(2048 + 40, 4096 + 8, 1032, 0, 1, F16, odt, True, 160)
+    set_opts(g, kernel=TC2)
+    assert g.plan(p.M, p.N, p.K, 0, 1, B.GEMM_F16,
+                  B.GEMM_F16 if odt == F16 else B.GEMM_F32)["dp_tiles"] == 9 * 17
+    C_dyn = run(g, p, dev)
+    C_dyn2 = run(g, p, dev)
+    set_opts(g, dyn=0)
+    C_st = run(g, p, dev)
+    assert torch.equal(C_dyn, C_dyn2) and torch.equal(C_dyn, C_st)
+    rows = sample_rows(p.M, 13)
+    check(as_f64(C_dyn, rows), oracle.gemm_rows(p.A, p.B, p.bias, b_major=1, rows=rows), p, rows)
+
+
 @pytest.mark.parametrize("grid", [2, 10, 38, 152])
 def test_pair_split_grid_sizes(g, dev, grid):
     """Two-SM Stream-K: every pair tile's k-blocks split over grid / 2 pairs;
@@ -600,12 +621,13 @@ def test_wait_timeout_selftest(g, dev):
 
 @pytest.mark.parametrize("kernel,shape", [
     (TC, (1024, 1024, 8192)),     # one-SM kernel, whole tiles
-    (SK, (512, 512, 8192)),       # one-SM kernel, Stream-K partials through the workspace
-    (SPLITC, (512, 512, 8192)),   # one-SM kernel, cluster split (partials on chip)
+    (SK, (512, 512, 65536)),      # one-SM kernel, Stream-K partials through the workspace
+    (SPLITC, (512, 512, 32768)),  # one-SM kernel, cluster split (partials on chip)
     (TC2, (2048, 2048, 8192)),    # two-SM kernel (CTA pairs)
 ])
 def test_real_kernel_wait_timeout(g, dev, kernel, shape):
-    """A wait limit of 1 us, far shorter than a launch, makes the kernels' own
+    """Each CTA of these launches waits tens of microseconds for its first
+    accumulator.  A wait limit of 1 us makes the kernels' own
     bounded waits give up mid-launch: gemm_status reports
     GEMM_ERR_DEVICE_TIMEOUT with the role whose wait expired first (TMA
     producer, MMA issuer or epilogue; never the clean-up, whose waits keep at
@@ -626,6 +648,43 @@ def test_real_kernel_wait_timeout(g, dev, kernel, shape):
     g.status()
     rows = sample_rows(M, 9)
     check(as_f64(C, rows), oracle.gemm_rows(p.A, p.B, p.bias, b_major=1, rows=rows), p, rows)
+
+
+def test_alloc_failure_injection(dev):
+    """Allocation failures made on the host (gemm_inject_alloc_failure): each
+    of gemm_create's three device allocations in turn fails with
+    GEMM_ERR_ALLOC and leaves nothing allocated; a failed buffer growth in
+    gemm_run_host returns GEMM_ERR_ALLOC and the handle keeps working, on
+    device buffers and, once the failure is disarmed, on host buffers."""
+    import ctypes
+    lib = B.load()
+    torch.cuda.synchronize(dev)
+    free0 = torch.cuda.mem_get_info(dev)[0]
+    try:
+        for k in (1, 2, 3):
+            assert B.gemm_inject_alloc_failure(k) == B.GEMM_OK
+            h = ctypes.c_void_p()
+            assert lib.gemm_create(ctypes.byref(h), dev.index) == B.GEMM_ERR_ALLOC
+            assert not h.value
+        assert B.gemm_inject_alloc_failure(0) == B.GEMM_OK
+        torch.cuda.synchronize(dev)
+        assert abs(torch.cuda.mem_get_info(dev)[0] - free0) < (4 << 20)  # the 38 MiB workspace is gone
+        g = Gemm(dev)
+        p = problem(300, 260, 200, 0, 1, F16, F32, True, 170)
+        hA, hB, hbias = (torch.from_numpy(x).pin_memory() for x in (p.A, p.B, p.bias))
+        hC = torch.empty((p.M, p.N), dtype=torch.float32).pin_memory()
+        B.gemm_inject_alloc_failure(1)
+        with pytest.raises(B.GemmError) as e:
+            g.run_host(hA, hB, hC, hbias, 0, 1)
+        assert e.value.code == B.GEMM_ERR_ALLOC
+        B.gemm_inject_alloc_failure(0)
+        full_check(g, dev, p)  # device buffers: unaffected
+        g.run_host(hA, hB, hC, hbias, 0, 1)
+        g.status()
+        check(as_f64(hC), oracle.gemm(p.A, p.B, p.bias, b_major=1), p)
+        g.close()
+    finally:
+        B.gemm_inject_alloc_failure(0)
 
 
 # ------------------------------------------------- the named workloads --
@@ -654,7 +713,8 @@ def test_workload_skinny_full(g, dev, M):
 
 @pytest.mark.parametrize("name,kind", [("gemm8192_f16_bias_f16out", None),
                                        ("gemm8192_f16_bias_f16out", "int"),
-                                       ("gemm16384_f16_f16out", None)])
+                                       ("gemm16384_f16_f16out", None),
+                                       ("gemm16384_f16_f16out", "int")])
 def test_workload_large_sampled_rows(g, dev, name, kind):
     """Full-size launch (the configuration the benchmark times), checked on one
     seeded row per 128-row tile plus edge rows, all N columns each."""

@@ -320,3 +320,11 @@ def test_drain_limit_has_a_floor():
         assert B.gemm_drain_limit_ns(limit) == 1_000_000_000
     assert B.gemm_drain_limit_ns(5_000_000_000) == 5_000_000_000
     assert B.gemm_drain_limit_ns(0) == B.gemm_drain_limit_ns(-1) == 2_000_000_000
+
+
+def test_alloc_failure_injection_arguments():
+    """The allocation-failure injector takes n >= 0 (0 disarms) and needs no
+    GPU to be armed or disarmed."""
+    assert B.gemm_inject_alloc_failure(-1) == B.GEMM_ERR_INVALID_ARG
+    assert B.gemm_inject_alloc_failure(3) == B.GEMM_OK
+    assert B.gemm_inject_alloc_failure(0) == B.GEMM_OK
