@@ -54,6 +54,9 @@ bool log_enabled() {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Tile width 16, 32, 64, 128, 256 -> 0 ... 4 (Options::lean_stages).
+int width_index(int bn) { return bn == 16 ? 0 : bn == 32 ? 1 : bn == 64 ? 2 : bn == 128 ? 3 : 4; }
+
 // Allocation-failure injection (gemm_inject_alloc_failure): when armed with n,
 // the n-th device allocation from now fails as if the device were full.
 std::atomic<int64_t> g_fail_alloc_in{0};
@@ -378,6 +381,16 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
       p->tile_n = bn;
       p->tile_k = kBK;
       p->stages = tc_stages_for(bn);
+      // A split over more than half the SMs leaves too few idle for the next
+      // launch's CTAs to start early: with a ring short enough that two CTAs
+      // share an SM, they start beside this launch's and have their setup and
+      // first loads done when it ends.  The split's own k-range needs few
+      // stages.  (Parked partials need the ring to hold the partial tile.)
+      const int lean = o.lean_stages[width_index(bn)][swap ? 1 : 0];
+      if (lean > 0 && T * cs > G / 2) p->stages = std::min(p->stages, lean);
+      if (o.stages > 0) p->stages = std::min(o.stages, tc_stages_for(bn));
+      // Tiles wider than 64 park their partial in the ring: it must hold it.
+      p->stages = std::max(p->stages, tc_min_stages(bn, cs));
       p->grid = int32_t(T * cs);
       p->tiles_m = int32_t(tiles_m);
       p->tiles_n = int32_t(tiles_n);
@@ -437,7 +450,7 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
   p->tile_m = kBM;
   p->tile_n = bn;
   p->tile_k = kBK;
-  p->stages = tc_stages_for(bn);
+  p->stages = o.stages > 0 ? std::min(o.stages, tc_stages_for(bn)) : tc_stages_for(bn);
   p->grid = int32_t(grid);
   p->tiles_m = int32_t(tiles_m);
   p->tiles_n = int32_t(tiles_n);
@@ -625,6 +638,23 @@ cudaError_t launch_tc(const TcLaunch& L) {
   return launch_tc_small(L);
 }
 
+int tc_lean_stages(int bn, bool trans) {
+  switch (bn) {
+    case 16: return trans ? lean_stages_small(16) : 0;
+    case 32: return trans ? lean_stages_small(32) : lean_stages_narrow(32);
+    case 64: return trans ? lean_stages_small(64) : lean_stages_narrow(64);
+    case 128: return lean_stages_n128(trans);
+    default: return 0;
+  }
+}
+
+int tc_min_stages(int bn, int csplit) {
+  if (csplit <= 1 || bn <= 64) return 1;  // no parked partial
+  const int64_t park = int64_t(kBM) * (bn + 4) * 4;  // rows (or columns) padded by 4 floats
+  const int64_t stage = int64_t(kBM + bn) * kBK * 2;
+  return int((park + stage - 1) / stage);
+}
+
 int tc_stages_for(int bn) {
   switch (bn) {
     case 256: return TcConfig<256>::kStages;
@@ -742,6 +772,14 @@ int gemm_create(gemm_handle_t* out, int device) {
       // a failed query leaves the SMs / s estimate
       h->opt.csplit_clusters[s] = n > 0 ? std::min(n, h->num_sms / s) : n == 0 ? -1 : h->num_sms / s;
     }
+    for (int bn : {16, 32, 64, 128})
+      for (int t = 0; t < 2; ++t) {
+        h->opt.lean_stages[dg::width_index(bn)][t] = dg::tc_lean_stages(bn, t != 0);
+        if (dg::log_enabled())
+          std::fprintf(stderr, "[gemm] device %d: tile width %d%s: two CTAs per SM with %d stages\n",
+                       device, bn, t ? " (swapped)" : "",
+                       h->opt.lean_stages[dg::width_index(bn)][t]);
+      }
     const int simt = dg::simt_ctas_per_sm();
     h->opt.simt_per_sm = simt > 0 ? simt : 2;
     h->workspace_bytes = size_t(2) * h->num_sms * dg::kBM * dg::kMaxTileN * sizeof(float);
@@ -841,6 +879,9 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value) {
     case GEMM_OPT_DYNAMIC_TILES:
       if (value > 1) return GEMM_ERR_INVALID_ARG;
       o.dyn_sched = value < 0 ? d.dyn_sched : int(value);
+      return GEMM_OK;
+    case GEMM_OPT_STAGES:
+      o.stages = value <= 0 ? d.stages : int(std::min<int64_t>(value, 64));
       return GEMM_OK;
     default:
       return GEMM_ERR_INVALID_ARG;
@@ -964,6 +1005,7 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, co
   // keep the static schedule.
   if (pair && plan.sk_tiles == 0 && !a.bias_init && h->opt.dyn_sched != 0)
     a.sched = h->tickets + dg::kTicketCap;
+  a.stages = pair ? 0 : plan.stages;
   // phase stamps only if the caller's buffer holds one row per CTA
   a.trace = (h->trace && h->trace_ctas >= plan.grid) ? h->trace : nullptr;
   a.idesc = dg::make_idesc_f16(pair ? dg::kPairBM : dg::kBM, plan.tile_n, plan.a_mn_major,

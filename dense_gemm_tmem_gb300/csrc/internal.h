@@ -29,6 +29,10 @@ struct Options {
                            // output or more output tiles than CTAs, 1 always, 0 never
   int bias_init = 0;       // seed the accumulators with the bias
   int dyn_sched = 1;       // two-SM kernel, whole tiles: tiles handed out at run time
+  int stages = -1;         // one-SM kernel ring stages: -1 picker, n >= 1 forced
+  // per tile width (16, 32, 64, 128, 256 -> 0..4) and operand order: the most
+  // stages that let two CTAs share an SM (0: none); set per device
+  int lean_stages[5][2] = {{0, 0}, {0, 0}, {0, 0}, {0, 0}, {0, 0}};
   int csplit_clusters[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};  // clusters of s resident (0: SMs/s)
   int simt_per_sm = 0;     // 128 x 128 CUDA-core CTAs resident per SM (0: 2); set per device
   uint64_t wait_limit_ns = 2000000000ull;
@@ -79,6 +83,18 @@ int tc2_max_active_clusters(bool out_f16);
 int tc_max_active_clusters(int s);
 int tc_stages_for(int bn);
 int tc_smem_bytes_for(int bn);
+// Fewest ring stages a launch of tile width bn with a cluster split of
+// csplit may use (a tile wider than 64 parks its fp32 partial in the ring).
+int tc_min_stages(int bn, int csplit);
+// Fewest stages a launch that shares its SM with the next launch may use.
+constexpr int kLeanMinStages = 3;
+// The most ring stages with which two CTAs of the one-SM kernel of tile width
+// bn (either output type) fit on one SM, or 0: the per-file queries and the
+// dispatcher over them.
+int lean_stages_small(int bn);
+int lean_stages_narrow(int bn);
+int lean_stages_n128(bool trans);
+int tc_lean_stages(int bn, bool trans);
 
 // CUDA-core GEMM with fp32 accumulation (simt_kernel.cuh): fp32 inputs
 // (simt.cu), or fp16 inputs the tensor-core path cannot read (simt_f16.cu).

@@ -65,7 +65,11 @@ struct TcConfig {
   static constexpr int kEpiStageBytes = BN == 64 ? 32768 : 4 * 32 * (kChunk + 4) * 4;
   static_assert(kEpiStageBytes % 1024 == 0 && (kChunk != 32 || kEpiStageBytes >= 4 * 4096),
                 "staging area");
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes + kEpiStageBytes;
+  // dynamic shared memory of a launch with `stages` ring stages (at most kStages)
+  static constexpr int smem_bytes(int stages) {
+    return 1024 + stages * kStageBytes + kBarBytes + kEpiStageBytes;
+  }
+  static constexpr int kSmemBytes = smem_bytes(kStages);
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128");
   static_assert((2 * kStages + 5) * 8 + 16 <= kBarBytes, "barrier area");
@@ -86,6 +90,7 @@ struct TcArgs {
   int32_t c_vec = 0;      // 1: C's base is 16-byte aligned and its row pitch a multiple of
                           // 16 bytes, so every 4-column group is whole and aligned
   int32_t bias_init = 0;  // 1: each tile's k-block-0 accumulator is seeded with the bias
+  int32_t stages = 0;      // ring stages of this launch, 1 ... TcConfig<BN>::kStages (0: all)
   uint32_t idesc;         // tcgen05 instruction descriptor
   uint64_t* trace = nullptr;  // NULL, or kTraceSlots %globaltimer stamps per CTA
   int* sched = nullptr;       // two-SM kernel, whole tiles: NULL for the static schedule,
@@ -656,7 +661,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                    const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcArgs args) {
   using Cfg = TcConfig<BN>;
-  constexpr int S = Cfg::kStages;
+  // A launch may use fewer stages than the ring can hold: less shared memory,
+  // so that the next launch's CTAs fit beside this one's.
+  const int S = args.stages > 0 ? args.stages : Cfg::kStages;
   constexpr int CW = Cfg::kChunk;
 
   const uint64_t t_entry = args.trace ? globaltimer_ns() : 0;

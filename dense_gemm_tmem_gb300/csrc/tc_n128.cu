@@ -11,4 +11,13 @@ cudaError_t launch_tc_n128(const TcLaunch& L) {
 // Cluster-split capacity: every instantiation uses one CTA per SM and about
 // the same shared memory, so one of them stands for all.
 int tc_max_active_clusters(int s) { return max_active_clusters_inst<128, false, false>(s); }
+
+int lean_stages_n128(bool trans) {
+  auto both = [](int a, int b) { return a < b ? a : b; };
+  if (trans)
+    return both(stages_for_two_per_sm<128, false, true>(kLeanMinStages),
+                stages_for_two_per_sm<128, true, true>(kLeanMinStages));
+  return both(stages_for_two_per_sm<128, false, false>(kLeanMinStages),
+              stages_for_two_per_sm<128, true, false>(kLeanMinStages));
+}
 }  // namespace dg

@@ -14,4 +14,18 @@ cudaError_t launch_tc_narrow(const TcLaunch& L) {
       return cudaErrorInvalidValue;
   }
 }
+
+int lean_stages_narrow(int bn) {
+  auto both = [](int a, int b) { return a < b ? a : b; };
+  switch (bn) {
+    case 32:
+      return both(stages_for_two_per_sm<32, false, false>(kLeanMinStages),
+                  stages_for_two_per_sm<32, true, false>(kLeanMinStages));
+    case 64:
+      return both(stages_for_two_per_sm<64, false, false>(kLeanMinStages),
+                  stages_for_two_per_sm<64, true, false>(kLeanMinStages));
+    default:
+      return 0;
+  }
+}
 }  // namespace dg

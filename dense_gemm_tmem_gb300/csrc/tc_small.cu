@@ -15,4 +15,21 @@ cudaError_t launch_tc_small(const TcLaunch& L) {
       return cudaErrorInvalidValue;
   }
 }
+
+int lean_stages_small(int bn) {
+  auto both = [](int a, int b) { return a < b ? a : b; };
+  switch (bn) {
+    case 16:
+      return both(stages_for_two_per_sm<16, false, true>(kLeanMinStages),
+                  stages_for_two_per_sm<16, true, true>(kLeanMinStages));
+    case 32:
+      return both(stages_for_two_per_sm<32, false, true>(kLeanMinStages),
+                  stages_for_two_per_sm<32, true, true>(kLeanMinStages));
+    case 64:
+      return both(stages_for_two_per_sm<64, false, true>(kLeanMinStages),
+                  stages_for_two_per_sm<64, true, true>(kLeanMinStages));
+    default:
+      return 0;
+  }
+}
 }  // namespace dg

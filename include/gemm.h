@@ -131,12 +131,18 @@ enum {
                                     reduction from the bias (seeded into the accumulator
                                     before the first MMA) instead of adding it to the sum;
                                     0 (default): added to the finished fp32 sum */
-  GEMM_OPT_DYNAMIC_TILES = 13    /* two-SM kernel with whole tiles: 1 (default) each pair
+  GEMM_OPT_DYNAMIC_TILES = 13,   /* two-SM kernel with whole tiles: 1 (default) each pair
                                     takes its next tile from a counter in the handle at run
                                     time, so the tiles in flight stay in raster order; 0 the
                                     static schedule gemm_work_units reports (pair c takes
                                     tiles c, c + pairs, ...).  The split tail and the bias
                                     seeding always use the static schedule. */
+  GEMM_OPT_STAGES = 14           /* one-SM tensor-core kernel: shared-memory ring stages.
+                                    -1 (default) the picker's: all the ring holds, or, for a
+                                    cluster split over more than half the SMs, as many as
+                                    let two CTAs share an SM (so the next launch's CTAs
+                                    start beside this one's); n >= 1 forced (at most the
+                                    ring's size) */
 };
 
 /* Creates a handle on CUDA device `device`.  Allocates, on that device, the
@@ -178,12 +184,15 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A,
  * completes before the call returns.  The device buffers grow to the largest
  * problem seen on the handle (a call that grows them first waits for the
  * handle's previous gemm_run_host call to finish) and are freed by
- * gemm_destroy.  Calls on one handle run in call order whatever their
- * streams: each call's copies wait (on the device) for the previous call's
- * work, so they never overwrite buffers still in use.  For one step's copies
- * to overlap another's compute, use two handles on two streams.  Not for
- * stream capture.  Errors: gemm_run's, ALLOC, and CUDA (a copy, event or
- * stream call failed). */
+ * gemm_destroy.  gemm_run_host calls on one handle run in call order
+ * whatever their streams: each call's copies wait (on the device) for the
+ * previous gemm_run_host call's work, so they never overwrite buffers still
+ * in use.  That ordering covers gemm_run_host calls only: a gemm_run on the
+ * same handle shares its workspace and counters with no such ordering, so,
+ * as for gemm_run, one handle must not run on two streams at once unless the
+ * caller orders the streams.  For one step's copies to overlap another's
+ * compute, use two handles on two streams.  Not for stream capture.
+ * Errors: gemm_run's, ALLOC, and CUDA (a copy, event or stream call failed). */
 int gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A,
                   const void *B, const float *bias, void *C, gemm_layout_t layout,
                   void *stream);

@@ -101,7 +101,8 @@ def set_opts(g, **kw):
              "min_split": B.GEMM_OPT_MIN_SPLIT_ITERS, "group_m": B.GEMM_OPT_GROUP_M,
              "pair": B.GEMM_OPT_PAIR, "csplit": B.GEMM_OPT_CLUSTER_SPLIT,
              "pair_split": B.GEMM_OPT_PAIR_SPLIT, "tma_store": B.GEMM_OPT_TMA_STORE,
-             "bias_init": B.GEMM_OPT_BIAS_INIT, "dyn": B.GEMM_OPT_DYNAMIC_TILES}
+             "bias_init": B.GEMM_OPT_BIAS_INIT, "dyn": B.GEMM_OPT_DYNAMIC_TILES,
+             "stages": B.GEMM_OPT_STAGES}
     for k, v in kw.items():
         g.set_option(names[k], v)
 
@@ -110,5 +111,6 @@ def reset_opts(g):
     for opt in (B.GEMM_OPT_FORCE_KERNEL, B.GEMM_OPT_FORCE_TILE_N, B.GEMM_OPT_FORCE_GRID,
                 B.GEMM_OPT_FORCE_SWAP_AB, B.GEMM_OPT_MIN_SPLIT_ITERS, B.GEMM_OPT_GROUP_M,
                 B.GEMM_OPT_PAIR, B.GEMM_OPT_CLUSTER_SPLIT, B.GEMM_OPT_PAIR_SPLIT,
-                B.GEMM_OPT_TMA_STORE, B.GEMM_OPT_BIAS_INIT, B.GEMM_OPT_DYNAMIC_TILES):
+                B.GEMM_OPT_TMA_STORE, B.GEMM_OPT_BIAS_INIT, B.GEMM_OPT_DYNAMIC_TILES,
+                B.GEMM_OPT_STAGES):
         g.set_option(opt, -1)

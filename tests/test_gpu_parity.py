@@ -169,6 +169,33 @@ def test_swapped_tile_widths(g, dev, tile_n, kernel):
     full_check(g, dev, p)
 
 
+@pytest.mark.parametrize("kernel,tile_n,stages,want", [
+    (TC, -1, 1, 1), (TC, -1, 2, 2), (SK, -1, 3, 3),
+    (SPLITC, 64, 1, 1),     # partials pushed into the staging area: any ring
+    (SPLITC, 128, 1, 3),    # parked in the ring: it must hold 128 x 132 fp32
+    (SPLITC, 128, 3, 3)])
+def test_short_rings(g, dev, kernel, tile_n, stages, want):
+    """The one-SM kernel with a ring of 1 to 3 stages (a launch may use fewer
+    stages than the ring holds): every stage is refilled many times.  A
+    cluster split that parks its partial in the ring keeps enough stages to
+    hold it, whatever is asked."""
+    set_opts(g, kernel=kernel, tile_n=tile_n, stages=stages)
+    p = problem(296, 520, 1000, 0, 1, F16, F32, True, 180 + stages)
+    assert g.plan(296, 520, 1000, 0, 1)["stages"] == want
+    full_check(g, dev, p)
+
+
+def test_lean_ring_for_wide_cluster_split(g, dev):
+    """A cluster split over more than half the SMs runs with a ring short
+    enough for two CTAs per SM where the kernel's registers allow it (so the
+    next launch's CTAs start beside this one's): skinny M = 16."""
+    w = inputs.WORKLOADS["skinny_m16_4096"]
+    pl = g.plan(w.M, w.N, w.K, w.a_major, w.b_major, B.GEMM_F16, B.GEMM_F32)
+    assert pl["kernel"] == SPLITC and pl["grid"] > 76
+    assert 3 <= pl["stages"] <= 5
+    full_check(g, dev, w.make())
+
+
 @pytest.mark.parametrize("grid", [1, 5, 37, 152])
 def test_split_grid_sizes(g, dev, grid):
     """Stream-K with awkward CTA counts: ranges start and end mid-tile."""
