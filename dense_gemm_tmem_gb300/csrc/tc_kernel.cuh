@@ -467,13 +467,11 @@ __device__ __forceinline__ void store_out(const TcArgs& a, const CUtensorMap* tm
 // at once: the reduction is bound by the round trip to the peers' memory.
 template <int BN, bool OUT_F16, bool TRANS>
 __device__ __forceinline__ void csplit_reduce(const TcArgs& a, const uint8_t* smem, int tid,
-                                              int nthreads) {
+                                              int nthreads, int32_t tm, int32_t tn) {
   const WorkSpec& W = a.work;
   const int s = W.csplit;
-  const int rank = int(blockIdx.x) % s;
+  const int rank = int(blockIdx.x) & (s - 1);
   const int R = kBM / s;  // 64, 32 or 16 rows
-  int32_t tm, tn;
-  tile_coords(W, int32_t(blockIdx.x) / s, tm, tn);
   const uint32_t local = smem_u32(smem);
   uint32_t peer[8];
 #pragma unroll
@@ -555,13 +553,12 @@ constexpr bool kPushReduce = BN <= 64;
 
 template <int BN, bool OUT_F16>
 __device__ __forceinline__ void csplit_reduce_pushed(const TcArgs& a, const uint8_t* stage,
-                                                     int tid, int nthreads) {
+                                                     int tid, int nthreads, int32_t tm,
+                                                     int32_t tn) {
   const WorkSpec& W = a.work;
   const int s = W.csplit;
-  const int rank = int(blockIdx.x) % s;
+  const int rank = int(blockIdx.x) & (s - 1);
   const int R = kBM / s;
-  int32_t tm, tn;
-  tile_coords(W, int32_t(blockIdx.x) / s, tm, tn);
   const float* slot = reinterpret_cast<const float*>(stage);
   const float* ob = out_bias(a);
   const int groups = BN * (R / 4);  // 4 consecutive rows of one column each
@@ -607,14 +604,13 @@ __device__ __forceinline__ uint32_t push_row_offset(int src, int R, int BN, int 
 
 template <int BN, bool OUT_F16>
 __device__ __forceinline__ void csplit_reduce_pushed_rows(const TcArgs& a, const uint8_t* stage,
-                                                          int tid, int nthreads) {
+                                                          int tid, int nthreads, int32_t tm,
+                                                          int32_t tn) {
   static_assert(BN == 32 || BN == 64, "row pushes: 8 or 16 float4 per row");
   const WorkSpec& W = a.work;
   const int s = W.csplit;
-  const int rank = int(blockIdx.x) % s;
+  const int rank = int(blockIdx.x) & (s - 1);
   const int R = kBM / s;
-  int32_t tm, tn;
-  tile_coords(W, int32_t(blockIdx.x) / s, tm, tn);
   const float* ob = out_bias(a);
   constexpr int G = BN / 4;  // float4 per row
   const int groups = R * G;
@@ -1060,6 +1056,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   __syncthreads();
   if (W.csplit > 1) {
+    // The cluster's tile (s = 2, 4 or 8 CTAs per tile), worked out before
+    // the barrier, whose wait hides the divisions.
+    int32_t ctm, ctn;
+    tile_coords(W, int32_t(blockIdx.x) >> (W.csplit == 8 ? 3 : W.csplit == 4 ? 2 : 1), ctm, ctn);
     // Every thread of every CTA of the cluster reaches the barriers, aborted
     // or not, so none can wait forever.
     cluster_sync_all();  // all partials parked (or pushed to their owners)
@@ -1068,15 +1068,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (threadIdx.x == kStampThread) trace_mark(args, blockIdx.x, kTraceClusterParked);
     if constexpr (kPushReduce<BN>) {
       if constexpr (TRANS)
-        csplit_reduce_pushed<BN, OUT_F16>(args, stage, threadIdx.x, kTcThreads);
+        csplit_reduce_pushed<BN, OUT_F16>(args, stage, threadIdx.x, kTcThreads, ctm, ctn);
       else
-        csplit_reduce_pushed_rows<BN, OUT_F16>(args, stage, threadIdx.x, kTcThreads);
+        csplit_reduce_pushed_rows<BN, OUT_F16>(args, stage, threadIdx.x, kTcThreads, ctm, ctn);
       if (threadIdx.x == kStampThread) {
         trace_mark(args, blockIdx.x, kTraceClusterReduced);
         trace_mark(args, blockIdx.x, kTraceClusterDone);
       }
     } else {
-      csplit_reduce<BN, OUT_F16, TRANS>(args, smem, threadIdx.x, kTcThreads);
+      csplit_reduce<BN, OUT_F16, TRANS>(args, smem, threadIdx.x, kTcThreads, ctm, ctn);
       if (threadIdx.x == kStampThread) trace_mark(args, blockIdx.x, kTraceClusterReduced);
       cluster_sync_all();  // no CTA still reads another's shared memory
       if (threadIdx.x == kStampThread) trace_mark(args, blockIdx.x, kTraceClusterDone);
