@@ -47,6 +47,9 @@ def parse():
                          "replaying them as one CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target duration of the CPU-baseline sample")
+    ap.add_argument("--opt", action="append", default=[], metavar="NAME=VALUE",
+                    help="set a library option before timing, e.g. DYNAMIC_TILES=0 or "
+                         "GROUP_M=4 (the GEMM_OPT_ names of include/gemm.h); repeatable")
     return ap.parse_args()
 
 
@@ -332,6 +335,11 @@ def run_ours(args):
     w = inputs.WORKLOADS[args.workload]
     p = w.make()
     g = Gemm(dev)
+    opts = {}
+    for kv in args.opt:
+        name, _, value = kv.partition("=")
+        opts[name.upper()] = int(value)
+        g.set_option(getattr(B, "GEMM_OPT_" + name.upper()), int(value))
     tdt = {inputs.F16: torch.float16, inputs.F32: torch.float32}
     in_t, out_t = tdt[p.in_dtype], tdt[p.out_dtype]
     esz_in = 2 if p.in_dtype == inputs.F16 else 4
@@ -457,6 +465,8 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         hs = [g, Gemm(dev)]
+        for name, value in opts.items():
+            hs[1].set_option(getattr(B, "GEMM_OPT_" + name), value)
         ss = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
         hCs = [torch.empty((p.M, p.N), dtype=out_t).pin_memory() for _ in range(2)]
 
@@ -516,6 +526,7 @@ def run_ours(args):
                      % (copies, (copies * step_bytes) >> 20),
                 "plan": {k: plan[k] for k in ("kernel", "swap_ab", "tile_m", "tile_n", "tile_k",
                                               "stages", "grid", "dp_tiles", "sk_tiles")},
+                **({"options": opts} if opts else {}),
             },
             "clocks": clocks,
             "e2e": e2e,

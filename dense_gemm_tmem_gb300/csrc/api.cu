@@ -386,11 +386,18 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
       // share an SM, they start beside this launch's and have their setup and
       // first loads done when it ends.  The split's own k-range needs few
       // stages.  (Parked partials need the ring to hold the partial tile.)
+      // The short ring must still keep enough loads in flight for the
+      // split's own streaming: measured, 5 stages of 18 KiB (16-wide tiles,
+      // skinny M = 16: 9.86 -> 9.35 us) help, 3 of 24 KiB (64-wide, M = 64:
+      // 10.84 -> 12.79 us) do not.  Tiles wider than 64 park their partial
+      // in the ring: it must hold it.
       const int lean = o.lean_stages[width_index(bn)][swap ? 1 : 0];
-      if (lean > 0 && T * cs > G / 2) p->stages = std::min(p->stages, lean);
+      const int64_t lean_inflight = int64_t(lean) * (kBM + bn) * kBK * 2;
+      if (lean >= tc_min_stages(bn, int(cs)) && lean_inflight >= kLeanMinInflight &&
+          T * cs > G / 2)
+        p->stages = std::min(p->stages, lean);
       if (o.stages > 0) p->stages = std::min(o.stages, tc_stages_for(bn));
-      // Tiles wider than 64 park their partial in the ring: it must hold it.
-      p->stages = std::max(p->stages, tc_min_stages(bn, cs));
+      p->stages = std::max(p->stages, tc_min_stages(bn, int(cs)));
       p->grid = int32_t(T * cs);
       p->tiles_m = int32_t(tiles_m);
       p->tiles_n = int32_t(tiles_n);

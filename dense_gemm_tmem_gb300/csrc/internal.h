@@ -86,8 +86,10 @@ int tc_smem_bytes_for(int bn);
 // Fewest ring stages a launch of tile width bn with a cluster split of
 // csplit may use (a tile wider than 64 parks its fp32 partial in the ring).
 int tc_min_stages(int bn, int csplit);
-// Fewest stages a launch that shares its SM with the next launch may use.
+// Fewest stages, and fewest bytes of loads in flight, a launch that shares
+// its SMs with the next launch's CTAs may keep.
 constexpr int kLeanMinStages = 3;
+constexpr int64_t kLeanMinInflight = 88 * 1024;
 // The most ring stages with which two CTAs of the one-SM kernel of tile width
 // bn (either output type) fit on one SM, or 0: the per-file queries and the
 // dispatcher over them.

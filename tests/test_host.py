@@ -45,7 +45,7 @@ def test_no_library_gemm_or_cuda_driver_link(lib):
     assert "libcuda.so" not in deps and "libcublas" not in deps
 
 
-@pytest.mark.parametrize("src", ["simt.cu", "tc2.cu", "tc_n256.cu", "tc_small.cu"])
+@pytest.mark.parametrize("src", ["simt.cu", "tc2.cu", "tc_n256.cu", "tc_n128.cu", "tc_small.cu", "tc_narrow.cu"])
 def test_kernels_keep_registers_without_spills(src):
     """The hot kernels fit their registers: ptxas reports no spill stores (the
     128 x 128 CUDA-core kernel sits at the 128-register cap of 2 CTAs per SM,
