@@ -27,7 +27,7 @@ GEMM_ROW_MAJOR, GEMM_COL_MAJOR = 0, 1
 (GEMM_OPT_FORCE_KERNEL, GEMM_OPT_FORCE_TILE_N, GEMM_OPT_FORCE_GRID, GEMM_OPT_WAIT_LIMIT_NS,
  GEMM_OPT_MIN_SPLIT_ITERS, GEMM_OPT_FORCE_SWAP_AB, GEMM_OPT_GROUP_M, GEMM_OPT_PAIR,
  GEMM_OPT_CLUSTER_SPLIT, GEMM_OPT_PDL, GEMM_OPT_PAIR_SPLIT, GEMM_OPT_TMA_STORE,
- GEMM_OPT_BIAS_INIT, GEMM_OPT_DYNAMIC_TILES, GEMM_OPT_STAGES) = range(15)
+ GEMM_OPT_BIAS_INIT, GEMM_OPT_DYNAMIC_TILES, GEMM_OPT_STAGES, GEMM_OPT_TILE_M) = range(16)
 
 
 class gemm_layout_t(ctypes.Structure):

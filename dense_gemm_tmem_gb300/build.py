@@ -16,9 +16,9 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libdgemm_gb300.so")
 SOURCES = ["api.cu", "simt.cu", "simt_f16.cu", "selftest.cu", "noalloc.cu", "tc2.cu",
-           "tc_n256.cu", "tc_n128.cu", "tc_small.cu", "tc_narrow.cu"]
-HEADERS = ["ptx.cuh", "work.cuh", "tc_kernel.cuh", "tc2_kernel.cuh", "tc_launch.cuh",
-           "simt_kernel.cuh", "internal.h"]
+           "tc_n256.cu", "tc_n128.cu", "tc_small.cu", "tc_narrow.cu", "tc64.cu"]
+HEADERS = ["ptx.cuh", "work.cuh", "tc_kernel.cuh", "tc2_kernel.cuh", "tc64_kernel.cuh",
+           "tc_launch.cuh", "simt_kernel.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                      "-I", os.path.join(ROOT, "include")]

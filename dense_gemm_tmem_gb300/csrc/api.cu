@@ -308,6 +308,7 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
                           : (bn == 32 || bn == 64 || bn == 128 || bn == 256);
   if (!bn_ok || (b_mn && bn % 64 != 0)) return GEMM_ERR_UNSUPPORTED;
 
+
   const int64_t tiles_m = ceil_div(Mm, kBM);
   int64_t tiles_n = ceil_div(Nm, bn);
   int64_t T = tiles_m * tiles_n;
@@ -317,6 +318,49 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
   const int64_t G = num_sms;
   int64_t dp = 0, sk = 0, grid = 0;
   const int64_t max_grid = o.force_grid > 0 ? std::min<int64_t>(o.force_grid, G) : G;
+
+  // 64-row tiles for a small, shallow product taken as whole tiles: twice the
+  // CTAs of 128-row tiles, each bringing in half the A rows and writing half
+  // the output (a small single-wave launch is bound by what each SM moves).
+  {
+    const bool shape_ok = !swap && (bn == 32 || bn == 64 || bn == 128);
+    const int64_t t64 = ceil_div(Mm, 64) * ceil_div(Nm, bn);
+    const bool use64 = shape_ok && (o.tile_m == 64 || (o.tile_m < 0 && narrow && t64 <= G));
+    if (o.tile_m == 64 &&
+        (!use64 || (o.force_kernel >= 0 && o.force_kernel != GEMM_KERNEL_TC)))
+      return GEMM_ERR_UNSUPPORTED;
+    if (use64) {
+      // Narrower still while the tiles fill under half the SMs (K-major B:
+      // an MN-major B box is 64 wide).  Measured, graph replay, cold inputs:
+      // one 128 x 128 output with K = 64, 8 tiles 32 wide 2.20 us against 4
+      // tiles 64 wide 2.39; 512^3, 128 tiles 32 wide 5.03 against 64 tiles
+      // 64 wide 4.96.
+      if (o.force_tile_n <= 0 && o.tile_m < 0 && bn == 64 && !b_mn &&
+          ceil_div(Mm, 64) * ceil_div(Nm, 32) < G / 2)
+        bn = 32;
+      const int64_t t64b = ceil_div(Mm, 64) * ceil_div(Nm, bn);
+      const int64_t I64 = ceil_div(K, kBK);
+      if (t64b > INT32_MAX / 2 || I64 > INT32_MAX / 2) return GEMM_ERR_UNSUPPORTED;
+      const int full = tc64_stages_for(bn);
+      p->kernel = GEMM_KERNEL_TC;
+      p->swap_ab = 0;
+      p->tile_m = 64;
+      p->tile_n = bn;
+      p->tile_k = kBK;
+      p->stages = o.stages > 0 ? std::min(o.stages, full) : full;
+      p->grid = int32_t(std::min(max_grid, t64b));
+      p->tiles_m = int32_t(ceil_div(Mm, 64));
+      p->tiles_n = int32_t(ceil_div(Nm, bn));
+      p->k_iters = int32_t(I64);
+      p->dp_tiles = int32_t(t64b);
+      p->sk_tiles = 0;
+      p->a_mn_major = a_mn;
+      p->b_mn_major = b_mn;
+      p->group_m = o.group_m > 0 ? o.group_m : 2048 / 64;
+      p->workspace_bytes = 0;
+      return GEMM_OK;
+    }
+  }
 
   // Cluster split: when the tiles fill few SMs, each tile's k-blocks are split
   // over a cluster of s CTAs (8, 4 or 2, whose clusters all fit at once and
@@ -639,6 +683,7 @@ void log_plan(const gemm_plan_t& p, int64_t M, int64_t N, int64_t K) {
 
 cudaError_t launch_tc(const TcLaunch& L) {
   if (L.pair) return launch_tc2(L);
+  if (L.bm == 64) return launch_tc64(L);
   if (L.bn == 256) return launch_tc_n256(L);
   if (L.bn == 128) return launch_tc_n128(L);
   if (!L.trans) return launch_tc_narrow(L);
@@ -890,6 +935,10 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value) {
     case GEMM_OPT_STAGES:
       o.stages = value <= 0 ? d.stages : int(std::min<int64_t>(value, 64));
       return GEMM_OK;
+    case GEMM_OPT_TILE_M:
+      if (value >= 0 && value != 64 && value != 128) return GEMM_ERR_INVALID_ARG;
+      o.tile_m = value < 0 ? d.tile_m : int(value);
+      return GEMM_OK;
     default:
       return GEMM_ERR_INVALID_ARG;
   }
@@ -959,6 +1008,7 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, co
 
   const bool pair = plan.kernel == GEMM_KERNEL_TC2;
   dg::TcLaunch L;
+  L.bm = pair ? dg::kPairBM : plan.tile_m;
   L.bn = plan.tile_n;
   L.out_f16 = layout.out_dtype == GEMM_F16;
   L.trans = swap;
@@ -966,8 +1016,9 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, co
   L.pdl = h->opt.pdl != 0;
   L.grid = plan.grid;
   L.stream = stream;
-  // each CTA loads 128 rows of A; a pair CTA loads half of the 256-column B tile
-  rc = dg::encode_operand(h, &L.tmA, opA, Mm, K, plan.a_mn_major, dg::kBM);
+  // each CTA loads 128 (or 64) rows of A; a pair CTA loads half of the
+  // 256-column B tile
+  rc = dg::encode_operand(h, &L.tmA, opA, Mm, K, plan.a_mn_major, pair ? dg::kBM : plan.tile_m);
   if (rc != GEMM_OK) return rc;
   rc = dg::encode_operand(h, &L.tmB, opB, Nm, K, plan.b_mn_major,
                           pair ? dg::kHalfBN : plan.tile_n);
@@ -997,7 +1048,7 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, co
       (h->opt.tma_store < 0 &&
        (layout.out_dtype == GEMM_F16 ||
         out_tiles * (plan.kernel == GEMM_KERNEL_TC2 ? 2 : 1) > plan.grid));
-  a.c_tma = (tma_wanted && !swap && plan.tile_n >= 32 &&
+  a.c_tma = (tma_wanted && !swap && plan.tile_n >= 32 && (pair || plan.tile_m == dg::kBM) &&
              plan.kernel != GEMM_KERNEL_SPLITC &&
              dg::encode_output(h, &L.tmC, C, M, N, layout.out_dtype == GEMM_F16))
                 ? 1
@@ -1015,7 +1066,7 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, co
   a.stages = pair ? 0 : plan.stages;
   // phase stamps only if the caller's buffer holds one row per CTA
   a.trace = (h->trace && h->trace_ctas >= plan.grid) ? h->trace : nullptr;
-  a.idesc = dg::make_idesc_f16(pair ? dg::kPairBM : dg::kBM, plan.tile_n, plan.a_mn_major,
+  a.idesc = dg::make_idesc_f16(pair ? dg::kPairBM : plan.tile_m, plan.tile_n, plan.a_mn_major,
                                plan.b_mn_major);
   return dg::on_device(h->device, [&]() -> int {
     return dg::launch_tc(L) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;

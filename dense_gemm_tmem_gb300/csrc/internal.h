@@ -30,6 +30,7 @@ struct Options {
   int bias_init = 0;       // seed the accumulators with the bias
   int dyn_sched = 1;       // two-SM kernel, whole tiles: tiles handed out at run time
   int stages = -1;         // one-SM kernel ring stages: -1 picker, n >= 1 forced
+  int tile_m = -1;         // one-SM kernel tile rows: -1 picker, 64 or 128 forced
   // per tile width (16, 32, 64, 128, 256 -> 0..4) and operand order: the most
   // stages that let two CTAs share an SM (0: none); set per device
   int lean_stages[5][2] = {{0, 0}, {0, 0}, {0, 0}, {0, 0}, {0, 0}};
@@ -54,6 +55,7 @@ EncodeTiledFn encode_fn();
 
 // One tensor-core launch, fully described.
 struct TcLaunch {
+  int bm = 128;       // MMA M tile of the one-SM kernels: 128, or 64 (tc64.cu)
   int bn;             // MMA N tile: 16, 32, 64, 128 or 256
   bool out_f16;
   bool trans;         // swapped operands, transposed store
@@ -77,6 +79,9 @@ cudaError_t launch_tc_small(const TcLaunch& L);
 cudaError_t launch_tc_narrow(const TcLaunch& L);
 // Two-SM kernel (tc2.cu): even grid, not swapped, whole 256 x 256 tiles.
 cudaError_t launch_tc2(const TcLaunch& L);
+// One-SM kernel with 64-row tiles (tc64.cu): not swapped, whole tiles.
+cudaError_t launch_tc64(const TcLaunch& L);
+int tc64_stages_for(int bn);
 // Clusters of two that fit on the device at once (-1 if the query fails).
 int tc2_max_active_clusters(bool out_f16);
 // Clusters of s one-SM CTAs (cluster split) that fit at once (-1 on failure).

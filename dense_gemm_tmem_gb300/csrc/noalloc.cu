@@ -176,13 +176,14 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
   const int64_t Nm = swap ? M : N;
   const bool pair = plan.kernel == GEMM_KERNEL_TC2;  // whole tiles: no scratch but status
   TcLaunch L;
+  L.bm = pair ? kPairBM : plan.tile_m;
   L.bn = plan.tile_n;
   L.out_f16 = layout.out_dtype == GEMM_F16;
   L.trans = swap;
   L.pair = pair;
   L.grid = plan.grid;
   L.stream = stream;
-  rc = encode_operand_na(&L.tmA, swap ? B : A, Mm, K, plan.a_mn_major, kBM);
+  rc = encode_operand_na(&L.tmA, swap ? B : A, Mm, K, plan.a_mn_major, pair ? kBM : plan.tile_m);
   if (rc != GEMM_OK) return rc;
   rc = encode_operand_na(&L.tmB, swap ? A : B, Nm, K, plan.b_mn_major,
                          pair ? kHalfBN : plan.tile_n);
@@ -200,7 +201,8 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
   a.wait_limit_ns = opt.wait_limit_ns;
   a.a_mn = plan.a_mn_major;
   a.b_mn = plan.b_mn_major;
-  a.idesc = make_idesc_f16(pair ? kPairBM : kBM, plan.tile_n, plan.a_mn_major, plan.b_mn_major);
+  a.idesc = make_idesc_f16(pair ? kPairBM : plan.tile_m, plan.tile_n, plan.a_mn_major,
+                           plan.b_mn_major);
   a.trace = nullptr;
   std::memset(&L.tmC, 0, sizeof(L.tmC));
   a.c_tma = 0;  // plain stores: no output tensor map to encode and keep

@@ -273,7 +273,7 @@ __device__ __forceinline__ void put4(const TcArgs& a, int64_t off, float4 v, int
 // sw (rows of CW + 4 floats: conflict-free 16-byte accesses) and come back out
 // as runs of CW consecutive columns, 32 / (CW / 4) rows per instruction.  The
 // bias is added in fp32 before the single rounding, as in every other store.
-template <int CW, bool OUT_F16>
+template <int CW, bool OUT_F16, int kRows = 32>
 __device__ __forceinline__ void store_rows_staged(const TcArgs& a, float* sw, int32_t mrow0,
                                                   int lane, int32_t nn0, const float (&v)[CW]) {
   if (mrow0 >= a.Mm || nn0 >= a.Nm) return;  // the same for the whole warp
@@ -301,7 +301,7 @@ __device__ __forceinline__ void store_rows_staged(const TcArgs& a, float* sw, in
   // generic C pointer could alias the staging block as far as the compiler
   // knows, so interleaving them would serialise every read behind the store
   // before it.
-  constexpr int kPasses = 32 / RPI;
+  constexpr int kPasses = kRows / RPI;  // only the first kRows rows of the block are real
   float4 x[kPasses];
 #pragma unroll
   for (int it = 0; it < kPasses; ++it)
@@ -321,13 +321,14 @@ __device__ __forceinline__ void store_rows_staged(const TcArgs& a, float* sw, in
 // the bounds and alignment are settled once per chunk and the row pointer
 // advances by a fixed step, so the stores of all passes issue back to back
 // instead of one guarded store after another.
-template <int CW, bool OUT_F16>
+template <int CW, bool OUT_F16, int kRows = 32>
 __device__ __forceinline__ void store_rows_vec(const TcArgs& a, float* sw, int32_t mrow0,
                                                int lane, int32_t nn0, const float (&v)[CW]) {
   constexpr int LD = CW + 4;
   constexpr int Q = CW / 4;    // float4 per row
   constexpr int RPI = 32 / Q;  // rows per pass
-  constexpr int kPasses = 32 / RPI;
+  constexpr int kPasses = kRows / RPI;  // only the first kRows rows of the block are real
+  static_assert(kPasses >= 1 && kRows % RPI == 0, "rows per pass");
   __syncwarp();                // the previous chunk's reads of sw are done
   float4* mine = reinterpret_cast<float4*>(sw + lane * LD);
 #pragma unroll

@@ -81,7 +81,7 @@ enum {
 typedef struct {
   int32_t kernel;      /* GEMM_KERNEL_* */
   int32_t swap_ab;     /* 1: operands swapped (skinny M), C written transposed */
-  int32_t tile_m;      /* CTA tile rows (MMA view) */
+  int32_t tile_m;      /* CTA tile rows (MMA view): 256 (CTA pairs), 128, or 64 */
   int32_t tile_n;      /* CTA tile columns (MMA view) */
   int32_t tile_k;      /* k-block depth per pipeline stage */
   int32_t stages;      /* shared-memory pipeline stages */
@@ -137,12 +137,17 @@ enum {
                                     static schedule gemm_work_units reports (pair c takes
                                     tiles c, c + pairs, ...).  The split tail and the bias
                                     seeding always use the static schedule. */
-  GEMM_OPT_STAGES = 14           /* one-SM tensor-core kernel: shared-memory ring stages.
+  GEMM_OPT_STAGES = 14,          /* one-SM tensor-core kernel: shared-memory ring stages.
                                     -1 (default) the picker's: all the ring holds, or, for a
                                     cluster split over more than half the SMs, as many as
                                     let two CTAs share an SM (so the next launch's CTAs
                                     start beside this one's); n >= 1 forced (at most the
                                     ring's size) */
+  GEMM_OPT_TILE_M = 15           /* one-SM tensor-core kernel: rows per tile.  -1 (default)
+                                    the picker's: 64 for a small, shallow product taken as
+                                    whole tiles when 64-row tiles still fit one wave, else
+                                    128; 64 or 128 forced (64: whole tiles, operands not
+                                    swapped, tile width 32, 64 or 128) */
 };
 
 /* Creates a handle on CUDA device `device`.  Allocates, on that device, the

@@ -169,6 +169,48 @@ def test_swapped_tile_widths(g, dev, tile_n, kernel):
     full_check(g, dev, p)
 
 
+@pytest.mark.parametrize("am,bm", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("odt", [F16, F32])
+@pytest.mark.parametrize("bias", [False, True])
+def test_tile64_layouts_ragged(g, dev, am, bm, odt, bias):
+    """64-row tiles (the M = 64 MMA: 16 rows per TMEM lane quarter) on 296 x
+    520 x 200: 5 tile rows (the last 40 high), 9 tile columns (the last 8
+    wide), 4 k-blocks (the last 8 deep), every layout, bias and output type."""
+    set_opts(g, tile_m=64)
+    p = problem(296, 520, 200, am, bm, F16, odt, bias, 300 + 2 * am + bm)
+    pl = g.plan(296, 520, 200, am, bm, B.GEMM_F16, B.GEMM_F16 if odt == F16 else B.GEMM_F32)
+    assert (pl["tile_m"], pl["kernel"]) == (64, TC)
+    full_check(g, dev, p)
+
+
+@pytest.mark.parametrize("tile_n,bm", [(32, 1), (64, 0), (128, 0), (128, 1)])
+@pytest.mark.parametrize("grid,stages", [(-1, -1), (5, 3)])
+def test_tile64_widths_rings_and_waves(g, dev, tile_n, bm, grid, stages):
+    """64-row tiles of every width on 200 x 296 x 2000 (32 k-blocks, more than
+    the ring holds), once one tile per CTA and once 5 CTAs walking all tiles
+    with a 3-stage ring (both accumulators and every ring phase wrap around)."""
+    set_opts(g, tile_m=64, tile_n=tile_n, grid=grid, stages=stages)
+    p = problem(200, 296, 2000, 0, bm, F16, F32, True, 310 + tile_n + grid)
+    pl = g.plan(200, 296, 2000, 0, bm)
+    assert (pl["kernel"], pl["tile_m"], pl["tile_n"]) == (TC, 64, tile_n)
+    if grid > 0:
+        assert pl["grid"] == grid and pl["stages"] == stages
+    full_check(g, dev, p)
+
+
+def test_tile64_unaligned_output(g, dev):
+    """64-row tiles writing a C whose rows are not 16-byte aligned (the
+    element-wise store path)."""
+    set_opts(g, tile_m=64)
+    p = problem(130, 70, 136, 0, 1, F16, F32, True, 320)
+    A, Bt, bias = to_dev(p, dev)
+    big = torch.empty(p.M * p.N + 1, dtype=torch.float32, device=dev)
+    C = big[1:].view(p.M, p.N)
+    g.run(A, Bt, C, bias, 0, 1)
+    g.status()
+    check(as_f64(C), oracle.gemm(p.A, p.B, p.bias, b_major=1), p)
+
+
 @pytest.mark.parametrize("kernel,tile_n,stages,want", [
     (TC, -1, 1, 1), (TC, -1, 2, 2), (SK, -1, 3, 3),
     (SPLITC, 64, 1, 1),     # partials pushed into the staging area: any ring

@@ -132,13 +132,21 @@ def test_picker_pair_rule():
 
 
 def test_picker_small_shapes():
-    # 512^3: 8 k-blocks per tile is shallow -> 32 whole tiles 64 columns wide
+    # 512^3: 8 k-blocks per tile is shallow -> whole tiles 64 columns wide, and
+    # 64 rows high while those still fit one wave: 64 CTAs instead of 32
     rc, p = plan(512, 512, 512)
     assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC
-    assert (p.tile_n, p.tiles_m, p.tiles_n, p.k_iters) == (64, 4, 8, 8)
-    assert (p.grid, p.dp_tiles, p.sk_tiles, p.workspace_bytes) == (32, 32, 0, 0)
+    assert (p.tile_m, p.tile_n, p.tiles_m, p.tiles_n, p.k_iters) == (64, 64, 8, 8, 8)
+    assert (p.grid, p.dp_tiles, p.sk_tiles, p.workspace_bytes) == (64, 64, 0, 0)
+    # one 128 x 128 output, K-major B: 64 x 32 tiles while they fill under
+    # half the SMs (row-major B keeps 64: its boxes are 64 columns wide)
+    rc, p = plan(128, 128, 64, bm=1)
+    assert (p.kernel, p.tile_m, p.tile_n, p.grid) == (B.GEMM_KERNEL_TC, 64, 32, 8)
+    rc, p = plan(128, 128, 64)
+    assert (p.tile_m, p.tile_n, p.grid) == (64, 64, 4)
+    # 64-row tiles would not fit one wave: 128-row tiles
     rc, p = plan(1024, 1024, 768)  # 12 k-blocks: still narrow whole tiles
-    assert (p.kernel, p.tile_n, p.grid) == (B.GEMM_KERNEL_TC, 64, 128)
+    assert (p.kernel, p.tile_m, p.tile_n, p.grid) == (B.GEMM_KERNEL_TC, 128, 64, 128)
     # 16 k-blocks: 32 tiles 64 columns wide in clusters of 4 (4 k-blocks each)
     # cost less per CTA than 16 tiles of 128 in clusters of 8: fewer operand
     # bytes (192 x 4 vs 256 x 2 rows of k-blocks) and far fewer partial bytes
