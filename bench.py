@@ -2,7 +2,8 @@
 """Benchmark: GEMM TFLOP/s on one GB300 (and N replicas under torchrun).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME]
+                    [--workload NAME | --workload MxNxK[:AB[:IO[:bias]]]]
+                    [--opt NAME=VALUE ...]
 
 A step is one C = A·B (+bias) through the library on resident device inputs.
 Default workload: M = N = K = 8192, fp16 row-major A, column-major B, fp32 bias,
@@ -39,7 +40,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    help="a named workload of dense_gemm_tmem_gb300/inputs.py, or a shape "
+                         "MxNxK[:AB[:IO[:bias]]] (A/B r|c for row/column-major, I/O h|f "
+                         "for fp16/fp32; default rc and hh), e.g. 2048x2048x2048:rc:hh")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--eager", action="store_true",
@@ -274,7 +278,7 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    w = inputs.WORKLOADS[args.workload]
+    w = inputs.workload(args.workload)
     p = w.make()
     threads = oracle.host_threads()
     rng = np.random.default_rng(11)
@@ -332,7 +336,7 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    w = inputs.WORKLOADS[args.workload]
+    w = inputs.workload(args.workload)
     p = w.make()
     g = Gemm(dev)
     opts = {}

@@ -147,3 +147,40 @@ WORKLOADS = {
                  "a 128 x 128 output with K=64 (one k-block): the fixed cost of a launch"),
     ]
 }
+
+
+def shape_workload(spec: str) -> Workload:
+    """A workload named by its shape: ``MxNxK[:AB[:IO[:bias]]]`` with A and B
+    each ``r`` (row-major) or ``c`` (column-major), I and O each ``h`` (fp16)
+    or ``f`` (fp32); the defaults are ``rc`` and ``hh``.  Inputs are U[-1,1]
+    (bias included) from the seeds of base 7.  ``4096x4096x1024:rc:hf`` is
+    row-major A, column-major B, fp16 in, fp32 out, no bias."""
+    parts = spec.split(":")
+    try:
+        M, N, K = (int(x) for x in parts[0].lower().split("x"))
+    except ValueError:
+        raise ValueError("workload %r: neither a named workload nor MxNxK" % spec) from None
+    lay = parts[1] if len(parts) > 1 else "rc"
+    io = parts[2] if len(parts) > 2 else "hh"
+    bias = len(parts) > 3 and parts[3] == "bias"
+    if (len(lay) != 2 or any(c not in "rc" for c in lay) or len(io) != 2
+            or any(c not in "hf" for c in io) or len(parts) > 4
+            or (len(parts) == 4 and not bias) or min(M, N, K) < 0):
+        raise ValueError("shape %r: want MxNxK[:AB[:IO[:bias]]], A/B in r|c, I/O in h|f"
+                         % spec)
+    maj = {"r": ROW, "c": COL}
+    dt = {"h": F16, "f": F32}
+    name = "shape_%dx%dx%d_%s_%s%s" % (M, N, K, lay, io, "_bias" if bias else "")
+    desc = "M=%d N=%d K=%d, %s A, %s B, %s in, %s out%s, U[-1,1]" % (
+        M, N, K, "row-major" if lay[0] == "r" else "column-major",
+        "row-major" if lay[1] == "r" else "column-major", dt[io[0]], dt[io[1]],
+        ", fp32 bias" if bias else "")
+    return Workload(name, M, N, K, maj[lay[0]], maj[lay[1]], dt[io[0]], dt[io[1]],
+                    "uniform", bias, 7, desc)
+
+
+def workload(name: str) -> Workload:
+    """A named workload of ``WORKLOADS``, or a shape spec (``shape_workload``)."""
+    if name in WORKLOADS:
+        return WORKLOADS[name]
+    return shape_workload(name)

@@ -336,3 +336,20 @@ def test_alloc_failure_injection_arguments():
     assert B.gemm_inject_alloc_failure(-1) == B.GEMM_ERR_INVALID_ARG
     assert B.gemm_inject_alloc_failure(3) == B.GEMM_OK
     assert B.gemm_inject_alloc_failure(0) == B.GEMM_OK
+
+
+def test_shape_workload_spec():
+    from dense_gemm_tmem_gb300 import inputs
+    w = inputs.workload("1x4096x4096:rr:hf")
+    assert (w.M, w.N, w.K, w.a_major, w.b_major) == (1, 4096, 4096, 0, 0)
+    assert (w.in_dtype, w.out_dtype, w.bias) == (inputs.F16, inputs.F32, False)
+    w = inputs.workload("300x200x100:cr:ff:bias")
+    assert (w.a_major, w.b_major, w.in_dtype, w.out_dtype, w.bias) == (1, 0, "f32", "f32", True)
+    p = w.make()
+    assert p.A.shape == (100, 300) and p.B.shape == (100, 200) and p.bias.shape == (200,)
+    w = inputs.workload("64x64x64")
+    assert (w.a_major, w.b_major, w.in_dtype, w.out_dtype) == (0, 1, "f16", "f16")
+    assert inputs.workload("gemm512_f16_f32out") is inputs.WORKLOADS["gemm512_f16_f32out"]
+    for bad in ("abc", "1x2", "1x2x3:rx", "1x2x3:rr:hq", "1x2x3:rr:hh:foo", "-1x2x3"):
+        with pytest.raises(ValueError):
+            inputs.workload(bad)
