@@ -39,7 +39,10 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--impl", choices=["ours", "reference", "cublas"], default="ours",
+                    help="ours: this library; reference: the CPU oracle on a bounded sample; "
+                         "cublas: torch.mm/addmm (cuBLAS) on the same operands and protocol, "
+                         "for context only (the library never calls it)")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     help="a named workload of dense_gemm_tmem_gb300/inputs.py, or a shape "
                          "MxNxK[:AB[:IO[:bias]]] (A/B r|c for row/column-major, I/O h|f "
@@ -269,6 +272,32 @@ def host_link(dev, hA, hB, hbias, hC, dev_set, step_flops, per_launch_s, reps=3)
                            "previous step's kernel (or the kernel, if slower)"}
 
 
+# --------------------------------------------------------------- cuBLAS arm --
+def cublas_step(p, sets):
+    """One step of the context arm: cuBLAS (through torch) on one set of the
+    same device operands.  fp32 inputs run with TF32 off; a bias is added in
+    the output type.  fp16 inputs with an fp32 output are computed with an
+    fp16 output instead (its own buffer), which writes half the bytes."""
+    import torch
+    torch.backends.cuda.matmul.allow_tf32 = False
+    copies = len(sets)
+    in_t = sets[0][0].dtype
+    outs = [C if C.dtype == in_t else torch.empty(C.shape, dtype=in_t, device=C.device)
+            for _, _, _, C in sets]
+    biases = [None if b is None else b.to(in_t) for _, _, b, _ in sets]
+
+    def step(i, s):
+        A, Bd, _, _ = sets[i % copies]
+        Aop = A if p.a_major == 0 else A.t()
+        Bop = Bd if p.b_major == 0 else Bd.t()
+        with torch.cuda.stream(s):
+            if biases[i % copies] is not None:
+                torch.addmm(biases[i % copies], Aop, Bop, out=outs[i % copies])
+            else:
+                torch.mm(Aop, Bop, out=outs[i % copies])
+    return step
+
+
 # ------------------------------------------------------------ reference arm --
 def run_reference(args):
     import numpy as np
@@ -338,9 +367,10 @@ def run_ours(args):
 
     w = inputs.workload(args.workload)
     p = w.make()
-    g = Gemm(dev)
+    cublas = args.impl == "cublas"
+    g = None if cublas else Gemm(dev)
     opts = {}
-    for kv in args.opt:
+    for kv in ([] if cublas else args.opt):
         name, _, value = kv.partition("=")
         opts[name.upper()] = int(value)
         g.set_option(getattr(B, "GEMM_OPT_" + name.upper()), int(value))
@@ -367,19 +397,28 @@ def run_ours(args):
         C = torch.empty((p.M, p.N), dtype=out_t, device=dev)
         sets.append((A, Bd, bias, C))
     torch.cuda.synchronize(dev)
-    plan = g.plan(p.M, p.N, p.K, p.a_major, p.b_major,
-                  B.GEMM_F16 if p.in_dtype == inputs.F16 else B.GEMM_F32,
-                  B.GEMM_F16 if p.out_dtype == inputs.F16 else B.GEMM_F32)
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = 0 if plan["kernel"] == B.GEMM_KERNEL_NONE else 1
+    if cublas:
+        plan = None
+        launches_per_step = 0  # none of this library's kernels
+        step = cublas_step(p, sets)
+    else:
+        plan = g.plan(p.M, p.N, p.K, p.a_major, p.b_major,
+                      B.GEMM_F16 if p.in_dtype == inputs.F16 else B.GEMM_F32,
+                      B.GEMM_F16 if p.out_dtype == inputs.F16 else B.GEMM_F32)
+        launches_per_step = 0 if plan["kernel"] == B.GEMM_KERNEL_NONE else 1
 
-    def step(i, s):
-        A, Bd, bias, C = sets[i % copies]
-        g.run(A, Bd, C, bias, p.a_major, p.b_major, stream=s)
+        def step(i, s):
+            A, Bd, bias, C = sets[i % copies]
+            g.run(A, Bd, C, bias, p.a_major, p.b_major, stream=s)
+
+    def check():
+        if g is not None:
+            g.status(stream)
 
     for i in range(args.warmup):
         step(i, stream)
-    g.status(stream)
+    check()
 
     def barrier():
         if dist is not None:
@@ -401,7 +440,7 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         graph.replay()  # one untimed replay
         torch.cuda.synchronize(dev)
-        g.status(stream)
+        check()
 
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     sampler = ClockSampler(local)
@@ -418,7 +457,7 @@ def run_ours(args):
             ev[i + 1].record(stream)
     barrier()
     clocks = sampler.stop()
-    g.status(stream)
+    check()
     elapsed_ms = ev[0].elapsed_time(ev[args.steps])
     if graph is not None:
         per_launch_ms = [elapsed_ms / args.steps]  # back-to-back launches inside the replay
@@ -457,7 +496,7 @@ def run_ours(args):
         roof = {"bound": "alu", "achieved": step_flops / avg_launch_s / 1e12, "peak": peak,
                 "unit": "TFLOP/s", "peak_source": "SMs x 128 FP32 lanes x 2 x max SM clock"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    traffic = recorded_traffic(args.workload, plan)
+    traffic = None if cublas else recorded_traffic(args.workload, plan)
     roof["traffic"] = traffic
     roof["algorithmic_bytes"] = step_bytes
 
@@ -467,7 +506,7 @@ def run_ours(args):
     # between two handles on two streams, so step i+1's inputs travel while
     # step i computes and its result comes back.
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not cublas:
         hs = [g, Gemm(dev)]
         for name, value in opts.items():
             hs[1].set_option(getattr(B, "GEMM_OPT_" + name), value)
@@ -505,7 +544,7 @@ def run_ours(args):
         e2e["link"]["frac"] = e2e["value"] / e2e["link"]["bound_tflops"]
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu:
+    if rank == 0 and world == 1 and not args.no_cpu and not cublas:
         import oracle
         cpu = cpu_baseline(p, args.cpu_seconds, oracle.host_threads())
 
@@ -528,8 +567,9 @@ def run_ours(args):
                 "l2": ("inputs exceed L2 (%d MiB per step)" % (step_bytes >> 20)) if copies == 1
                 else "rotating %d input copies (%d MiB) so each step misses L2"
                      % (copies, (copies * step_bytes) >> 20),
-                "plan": {k: plan[k] for k in ("kernel", "swap_ab", "tile_m", "tile_n", "tile_k",
-                                              "stages", "grid", "dp_tiles", "sk_tiles")},
+                **({"plan": {k: plan[k] for k in ("kernel", "swap_ab", "tile_m", "tile_n",
+                                                  "tile_k", "stages", "grid", "dp_tiles",
+                                                  "sk_tiles")}} if plan else {}),
                 **({"options": opts} if opts else {}),
             },
             "clocks": clocks,
@@ -538,8 +578,15 @@ def run_ours(args):
             "roofline": roof,
             "cpu_baseline": cpu,
         }
+        if cublas:
+            line = {"impl": "cublas", **line,
+                    "note": "cuBLAS through torch.mm / torch.addmm on the same operands and "
+                            "protocol, for context only (the library never calls it); a bias is "
+                            "added in the output type; fp16 inputs with fp32 output are "
+                            "computed with fp16 output"}
         print(json.dumps(line), flush=True)
-    g.close()
+    if g is not None:
+        g.close()
     if dist is not None:
         dist.destroy_process_group()
     return 0

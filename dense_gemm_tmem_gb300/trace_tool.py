@@ -35,11 +35,13 @@ def _stat(t, i, k, how):
 
 
 def phases(t: np.ndarray) -> dict:
-    """Median over launches 1.. of each phase in microseconds; t holds
-    (launches, ctas, slots) nanosecond stamps."""
+    """Mean over launches 1.. of each phase in microseconds; t holds
+    (launches, ctas, slots) nanosecond stamps.  A phase's ends are averaged
+    over the CTAs (and the launches), which resolves phases shorter than the
+    timer's tick: the stamps fall at every offset from the ticks."""
     rows = []
     for i in range(1, t.shape[0]):
-        med = lambda k: _stat(t, i, k, np.median)  # noqa: E731
+        med = lambda k: _stat(t, i, k, np.mean)  # noqa: E731
         first_entry = _stat(t, i, ENTRY, np.min)
         rows.append({
             "gap_after_previous_launch": first_entry - _stat(t, i - 1, EXIT, np.max),
@@ -58,14 +60,16 @@ def phases(t: np.ndarray) -> dict:
     for k in rows[0]:
         vals = [r[k] for r in rows if not np.isnan(r[k])]
         if vals:
-            out[k] = round(float(np.median(vals)) / 1e3, 3)
+            out[k] = round(float(np.mean(vals)) / 1e3, 3)
     return out
 
 
-def run(workload: str, launches: int, pdl: int, device: int = 0) -> dict:
+def run(workload: str, launches: int, pdl: int, device: int = 0, opts=None) -> dict:
     dev = torch.device("cuda", device)
     g = Gemm(dev)
-    w = inputs.WORKLOADS[workload]
+    for name, value in (opts or {}).items():
+        g.set_option(getattr(B, "GEMM_OPT_" + name.upper()), int(value))
+    w = inputs.workload(workload)
     p = w.make()
     A = torch.from_numpy(p.A).to(dev)
     Bm = torch.from_numpy(p.B).to(dev)
@@ -101,21 +105,30 @@ def run(workload: str, launches: int, pdl: int, device: int = 0) -> dict:
     g.status()
     t = bufs.cpu().numpy().astype(np.float64)
     res = {"workload": workload, "pdl": pdl, "grid": grid, "kernel": plan["kernel"],
+           "tile": [plan["tile_m"], plan["tile_n"]], "cluster_split": plan["cluster_split"],
            "us_per_launch": round(e0.elapsed_time(e1) * 1e3 / launches, 2),
-           "median_phase_us": phases(t)}
+           "mean_phase_us": phases(t)}
     g.close()
     return res
 
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
-    ap.add_argument("--workload", default="skinny_m16_4096", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--workload", default="skinny_m16_4096",
+                    help="a named workload (dense_gemm_tmem_gb300/inputs.py) or a shape "
+                         "MxNxK[:AB[:IO[:bias]]]")
     ap.add_argument("--launches", type=int, default=20)
     ap.add_argument("--pdl", type=int, default=0, choices=[0, 1],
                     help="programmatic dependent launch (1 overlaps each launch's setup with "
                          "the previous launch, which makes the phases harder to read)")
+    ap.add_argument("--opt", action="append", default=[], metavar="NAME=VALUE",
+                    help="set a library option (a GEMM_OPT_ name of include/gemm.h); repeatable")
     a = ap.parse_args()
-    print(json.dumps(run(a.workload, a.launches, a.pdl)))
+    opts = dict(kv.split("=", 1) for kv in a.opt)
+    res = run(a.workload, a.launches, a.pdl, opts=opts)
+    if opts:
+        res["options"] = opts
+    print(json.dumps(res))
 
 
 if __name__ == "__main__":

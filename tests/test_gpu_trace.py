@@ -85,10 +85,10 @@ def test_trace_tool_timeline(dev):
     """The timeline tool reads back stamps from every launch of a replayed graph."""
     from dense_gemm_tmem_gb300 import trace_tool
     res = trace_tool.run("tile128_f16_f32out", 6, 0)
-    ph = res["median_phase_us"]
+    ph = res["mean_phase_us"]
     assert 1 <= res["grid"] <= 8 and res["us_per_launch"] > 0  # a few whole tiles
     for k in ("entry_to_setup_done", "setup_to_first_load", "main_loop", "epilogue",
               "entry_to_exit"):
         assert 0 <= ph[k] < 1000, (k, ph)
     res = trace_tool.run("skinny_m16_4096", 4, 1)
-    assert res["kernel"] == B.GEMM_KERNEL_SPLITC and "cluster_reduce" in res["median_phase_us"]
+    assert res["kernel"] == B.GEMM_KERNEL_SPLITC and "cluster_reduce" in res["mean_phase_us"]
