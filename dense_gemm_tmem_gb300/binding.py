@@ -27,7 +27,8 @@ GEMM_ROW_MAJOR, GEMM_COL_MAJOR = 0, 1
 (GEMM_OPT_FORCE_KERNEL, GEMM_OPT_FORCE_TILE_N, GEMM_OPT_FORCE_GRID, GEMM_OPT_WAIT_LIMIT_NS,
  GEMM_OPT_MIN_SPLIT_ITERS, GEMM_OPT_FORCE_SWAP_AB, GEMM_OPT_GROUP_M, GEMM_OPT_PAIR,
  GEMM_OPT_CLUSTER_SPLIT, GEMM_OPT_PDL, GEMM_OPT_PAIR_SPLIT, GEMM_OPT_TMA_STORE,
- GEMM_OPT_BIAS_INIT, GEMM_OPT_DYNAMIC_TILES, GEMM_OPT_STAGES, GEMM_OPT_TILE_M) = range(16)
+ GEMM_OPT_BIAS_INIT, GEMM_OPT_DYNAMIC_TILES, GEMM_OPT_STAGES, GEMM_OPT_TILE_M,
+ GEMM_OPT_K_GROUP) = range(17)
 
 
 class gemm_layout_t(ctypes.Structure):
@@ -39,7 +40,8 @@ class gemm_plan_t(ctypes.Structure):
     _fields_ = [(n, c_int32) for n in (
         "kernel", "swap_ab", "tile_m", "tile_n", "tile_k", "stages", "grid", "tiles_m",
         "tiles_n", "k_iters", "dp_tiles", "sk_tiles", "a_mn_major", "b_mn_major", "group_m",
-        "cluster_split")] + [("workspace_bytes", c_int64)]
+        "cluster_split")] + [("workspace_bytes", c_int64), ("k_group", c_int32),
+                             ("reserved", c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

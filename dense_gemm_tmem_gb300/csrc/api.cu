@@ -30,9 +30,10 @@ struct TmapKey {
   int64_t rows, k;
   int mn_major, box_rows;
   int kind;  // 0 fp16 operand, 1 fp32 output, 2 fp16 output
+  int kgroup;  // k-blocks per box (operands)
   bool operator==(const TmapKey& o) const {
     return ptr == o.ptr && rows == o.rows && k == o.k && mn_major == o.mn_major &&
-           box_rows == o.box_rows && kind == o.kind;
+           box_rows == o.box_rows && kind == o.kind && kgroup == o.kgroup;
   }
 };
 
@@ -179,6 +180,7 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
              const Options& o, gemm_plan_t* p) {
   if (!p) return GEMM_ERR_INVALID_ARG;
   std::memset(p, 0, sizeof(*p));
+  p->k_group = 1;
   if (M < 0 || N < 0 || K < 0 || num_sms <= 0) return GEMM_ERR_INVALID_ARG;
   if (L.a_major > 1 || L.b_major > 1 || L.in_dtype > 1 || L.out_dtype > 1)
     return GEMM_ERR_INVALID_ARG;
@@ -342,12 +344,21 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
       const int64_t I64 = ceil_div(K, kBK);
       if (t64b > INT32_MAX / 2 || I64 > INT32_MAX / 2) return GEMM_ERR_UNSUPPORTED;
       const int full = tc64_stages_for(bn);
+      // k-blocks per TMA copy: the unit takes about the same time per copy up
+      // to 32 KiB, so a shallow product loads in a few deep boxes (up to 4
+      // k-blocks: an MN-major box is at most 256 deep).  A K-major operand is
+      // read through a 3-D view of whole k-blocks, so K must be a multiple of 64.
+      int kg = I64 >= 4 ? 4 : I64 >= 2 ? 2 : 1;
+      if (o.k_group > 0) kg = std::min<int64_t>(o.k_group, kg > 1 ? kg : 1);
+      if (K % kBK != 0 && !(a_mn && b_mn)) kg = 1;
+      p->k_group = kg;
       p->kernel = GEMM_KERNEL_TC;
       p->swap_ab = 0;
       p->tile_m = 64;
       p->tile_n = bn;
       p->tile_k = kBK;
       p->stages = o.stages > 0 ? std::min(o.stages, full) : full;
+      p->stages = std::max(kg, p->stages - p->stages % kg);  // whole groups
       p->grid = int32_t(std::min(max_grid, t64b));
       p->tiles_m = int32_t(ceil_div(Mm, 64));
       p->tiles_n = int32_t(ceil_div(Nm, bn));
@@ -569,13 +580,18 @@ struct gemm_ctx {
 namespace dg {
 namespace {
 
-// An fp16 operand with `rows` rows (MMA view) and depth K:
-//   K-major  (K contiguous):      dims {K, rows}, box {64, box_rows}
-//   MN-major (rows contiguous):   dims {rows, K}, box {64, 64}
+// An fp16 operand with `rows` rows (MMA view) and depth K, in boxes of
+// `kgroup` k-blocks:
+//   K-major  (K contiguous):    dims {K, rows}, box {64, box_rows}; for kgroup > 1
+//                               (K a multiple of 64) the 3-D view {64, rows, K / 64}
+//                               (strides K * 2 and 128 bytes), box {64, box_rows, kgroup}
+//   MN-major (rows contiguous): dims {rows, K}, box {64, 64 * kgroup}
 // 128-byte swizzle; out-of-range elements read as zero.
 int encode_operand(gemm_ctx* h, CUtensorMap* out, const void* ptr, int64_t rows, int64_t K,
-                   int mn_major, int box_rows) {
-  const TmapKey key{ptr, rows, K, mn_major, box_rows, 0};
+                   int mn_major, int box_rows, int kgroup = 1) {
+  if (kgroup > 1 && ((!mn_major && K % kBK != 0) || kgroup * kBK > 256))
+    return GEMM_ERR_UNSUPPORTED;
+  const TmapKey key{ptr, rows, K, mn_major, box_rows, 0, kgroup};
   {
     std::lock_guard<std::mutex> g(h->mu);
     for (auto& e : h->cache)
@@ -586,9 +602,20 @@ int encode_operand(gemm_ctx* h, CUtensorMap* out, const void* ptr, int64_t rows,
   }
   EncodeTiledFn fn = encode_fn();
   if (!fn) return GEMM_ERR_CUDA;
-  cuuint64_t dims[2], strides[1];
-  cuuint32_t box[2], estr[2] = {1, 1};
-  if (!mn_major) {
+  cuuint64_t dims[3], strides[2];
+  cuuint32_t box[3], estr[3] = {1, 1, 1};
+  cuuint32_t rank = 2;
+  if (!mn_major && kgroup > 1) {
+    rank = 3;
+    dims[0] = kBK;
+    dims[1] = cuuint64_t(rows);
+    dims[2] = cuuint64_t(K / kBK);
+    strides[0] = cuuint64_t(K) * 2;
+    strides[1] = kBK * 2;
+    box[0] = kBK;
+    box[1] = cuuint32_t(box_rows);
+    box[2] = cuuint32_t(kgroup);
+  } else if (!mn_major) {
     dims[0] = cuuint64_t(K);
     dims[1] = cuuint64_t(rows);
     strides[0] = cuuint64_t(K) * 2;
@@ -599,10 +626,10 @@ int encode_operand(gemm_ctx* h, CUtensorMap* out, const void* ptr, int64_t rows,
     dims[1] = cuuint64_t(K);
     strides[0] = cuuint64_t(rows) * 2;
     box[0] = 64;
-    box[1] = kBK;
+    box[1] = cuuint32_t(kBK * kgroup);
   }
   CUtensorMap map;
-  const CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims,
+  const CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rank, const_cast<void*>(ptr), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -627,7 +654,7 @@ bool encode_output(gemm_ctx* h, CUtensorMap* out, void* C, int64_t M, int64_t N,
   if ((reinterpret_cast<uintptr_t>(C) & 15) || pitch % 16 != 0 || M > kMaxCoord ||
       N > kMaxCoord)
     return false;
-  const TmapKey key{C, M, N, 0, 32, f16 ? 2 : 1};
+  const TmapKey key{C, M, N, 0, 32, f16 ? 2 : 1, 1};
   {
     std::lock_guard<std::mutex> g(h->mu);
     for (auto& e : h->cache)
@@ -939,6 +966,10 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value) {
       if (value >= 0 && value != 64 && value != 128) return GEMM_ERR_INVALID_ARG;
       o.tile_m = value < 0 ? d.tile_m : int(value);
       return GEMM_OK;
+    case GEMM_OPT_K_GROUP:
+      if (value >= 0 && value != 1 && value != 2 && value != 4) return GEMM_ERR_INVALID_ARG;
+      o.k_group = value < 0 ? d.k_group : int(value);
+      return GEMM_OK;
     default:
       return GEMM_ERR_INVALID_ARG;
   }
@@ -1018,10 +1049,12 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, co
   L.stream = stream;
   // each CTA loads 128 (or 64) rows of A; a pair CTA loads half of the
   // 256-column B tile
-  rc = dg::encode_operand(h, &L.tmA, opA, Mm, K, plan.a_mn_major, pair ? dg::kBM : plan.tile_m);
+  const int kgroup = plan.k_group > 1 ? plan.k_group : 1;
+  rc = dg::encode_operand(h, &L.tmA, opA, Mm, K, plan.a_mn_major, pair ? dg::kBM : plan.tile_m,
+                          kgroup);
   if (rc != GEMM_OK) return rc;
   rc = dg::encode_operand(h, &L.tmB, opB, Nm, K, plan.b_mn_major,
-                          pair ? dg::kHalfBN : plan.tile_n);
+                          pair ? dg::kHalfBN : plan.tile_n, kgroup);
   if (rc != GEMM_OK) return rc;
   dg::TcArgs& a = L.args;
   a.work = dg::spec_of(plan);
@@ -1064,6 +1097,7 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, co
   if (pair && plan.sk_tiles == 0 && !a.bias_init && h->opt.dyn_sched != 0)
     a.sched = h->tickets + dg::kTicketCap;
   a.stages = pair ? 0 : plan.stages;
+  a.kgroup = kgroup;
   // phase stamps only if the caller's buffer holds one row per CTA
   a.trace = (h->trace && h->trace_ctas >= plan.grid) ? h->trace : nullptr;
   a.idesc = dg::make_idesc_f16(pair ? dg::kPairBM : plan.tile_m, plan.tile_n, plan.a_mn_major,

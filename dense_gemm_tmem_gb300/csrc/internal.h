@@ -31,6 +31,7 @@ struct Options {
   int dyn_sched = 1;       // two-SM kernel, whole tiles: tiles handed out at run time
   int stages = -1;         // one-SM kernel ring stages: -1 picker, n >= 1 forced
   int tile_m = -1;         // one-SM kernel tile rows: -1 picker, 64 or 128 forced
+  int k_group = -1;        // k-blocks per TMA copy (64-row kernel): -1 picker, 1/2/4 forced
   // per tile width (16, 32, 64, 128, 256 -> 0..4) and operand order: the most
   // stages that let two CTAs share an SM (0: none); set per device
   int lean_stages[5][2] = {{0, 0}, {0, 0}, {0, 0}, {0, 0}, {0, 0}};

@@ -14,8 +14,11 @@ cudaError_t launch_tc64_inst(const TcLaunch& L) {
                                        Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int stages = L.args.stages > 0 ? L.args.stages : Cfg::kStages;
+  const int J = L.args.kgroup;
   if (stages > Cfg::kStages || L.args.work.csplit > 1 || L.args.work.sk_tiles > 0)
     return cudaErrorInvalidValue;  // whole tiles only
+  // whole groups of J k-blocks; an MN-major box is at most 256 k deep
+  if (J < 1 || J > 4 || stages % J != 0) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

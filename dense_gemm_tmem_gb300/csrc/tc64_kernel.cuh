@@ -44,21 +44,29 @@ struct Tc64Config {
   static_assert((2 * kStages + 5) * 8 + 16 <= kBarBytes, "barrier area");
 };
 
+// The ring holds `stages` k-blocks, taken J = args.kgroup at a time: one TMA
+// copy per operand brings J consecutive k-blocks (a 3-D box for a K-major
+// operand, a box J k-blocks deep for an MN-major one), so a small launch
+// issues a few large copies instead of two per k-block (the TMA unit of an SM
+// takes about the same time per copy up to 32 KiB).  Group g of a tile
+// covers k-blocks kb0 + g*J ...; the last group may be short: its box reads
+// zeros (or unused k-blocks) past the tile's range, and its MMAs stop there.
 template <int BN, bool OUT_F16>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc64_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const TcArgs args) {
   using Cfg = Tc64Config<BN>;
-  const int S = args.stages > 0 ? args.stages : Cfg::kStages;
+  const int J = args.kgroup > 1 ? args.kgroup : 1;
+  const int S = (args.stages > 0 ? args.stages : Cfg::kStages) / J;  // ring stages of J blocks
   constexpr int CW = 32;  // TMEM columns per epilogue load
 
   const uint64_t t_entry = args.trace ? globaltimer_ns() : 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;                      // S x 8 KiB
-  uint8_t* sB = smem + S * Cfg::kABytes;   // S x BN*128 B
-  uint8_t* stage = sB + S * Cfg::kBBytes;  // epilogue staging
+  uint8_t* sA = smem;                          // S x J x 8 KiB
+  uint8_t* sB = smem + S * J * Cfg::kABytes;   // S x J x BN*128 B
+  uint8_t* stage = sB + S * J * Cfg::kBBytes;  // epilogue staging
   uint64_t* bars = reinterpret_cast<uint64_t*>(stage + Cfg::kEpiStageBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
@@ -115,7 +123,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       while (ok && it.next(W, u)) {
         int32_t tm, tn;
         tile_coords(W, u.tile, tm, tn);
-        for (int32_t kb = u.kb0; kb < u.kb1; ++kb) {
+        for (int32_t kb = u.kb0; kb < u.kb1; kb += J) {
           if (!wait_bounded(smem_u32(&empty[s]), ph ^ 1, wc, kSiteProducer)) {
             ok = false;
             break;
@@ -129,22 +137,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
           const uint32_t fb = smem_u32(&full[s]);
-          mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
-          const uint32_t a_dst = smem_u32(sA + s * Cfg::kABytes);
-          const uint32_t b_dst = smem_u32(sB + s * Cfg::kBBytes);
+          mbar_arrive_expect_tx(fb, J * Cfg::kStageBytes);  // whole boxes, zero-filled past K
+          const uint32_t a_dst = smem_u32(sA + s * J * Cfg::kABytes);
+          const uint32_t b_dst = smem_u32(sB + s * J * Cfg::kBBytes);
           const int32_t k0 = kb * kBK;
-          // A: 64 rows x 64 k, one box either way round
-          if (!args.a_mn)
-            tma_load_2d(a_dst, &tmA, fb, k0, tm * kBM64);
-          else
+          // A: 64 rows x 64 J k, one box either way round
+          if (args.a_mn)
             tma_load_2d(a_dst, &tmA, fb, tm * kBM64, k0);
+          else if (J > 1)
+            tma_load_3d(a_dst, &tmA, fb, 0, tm * kBM64, kb);
+          else
+            tma_load_2d(a_dst, &tmA, fb, k0, tm * kBM64);
           if (!args.b_mn) {
-            tma_load_2d(b_dst, &tmB, fb, k0, tn * BN);
+            if (J > 1)
+              tma_load_3d(b_dst, &tmB, fb, 0, tn * BN, kb);
+            else
+              tma_load_2d(b_dst, &tmB, fb, k0, tn * BN);
           } else {
             if constexpr (BN >= 64) {
+              // 64-column halves, each J k-blocks deep
 #pragma unroll
               for (int j = 0; j < BN / 64; ++j)
-                tma_load_2d(b_dst + j * 8192, &tmB, fb, tn * BN + 64 * j, k0);
+                tma_load_2d(b_dst + j * J * 8192, &tmB, fb, tn * BN + 64 * j, k0);
             }
           }
           if (first) {
@@ -177,10 +191,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int s = 0, b = 0;
       uint32_t ph = 0, aph = 0;
       bool ok = true, any = false;
+      // an MN-major B's 64-column halves sit J k-blocks apart
       const uint32_t a_lbo = args.a_mn ? 8192u : 16u;
-      const uint32_t b_lbo = args.b_mn ? 8192u : 16u;
+      const uint32_t b_lbo = args.b_mn ? uint32_t(J) * 8192u : 16u;
       const uint32_t a_step = args.a_mn ? (2048u >> 4) : (32u >> 4);
       const uint32_t b_step = args.b_mn ? (2048u >> 4) : (32u >> 4);
+      // k-block j of a group: A blocks are 8 KiB either way round; a K-major B
+      // block holds BN rows, an MN-major one 64 k rows of each half
+      const uint32_t b_blk = args.b_mn ? 8192u : uint32_t(Cfg::kBBytes);
       while (ok && it.next(W, u)) {
         if (!wait_bounded(smem_u32(&acc_empty[b]), aph, wc, kSiteMmaAccum)) {
           ok = false;
@@ -188,19 +206,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(b * BN);
-        for (int32_t kb = u.kb0; kb < u.kb1; ++kb) {
+        for (int32_t kb = u.kb0; kb < u.kb1; kb += J) {
           if (!wait_bounded(smem_u32(&full[s]), ph, wc, kSiteMmaFull)) {
             ok = false;
             break;
           }
           tc_fence_after();
           if (!any) trace_mark(args, blockIdx.x, kTraceFirstData);
-          const uint64_t adesc = make_sdesc_sw128(smem_u32(sA + s * Cfg::kABytes), a_lbo, 1024);
-          const uint64_t bdesc = make_sdesc_sw128(smem_u32(sB + s * Cfg::kBBytes), b_lbo, 1024);
+          const uint32_t a0 = smem_u32(sA + s * J * Cfg::kABytes);
+          const uint32_t b0 = smem_u32(sB + s * J * Cfg::kBBytes);
+          const int nj = u.kb1 - kb < J ? u.kb1 - kb : J;
+#pragma unroll 1
+          for (int j = 0; j < nj; ++j) {
+            const uint64_t adesc = make_sdesc_sw128(a0 + uint32_t(j) * 8192u, a_lbo, 1024);
+            const uint64_t bdesc = make_sdesc_sw128(b0 + uint32_t(j) * b_blk, b_lbo, 1024);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            tc_mma_f16(d_tmem, adesc + uint64_t(kk * a_step), bdesc + uint64_t(kk * b_step),
-                       args.idesc, (kb > u.kb0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              tc_mma_f16(d_tmem, adesc + uint64_t(kk * a_step), bdesc + uint64_t(kk * b_step),
+                         args.idesc, (kb > u.kb0 || j > 0 || kk > 0) ? 1u : 0u);
+          }
           any = true;
           tc_commit(smem_u32(&empty[s]));
           if (++s == S) {

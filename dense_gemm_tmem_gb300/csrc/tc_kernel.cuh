@@ -91,6 +91,9 @@ struct TcArgs {
                           // 16 bytes, so every 4-column group is whole and aligned
   int32_t bias_init = 0;  // 1: each tile's k-block-0 accumulator is seeded with the bias
   int32_t stages = 0;      // ring stages of this launch, 1 ... TcConfig<BN>::kStages (0: all)
+  int32_t kgroup = 1;      // k-blocks per TMA copy (64-row and two-SM kernels): the ring's
+                           // stages are taken kgroup at a time, one copy per operand each;
+                           // > 1 needs the operands' maps encoded for it (3-D for K-major)
   uint32_t idesc;         // tcgen05 instruction descriptor
   uint64_t* trace = nullptr;  // NULL, or kTraceSlots %globaltimer stamps per CTA
   int* sched = nullptr;       // two-SM kernel, whole tiles: NULL for the static schedule,

@@ -84,7 +84,7 @@ typedef struct {
   int32_t tile_m;      /* CTA tile rows (MMA view): 256 (CTA pairs), 128, or 64 */
   int32_t tile_n;      /* CTA tile columns (MMA view) */
   int32_t tile_k;      /* k-block depth per pipeline stage */
-  int32_t stages;      /* shared-memory pipeline stages */
+  int32_t stages;      /* shared-memory pipeline stages (k-blocks the ring holds) */
   int32_t grid;        /* CTAs launched */
   int32_t tiles_m;     /* output tiles along the MMA M side */
   int32_t tiles_n;     /* output tiles along the MMA N side */
@@ -96,6 +96,9 @@ typedef struct {
   int32_t group_m;     /* tile raster: groups of group_m tile rows */
   int32_t cluster_split; /* GEMM_KERNEL_SPLITC: CTAs per tile (2, 4 or 8), else 0 */
   int64_t workspace_bytes; /* fp32 partial-tile bytes the split needs */
+  int32_t k_group;     /* k-blocks each TMA copy brings (the ring is taken k_group
+                          stages at a time); 1 = one copy per operand and k-block */
+  int32_t reserved;    /* 0 */
 } gemm_plan_t;
 
 /* Options for tests and tuning (gemm_set_option).  Values < 0 restore the default. */
@@ -143,11 +146,15 @@ enum {
                                     let two CTAs share an SM (so the next launch's CTAs
                                     start beside this one's); n >= 1 forced (at most the
                                     ring's size) */
-  GEMM_OPT_TILE_M = 15           /* one-SM tensor-core kernel: rows per tile.  -1 (default)
+  GEMM_OPT_TILE_M = 15,          /* one-SM tensor-core kernel: rows per tile.  -1 (default)
                                     the picker's: 64 for a small, shallow product taken as
                                     whole tiles when 64-row tiles still fit one wave, else
                                     128; 64 or 128 forced (64: whole tiles, operands not
                                     swapped, tile width 32, 64 or 128) */
+  GEMM_OPT_K_GROUP = 16          /* k-blocks per TMA copy where the kernel groups them (the
+                                    64-row kernel): -1 (default) the picker's (up to 4 when
+                                    K is a multiple of 64 or both operands are MN-major);
+                                    1, 2 or 4 forced (rounded down to what the shape allows) */
 };
 
 /* Creates a handle on CUDA device `device`.  Allocates, on that device, the

@@ -102,7 +102,8 @@ def set_opts(g, **kw):
              "pair": B.GEMM_OPT_PAIR, "csplit": B.GEMM_OPT_CLUSTER_SPLIT,
              "pair_split": B.GEMM_OPT_PAIR_SPLIT, "tma_store": B.GEMM_OPT_TMA_STORE,
              "bias_init": B.GEMM_OPT_BIAS_INIT, "dyn": B.GEMM_OPT_DYNAMIC_TILES,
-             "stages": B.GEMM_OPT_STAGES, "tile_m": B.GEMM_OPT_TILE_M}
+             "stages": B.GEMM_OPT_STAGES, "tile_m": B.GEMM_OPT_TILE_M,
+             "k_group": B.GEMM_OPT_K_GROUP}
     for k, v in kw.items():
         g.set_option(names[k], v)
 
@@ -112,5 +113,5 @@ def reset_opts(g):
                 B.GEMM_OPT_FORCE_SWAP_AB, B.GEMM_OPT_MIN_SPLIT_ITERS, B.GEMM_OPT_GROUP_M,
                 B.GEMM_OPT_PAIR, B.GEMM_OPT_CLUSTER_SPLIT, B.GEMM_OPT_PAIR_SPLIT,
                 B.GEMM_OPT_TMA_STORE, B.GEMM_OPT_BIAS_INIT, B.GEMM_OPT_DYNAMIC_TILES,
-                B.GEMM_OPT_STAGES, B.GEMM_OPT_TILE_M):
+                B.GEMM_OPT_STAGES, B.GEMM_OPT_TILE_M, B.GEMM_OPT_K_GROUP):
         g.set_option(opt, -1)

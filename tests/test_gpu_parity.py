@@ -198,6 +198,48 @@ def test_tile64_widths_rings_and_waves(g, dev, tile_n, bm, grid, stages):
     full_check(g, dev, p)
 
 
+@pytest.mark.parametrize("am,bm,tile_n", [(0, 0, 64), (0, 1, 32), (1, 0, 128), (1, 1, 64),
+                                          (0, 1, 128)])
+def test_tile64_k_groups(g, dev, am, bm, tile_n):
+    """64-row tiles with 1, 2 and 4 k-blocks per TMA copy (3-D boxes for a
+    K-major operand, deeper boxes for an MN-major one) on 296 x 520 x 320:
+    5 k-blocks, so the last group is short.  Every grouping gives the same
+    bits (the MMAs run in the same k order) and matches the oracle."""
+    p = problem(296, 520, 320, am, bm, F16, F32, True, 330 + 2 * am + bm)
+    ref = oracle.gemm(p.A, p.B, p.bias, a_major=am, b_major=bm)
+    outs = []
+    for kg in (1, 2, 4):
+        set_opts(g, tile_m=64, tile_n=tile_n, k_group=kg)
+        pl = g.plan(296, 520, 320, am, bm)
+        assert (pl["kernel"], pl["tile_m"], pl["tile_n"], pl["k_group"]) == (TC, 64, tile_n, kg)
+        C = run(g, p, dev)
+        check(as_f64(C), ref, p)
+        outs.append(C.cpu())
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+@pytest.mark.parametrize("kg,stages", [(2, 4), (4, 4), (4, 8)])
+def test_tile64_k_groups_ring_wrap(g, dev, kg, stages):
+    """Groups of k-blocks through a short ring: 5 CTAs walk all 20 tiles of
+    200 x 296 x 1024 (16 k-blocks each), so ring phases and accumulators wrap
+    many times."""
+    set_opts(g, tile_m=64, tile_n=64, grid=5, stages=stages, k_group=kg)
+    p = problem(200, 296, 1024, 0, 1, F16, F16, True, 340 + kg + stages)
+    pl = g.plan(200, 296, 1024, 0, 1, B.GEMM_F16, B.GEMM_F16)
+    assert (pl["tile_m"], pl["grid"], pl["stages"], pl["k_group"]) == (64, 5, stages, kg)
+    full_check(g, dev, p)
+
+
+def test_tile64_k_groups_mn_major_ragged_k(g, dev):
+    """Both operands MN-major with K = 200 (not a multiple of 64): 4 k-blocks
+    in one copy per operand, the zeros past K filled by the TMA unit."""
+    set_opts(g, tile_m=64)
+    p = problem(256, 384, 200, 1, 0, F16, F32, False, 350)
+    pl = g.plan(256, 384, 200, 1, 0)
+    assert (pl["tile_m"], pl["k_group"]) == (64, 4)
+    full_check(g, dev, p)
+
+
 def test_tile64_unaligned_output(g, dev):
     """64-row tiles writing a C whose rows are not 16-byte aligned (the
     element-wise store path)."""

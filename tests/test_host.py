@@ -138,6 +138,8 @@ def test_picker_small_shapes():
     assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC
     assert (p.tile_m, p.tile_n, p.tiles_m, p.tiles_n, p.k_iters) == (64, 64, 8, 8, 8)
     assert (p.grid, p.dp_tiles, p.sk_tiles, p.workspace_bytes) == (64, 64, 0, 0)
+    # the 8 k-blocks arrive in two copies of 4 per operand: a 12-block ring of 3 groups
+    assert (p.k_group, p.stages) == (4, 12)
     # one 128 x 128 output, K-major B: 64 x 32 tiles while they fill under
     # half the SMs (row-major B keeps 64: its boxes are 64 columns wide)
     rc, p = plan(128, 128, 64, bm=1)
@@ -353,3 +355,23 @@ def test_shape_workload_spec():
     for bad in ("abc", "1x2", "1x2x3:rx", "1x2x3:rr:hq", "1x2x3:rr:hh:foo", "-1x2x3"):
         with pytest.raises(ValueError):
             inputs.workload(bad)
+
+
+def test_picker_k_group():
+    """k-blocks per TMA copy on the 64-row kernel: up to 4, whole groups in
+    the ring; a K-major operand needs K a multiple of 64 (its 3-D view holds
+    whole k-blocks), two MN-major operands do not; other kernels copy one
+    k-block at a time."""
+    cases = [  # (M, N, K, a_major, b_major) -> (tile_m, k_group)
+        ((512, 512, 512, 0, 0), (64, 4)),
+        ((512, 512, 128, 0, 0), (64, 2)),
+        ((512, 512, 192, 0, 1), (64, 2)),
+        ((128, 128, 64, 0, 1), (64, 1)),
+        ((512, 512, 200, 0, 0), (64, 1)),    # row-major A is K-major: K % 64 != 0
+        ((512, 512, 200, 1, 0), (64, 4)),    # both MN-major: zero fill past K
+        ((4096, 4096, 4096, 0, 1), (256, 1)),
+    ]
+    for (M, N, K, am, bm), want in cases:
+        rc, p = plan(M, N, K, am=am, bm=bm)
+        assert rc == 0 and (p.tile_m, p.k_group) == want, (M, N, K, am, bm, p.as_dict())
+        assert p.stages % p.k_group == 0
