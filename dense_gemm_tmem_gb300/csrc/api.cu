@@ -260,6 +260,13 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
         }
       }
       if (2 * sk2 > kTicketCap) return GEMM_ERR_UNSUPPORTED;  // a counter per CTA half
+      // two k-blocks per stage and TMA copy (32 KiB boxes): each SM's TMA
+      // unit then issues one copy per k-block instead of two, where a copy
+      // of up to 32 KiB takes it about as long as a 16 KiB one.  A K-major
+      // operand is read through a 3-D view of whole k-blocks (K a multiple
+      // of 64).
+      const bool kg_ok = I2 >= 2 && (K % kBK == 0 || (a_mn && b_mn));
+      p->k_group = !kg_ok ? 1 : o.k_group > 0 ? int(std::min<int64_t>({o.k_group, 3, I2})) : 2;
       p->kernel = GEMM_KERNEL_TC2;
       p->swap_ab = 0;
       p->tile_m = kPairBM;
@@ -967,7 +974,7 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value) {
       o.tile_m = value < 0 ? d.tile_m : int(value);
       return GEMM_OK;
     case GEMM_OPT_K_GROUP:
-      if (value >= 0 && value != 1 && value != 2 && value != 4) return GEMM_ERR_INVALID_ARG;
+      if (value >= 0 && (value < 1 || value > 4)) return GEMM_ERR_INVALID_ARG;
       o.k_group = value < 0 ? d.k_group : int(value);
       return GEMM_OK;
     default:

@@ -5,9 +5,9 @@
 namespace dg {
 
 namespace {
-template <bool OUT_F16>
+template <bool OUT_F16, int G>
 cudaError_t launch_tc2_inst(const TcLaunch& L) {
-  auto kern = tc2_gemm_kernel<OUT_F16>;
+  auto kern = tc2_gemm_kernel<OUT_F16, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Tc2Config::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -28,7 +28,12 @@ cudaError_t launch_tc2_inst(const TcLaunch& L) {
 
 cudaError_t launch_tc2(const TcLaunch& L) {
   if (L.trans || L.grid <= 0 || (L.grid & 1)) return cudaErrorInvalidValue;
-  return L.out_f16 ? launch_tc2_inst<true>(L) : launch_tc2_inst<false>(L);
+  switch (L.args.kgroup) {  // k-blocks per stage: the operands' maps are encoded for it
+    case 1: return L.out_f16 ? launch_tc2_inst<true, 1>(L) : launch_tc2_inst<false, 1>(L);
+    case 2: return L.out_f16 ? launch_tc2_inst<true, 2>(L) : launch_tc2_inst<false, 2>(L);
+    case 3: return L.out_f16 ? launch_tc2_inst<true, 3>(L) : launch_tc2_inst<false, 3>(L);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 int tc2_max_active_clusters(bool out_f16) {
@@ -46,13 +51,13 @@ int tc2_max_active_clusters(bool out_f16) {
   int n = 0;
   cudaError_t e;
   if (out_f16) {
-    e = cudaFuncSetAttribute(tc2_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(tc2_gemm_kernel<true, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Tc2Config::kSmemBytes);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, tc2_gemm_kernel<true>, &cfg);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, tc2_gemm_kernel<true, 1>, &cfg);
   } else {
-    e = cudaFuncSetAttribute(tc2_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(tc2_gemm_kernel<false, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Tc2Config::kSmemBytes);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, tc2_gemm_kernel<false>, &cfg);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, tc2_gemm_kernel<false, 1>, &cfg);
   }
   return e == cudaSuccess ? n : -1;
 }

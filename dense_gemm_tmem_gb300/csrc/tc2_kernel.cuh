@@ -100,6 +100,17 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// The same for a 3-D box (a group of k-blocks of a K-major operand).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int32_t c0, int32_t c1,
+                                                 int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
                : "memory");
@@ -149,13 +160,23 @@ struct TileRing {
   }
 };
 
+// k-block groups: a stage holds G consecutive k-blocks of a unit, brought by
+// one copy per operand half (a 3-D box {64, 128, G} for a K-major operand,
+// boxes {64, 64 G} for an MN-major one), since the TMA unit of an SM takes
+// about the same time per copy up to 32 KiB.  Group g covers k-blocks
+// kb0 + gG ... of the unit; the last may be short (its boxes read zeros past
+// K, or k-blocks of the next unit, which no MMA uses).
+__device__ __forceinline__ int32_t tc2_groups(const Unit& u, int G) {
+  return (u.kb1 - u.kb0 + G - 1) / G;
+}
+
 // TMA producer (one thread in each CTA): this CTA's A rows and B half per
-// k-block; the leader's arrive.expect_tx covers both CTAs' bytes.  Both
-// producers walk the same sequence of (stage, phase) slots; the return value is
-// how many of them this one filled (issued loads for), which is all of them
-// unless a wait gave up.  Loads still in flight after an abort are waited for
-// by tc2_drain_loads once both producers have stopped.
-template <int S>
+// group of G k-blocks; the leader's arrive.expect_tx covers both CTAs' bytes.
+// Both producers walk the same sequence of (stage, phase) slots; the return
+// value is how many of them this one filled (issued loads for), which is all
+// of them unless a wait gave up.  Loads still in flight after an abort are
+// waited for by tc2_drain_loads once both producers have stopped.
+template <int S, int G>
 __device__ __forceinline__ uint32_t tc2_producer(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                              const TcArgs& args, uint8_t* sA, uint8_t* sB,
                                              uint64_t* full, uint64_t* empty, const WaitCtl& wc,
@@ -221,31 +242,38 @@ __device__ __forceinline__ uint32_t tc2_producer(const CUtensorMap& tmA, const C
     // `pairs` at a time), not by this pair's units, so that a tile's k order,
     // and with it its fp32 sum, is the same whichever pair computes it.  The
     // MMA issuer consumes the stages in the order they are loaded.
+    // Groups are walked last to first on such a wave (and the MMA issuer
+    // takes a group's k-blocks last to first), so the k order is exactly the
+    // reverse of the forward one, whatever G.
     const bool rev = ((u.tile / W.grid) & 1) != 0;
-    for (int32_t i = 0; i < u.kb1 - u.kb0; ++i) {
-      const int32_t kb = rev ? u.kb1 - 1 - i : u.kb0 + i;
+    const int32_t ng = tc2_groups(u, G);
+    for (int32_t i = 0; i < ng; ++i) {
+      const int32_t kb = u.kb0 + (rev ? ng - 1 - i : i) * G;  // the group's first k-block
       if (!wait_bounded(smem_u32(&empty[s]), ph ^ 1, wc, kSiteProducer)) {
         ok = false;
         break;
       }
       if (!waited) prerequisites_done();  // the first load: the operands are now final
       const uint32_t fb_local = smem_u32(&full[s]);
-      if (rank == 0) mbar_arrive_expect_tx(fb_local, 2 * Cfg::kStageBytes);
+      if (rank == 0) mbar_arrive_expect_tx(fb_local, 2 * G * Cfg::kStageBytes);
       const uint32_t fb = map_to_rank(fb_local, 0);
-      const uint32_t a_dst = smem_u32(sA + s * Cfg::kABytes);
-      const uint32_t b_dst = smem_u32(sB + s * Cfg::kBBytes);
+      const uint32_t a_dst = smem_u32(sA + s * G * Cfg::kABytes);
+      const uint32_t b_dst = smem_u32(sB + s * G * Cfg::kBBytes);
       const int32_t k0 = kb * kBK;
+      // an MN-major operand: two 64-wide halves, each G k-blocks deep
       if (!args.a_mn) {
-        tma_load_2d_pair(a_dst, &tmA, fb, k0, a_row);
+        if constexpr (G > 1) tma_load_3d_pair(a_dst, &tmA, fb, 0, a_row, kb);
+        else tma_load_2d_pair(a_dst, &tmA, fb, k0, a_row);
       } else {
         tma_load_2d_pair(a_dst, &tmA, fb, a_row, k0);
-        tma_load_2d_pair(a_dst + 8192, &tmA, fb, a_row + 64, k0);
+        tma_load_2d_pair(a_dst + G * 8192, &tmA, fb, a_row + 64, k0);
       }
       if (!args.b_mn) {
-        tma_load_2d_pair(b_dst, &tmB, fb, k0, b_row);
+        if constexpr (G > 1) tma_load_3d_pair(b_dst, &tmB, fb, 0, b_row, kb);
+        else tma_load_2d_pair(b_dst, &tmB, fb, k0, b_row);
       } else {
         tma_load_2d_pair(b_dst, &tmB, fb, b_row, k0);
-        tma_load_2d_pair(b_dst + 8192, &tmB, fb, b_row + 64, k0);
+        tma_load_2d_pair(b_dst + G * 8192, &tmB, fb, b_row + 64, k0);
       }
       if (filled++ == 0) trace_mark(args, blockIdx.x, kTraceFirstLoad);
       if (++s == S) {
@@ -268,7 +296,7 @@ __device__ __forceinline__ uint32_t tc2_producer(const CUtensorMap& tmA, const C
 // needed both halves), so for each stage only its last slot can be one-sided:
 // filled by the peer alone, the leader arms it for the peer's half; filled by
 // the leader alone, the peer's half that will never come is counted as done.
-template <int S>
+template <int S, int G>
 __device__ __forceinline__ void tc2_drain_loads(uint64_t* full, uint32_t n0, uint32_t n1,
                                                 const WaitCtl& wc) {
   const uint32_t n = n0 > n1 ? n0 : n1;
@@ -277,15 +305,15 @@ __device__ __forceinline__ void tc2_drain_loads(uint64_t* full, uint32_t n0, uin
     const uint32_t q = s + ((n - 1 - s) / S) * S;  // the stage's last filled slot
     const uint32_t bar = smem_u32(&full[s]);
     if (q >= n0)
-      mbar_arrive_expect_tx(bar, Tc2Config::kStageBytes);  // the peer's half only
+      mbar_arrive_expect_tx(bar, G * Tc2Config::kStageBytes);  // the peer's half only
     else if (q >= n1)
-      mbar_complete_tx(bar, Tc2Config::kStageBytes);       // the peer's half never comes
+      mbar_complete_tx(bar, G * Tc2Config::kStageBytes);       // the peer's half never comes
     wait_drain(bar, (q / S) & 1, wc);
   }
 }
 
 // MMA issuer (one thread of the leader CTA).
-template <int S>
+template <int S, int G>
 __device__ __forceinline__ void tc2_mma(const TcArgs& args, uint8_t* sA, uint8_t* sB,
                                         uint64_t* full, uint64_t* empty, uint64_t* acc_full,
                                         uint64_t* acc_empty, uint64_t* drain, const WaitCtl& wc,
@@ -309,10 +337,15 @@ __device__ __forceinline__ void tc2_mma(const TcArgs& args, uint8_t* sA, uint8_t
     u.kb1 = W.k_iters;
     return true;
   };
-  const uint32_t a_lbo = args.a_mn ? 8192u : 16u;
-  const uint32_t b_lbo = args.b_mn ? 8192u : 16u;
+  // an MN-major operand's 64-wide halves sit G k-blocks apart; k-block j of
+  // a group starts j blocks into the stage (16 KiB K-major, 8 KiB per half
+  // MN-major)
+  const uint32_t a_lbo = args.a_mn ? uint32_t(G) * 8192u : 16u;
+  const uint32_t b_lbo = args.b_mn ? uint32_t(G) * 8192u : 16u;
   const uint32_t a_step = args.a_mn ? (2048u >> 4) : (32u >> 4);
   const uint32_t b_step = args.b_mn ? (2048u >> 4) : (32u >> 4);
+  const uint32_t a_blk = args.a_mn ? 8192u : uint32_t(Cfg::kABytes);
+  const uint32_t b_blk = args.b_mn ? 8192u : uint32_t(Cfg::kBBytes);
   while (ok && next_unit()) {
     // both CTAs' epilogues release each buffer once before its first use
     // (after seeding it, if asked) and once after each drain
@@ -323,21 +356,35 @@ __device__ __forceinline__ void tc2_mma(const TcArgs& args, uint8_t* sA, uint8_t
     tc_fence_after();
     const uint32_t d_tmem = tmem_base + uint32_t(b * kPairBN);
     const bool seeded = args.bias_init && u.kb0 == 0;  // accumulate onto the bias
-    // stages arrive in the producer's order (k ascending, or descending on
-    // every other unit); the first MMA of the unit starts the sum
-    for (int32_t i = 0; i < u.kb1 - u.kb0; ++i) {
+    // groups arrive in the producer's order (k ascending, or descending on
+    // every other wave of tiles, the k-blocks of a group then taken last to
+    // first); the first MMA of the unit starts the sum
+    const bool rev = ((u.tile / W.grid) & 1) != 0;
+    const int32_t ng = tc2_groups(u, G);
+    for (int32_t i = 0; i < ng; ++i) {
       if (!wait_bounded(smem_u32(&full[s]), ph, wc, kSiteMmaFull)) {
         ok = false;
         break;
       }
       tc_fence_after();
       if (!any) trace_mark(args, blockIdx.x, kTraceFirstData);
-      const uint64_t adesc = make_sdesc_sw128(smem_u32(sA + s * Cfg::kABytes), a_lbo, 1024);
-      const uint64_t bdesc = make_sdesc_sw128(smem_u32(sB + s * Cfg::kBBytes), b_lbo, 1024);
+      const int32_t kb = u.kb0 + (rev ? ng - 1 - i : i) * G;
+      const int nj = u.kb1 - kb < G ? int(u.kb1 - kb) : G;
+      const uint32_t a0 = smem_u32(sA + s * G * Cfg::kABytes);
+      const uint32_t b0 = smem_u32(sB + s * G * Cfg::kBBytes);
 #pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk)
-        tc_mma_f16_pair(d_tmem, adesc + uint64_t(kk * a_step), bdesc + uint64_t(kk * b_step),
-                        args.idesc, (i > 0 || kk > 0 || seeded) ? 1u : 0u);
+      for (int jj = 0; jj < G; ++jj) {
+        if (jj < nj) {
+          const int j = rev ? nj - 1 - jj : jj;
+          const uint64_t adesc = make_sdesc_sw128(a0 + uint32_t(j) * a_blk, a_lbo, 1024);
+          const uint64_t bdesc = make_sdesc_sw128(b0 + uint32_t(j) * b_blk, b_lbo, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            tc_mma_f16_pair(d_tmem, adesc + uint64_t(kk * a_step),
+                            bdesc + uint64_t(kk * b_step), args.idesc,
+                            (i > 0 || jj > 0 || kk > 0 || seeded) ? 1u : 0u);
+        }
+      }
       any = true;
       tc_commit_pair_both(smem_u32(&empty[s]));
       if (++s == S) {
@@ -546,21 +593,24 @@ __device__ __forceinline__ void tc2_epilogue(const TcArgs& args, uint64_t* acc_f
 }
 
 // args.work counts cluster tiles (256 x 256) and clusters (work.grid = CTAs / 2).
-template <bool OUT_F16>
+// G: k-blocks per stage and TMA copy (args.kgroup; the operands' maps are
+// encoded for it).
+template <bool OUT_F16, int G>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const TcArgs args) {
   using Cfg = Tc2Config;
-  constexpr int S = Cfg::kStages;
+  static_assert(Cfg::kStages % G == 0, "whole groups");
+  constexpr int S = Cfg::kStages / G;  // ring stages of G k-blocks
 
   const uint64_t t_entry = args.trace ? globaltimer_ns() : 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + S * Cfg::kABytes;
-  uint8_t* stage = sB + S * Cfg::kBBytes;  // epilogue staging, 1024-byte aligned
+  uint8_t* sB = smem + S * G * Cfg::kABytes;
+  uint8_t* stage = sB + S * G * Cfg::kBBytes;  // epilogue staging, 1024-byte aligned
   uint64_t* bars = reinterpret_cast<uint64_t*>(stage + Cfg::kEpiStageBytes);
   uint64_t* full = bars;               // leader's counts both CTAs' bytes
   uint64_t* empty = bars + S;          // one multicast commit per phase, in both CTAs
@@ -621,7 +671,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   uint32_t filled = 0;  // thread 0: load slots this CTA's producer filled
   if (warp == 0) {
     if (lane == 0) {
-      filled = tc2_producer<S>(tmA, tmB, args, sA, sB, full, empty, wc, rank, cluster_id,
+      filled = tc2_producer<S, G>(tmA, tmB, args, sA, sB, full, empty, wc, rank, cluster_id,
                                t_entry, ring);
       if (rank != 0) st_dsmem_u32(map_to_rank(smem_u32(peer_filled), 0), filled);
     } else {
@@ -630,7 +680,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   } else if (warp == 1) {
     pdl_wait_prerequisites();
     if (lane == 0 && rank == 0)
-      tc2_mma<S>(args, sA, sB, full, empty, acc_full, acc_empty, drain, wc, tmem_base,
+      tc2_mma<S, G>(args, sA, sB, full, empty, acc_full, acc_empty, drain, wc, tmem_base,
                  cluster_id, ring);
   } else {
     tc2_epilogue<OUT_F16>(args, acc_full, acc_empty, wc, tmem_base, rank, cluster_id,
@@ -642,7 +692,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   // Both CTAs' roles are done: no MMA or remote arrive is still aimed at
   // either CTA, no load will be issued, and the peer's fill count is in.
   cluster_sync_all();
-  if (rank == 0 && threadIdx.x == 0) tc2_drain_loads<S>(full, filled, *peer_filled, wc);
+  if (rank == 0 && threadIdx.x == 0) tc2_drain_loads<S, G>(full, filled, *peer_filled, wc);
   cluster_sync_all();  // no copy still lands in either CTA's shared memory
   if (warp == 1) {
     tc_fence_after();

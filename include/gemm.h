@@ -152,9 +152,11 @@ enum {
                                     128; 64 or 128 forced (64: whole tiles, operands not
                                     swapped, tile width 32, 64 or 128) */
   GEMM_OPT_K_GROUP = 16          /* k-blocks per TMA copy where the kernel groups them (the
-                                    64-row kernel): -1 (default) the picker's (up to 4 when
-                                    K is a multiple of 64 or both operands are MN-major);
-                                    1, 2 or 4 forced (rounded down to what the shape allows) */
+                                    64-row and two-SM kernels): -1 (default) the picker's
+                                    (up to 4, and 2 on the two-SM kernel, when K is a
+                                    multiple of 64 or both operands are MN-major); 1, 2 or
+                                    4 forced (rounded down to what the shape and kernel
+                                    allow) */
 };
 
 /* Creates a handle on CUDA device `device`.  Allocates, on that device, the

@@ -333,6 +333,32 @@ def test_pair_dynamic_matches_static(g, dev, odt):
     check(as_f64(C_dyn, rows), oracle.gemm_rows(p.A, p.B, p.bias, b_major=1, rows=rows), p, rows)
 
 
+@pytest.mark.parametrize("am,bm,odt", [(0, 1, F16), (0, 0, F32), (1, 0, F16), (1, 1, F32)])
+@pytest.mark.parametrize("split", [False, True])
+def test_pair_k_groups(g, dev, am, bm, odt, split):
+    """Two-SM kernel with 2 or 3 k-blocks per stage and TMA copy (3-D boxes
+    for a K-major operand, deeper boxes for an MN-major one) against 1, on
+    1040 x 1040 x 1088: 17 k-blocks, so the last group is short.  Whole tiles:
+    25 pair tiles on 3 pairs, every other wave walking k backwards; split: a
+    Stream-K split over 7 pairs, whose ranges start and end inside groups.
+    Both groupings give the same bits (the same k order) and match the
+    oracle."""
+    M = N = 1040
+    K = 1088
+    odt_b = B.GEMM_F16 if odt == F16 else B.GEMM_F32
+    p = problem(M, N, K, am, bm, F16, odt, True, 170 + 2 * am + bm + 4 * split)
+    opts = dict(kernel=TC2, pair_split=1, grid=14) if split else dict(kernel=TC2, grid=6)
+    outs = []
+    for kg in (1, 2, 3):
+        set_opts(g, k_group=kg, **opts)
+        pl = g.plan(M, N, K, am, bm, B.GEMM_F16, odt_b)
+        assert (pl["kernel"], pl["k_group"], pl["sk_tiles"] > 0) == (TC2, kg, split)
+        outs.append(run(g, p, dev).cpu())
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    ref = oracle.gemm(p.A, p.B, p.bias, a_major=am, b_major=bm)
+    check(as_f64(outs[1]), ref, p)
+
+
 @pytest.mark.parametrize("grid", [2, 10, 38, 152])
 def test_pair_split_grid_sizes(g, dev, grid):
     """Two-SM Stream-K: every pair tile's k-blocks split over grid / 2 pairs;

@@ -369,7 +369,10 @@ def test_picker_k_group():
         ((128, 128, 64, 0, 1), (64, 1)),
         ((512, 512, 200, 0, 0), (64, 1)),    # row-major A is K-major: K % 64 != 0
         ((512, 512, 200, 1, 0), (64, 4)),    # both MN-major: zero fill past K
-        ((4096, 4096, 4096, 0, 1), (256, 1)),
+        ((4096, 4096, 4096, 0, 1), (256, 2)),   # two-SM kernel: 2 per copy
+        ((4096, 4096, 4104, 0, 1), (256, 1)),   # K-major operands, K % 64 != 0
+        ((4096, 4096, 4104, 1, 0), (256, 2)),   # both MN-major
+        ((1024, 1024, 768, 0, 1), (128, 1)),    # one-SM 128-row kernel: 1
     ]
     for (M, N, K, am, bm), want in cases:
         rc, p = plan(M, N, K, am=am, bm=bm)
