@@ -176,6 +176,26 @@ int plan_simt(int64_t M, int64_t N, int64_t K, int num_sms, const Options& o, ge
 //        (Stream-K), at least enough k-blocks per CTA that it reads 4x its
 //        fp32 partial tile in operands (else whole tiles, one per CTA);
 //      otherwise whole tiles, persistent over the SMs.
+// k-blocks per TMA copy on a 128-row one-SM plan with `stages` ring slots:
+// 2 by default where the ring then still has 3 stages (6 slots or more), else
+// 1; GEMM_OPT_K_GROUP forces it.  Measured (graph replay, cold inputs, us per
+// launch, 1 vs 2): 2048x1024x2048 16.5 vs 13.9, 1024x1024x768 8.1 vs 7.1,
+// skinny M = 64 / 128 11.7 / 14.3 vs 10.9 / 13.7; the 5-slot short rings of
+// skinny M <= 32 were slower as 2 stages of 2 (10.0 vs 10.8).  A K-major
+// operand needs K a multiple of 64 (its 3-D view holds whole k-blocks); the
+// ring keeps whole groups and at least `min_stages` slots.  Returns the group
+// and trims *stages.
+int one_sm_k_group(const Options& o, int64_t K, bool a_mn, bool b_mn, int* stages,
+                   int min_stages) {
+  if (K % kBK != 0 && !(a_mn && b_mn)) return 1;
+  const int kg = o.k_group > 0 ? std::min(o.k_group, 4) : (*stages >= 6 ? 2 : 1);
+  if (kg <= 1) return 1;
+  const int st = *stages - *stages % kg;
+  if (st < kg || st < min_stages) return 1;
+  *stages = st;
+  return kg;
+}
+
 int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
              const Options& o, gemm_plan_t* p) {
   if (!p) return GEMM_ERR_INVALID_ARG;
@@ -460,6 +480,7 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
         p->stages = std::min(p->stages, lean);
       if (o.stages > 0) p->stages = std::min(o.stages, tc_stages_for(bn));
       p->stages = std::max(p->stages, tc_min_stages(bn, int(cs)));
+      p->k_group = one_sm_k_group(o, K, a_mn, b_mn, &p->stages, tc_min_stages(bn, int(cs)));
       p->grid = int32_t(T * cs);
       p->tiles_m = int32_t(tiles_m);
       p->tiles_n = int32_t(tiles_n);
@@ -520,6 +541,7 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
   p->tile_n = bn;
   p->tile_k = kBK;
   p->stages = o.stages > 0 ? std::min(o.stages, tc_stages_for(bn)) : tc_stages_for(bn);
+  p->k_group = one_sm_k_group(o, K, a_mn, b_mn, &p->stages, 1);
   p->grid = int32_t(grid);
   p->tiles_m = int32_t(tiles_m);
   p->tiles_n = int32_t(tiles_n);

@@ -91,9 +91,9 @@ struct TcArgs {
                           // 16 bytes, so every 4-column group is whole and aligned
   int32_t bias_init = 0;  // 1: each tile's k-block-0 accumulator is seeded with the bias
   int32_t stages = 0;      // ring stages of this launch, 1 ... TcConfig<BN>::kStages (0: all)
-  int32_t kgroup = 1;      // k-blocks per TMA copy (64-row and two-SM kernels): the ring's
-                           // stages are taken kgroup at a time, one copy per operand each;
-                           // > 1 needs the operands' maps encoded for it (3-D for K-major)
+  int32_t kgroup = 1;      // k-blocks per TMA copy: the ring's stages are taken kgroup at
+                           // a time, one copy per operand (half) each; > 1 needs the
+                           // operands' maps encoded for it (3-D for K-major)
   uint32_t idesc;         // tcgen05 instruction descriptor
   uint64_t* trace = nullptr;  // NULL, or kTraceSlots %globaltimer stamps per CTA
   int* sched = nullptr;       // two-SM kernel, whole tiles: NULL for the static schedule,
@@ -662,17 +662,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                    const __grid_constant__ CUtensorMap tmC, const TcArgs args) {
   using Cfg = TcConfig<BN>;
   // A launch may use fewer stages than the ring can hold: less shared memory,
-  // so that the next launch's CTAs fit beside this one's.
-  const int S = args.stages > 0 ? args.stages : Cfg::kStages;
+  // so that the next launch's CTAs fit beside this one's.  The ring's k-block
+  // slots are taken J = args.kgroup at a time: one TMA copy per operand (half)
+  // brings J consecutive k-blocks (a 3-D box for a K-major operand, a box J
+  // k-blocks deep for an MN-major one), as in the 64-row kernel.
+  const int J = args.kgroup > 1 ? args.kgroup : 1;
+  const int S = (args.stages > 0 ? args.stages : Cfg::kStages) / J;  // stages of J blocks
   constexpr int CW = Cfg::kChunk;
 
   const uint64_t t_entry = args.trace ? globaltimer_ns() : 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;                         // S x 16 KiB
-  uint8_t* sB = smem + S * Cfg::kABytes;      // S x BN*128 B
-  uint8_t* stage = sB + S * Cfg::kBBytes;     // epilogue staging, 1024-byte aligned
+  uint8_t* sA = smem;                         // S x J x 16 KiB
+  uint8_t* sB = smem + S * J * Cfg::kABytes;  // S x J x BN*128 B
+  uint8_t* stage = sB + S * J * Cfg::kBBytes; // epilogue staging, 1024-byte aligned
   uint64_t* bars = reinterpret_cast<uint64_t*>(stage + Cfg::kEpiStageBytes);
   uint64_t* full = bars;                      // TMA bytes landed in stage s
   uint64_t* empty = bars + S;                 // MMAs reading stage s are done
@@ -745,7 +749,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       while (ok && it.next(W, u)) {
         int32_t tm, tn;
         tile_coords(W, u.tile, tm, tn);
-        for (int32_t kb = u.kb0; kb < u.kb1; ++kb) {
+        for (int32_t kb = u.kb0; kb < u.kb1; kb += J) {
           if (!wait_bounded(smem_u32(&empty[s]), ph ^ 1, wc, kSiteProducer)) {
             ok = false;
             break;
@@ -754,24 +758,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             prerequisites_done();
             waited = true;
           }
+          // whole boxes: zeros past K, or k-blocks past the unit no MMA uses
           const uint32_t fb = smem_u32(&full[s]);
-          mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
-          const uint32_t a_dst = smem_u32(sA + s * Cfg::kABytes);
-          const uint32_t b_dst = smem_u32(sB + s * Cfg::kBBytes);
+          mbar_arrive_expect_tx(fb, J * Cfg::kStageBytes);
+          const uint32_t a_dst = smem_u32(sA + s * J * Cfg::kABytes);
+          const uint32_t b_dst = smem_u32(sB + s * J * Cfg::kBBytes);
           const int32_t k0 = kb * kBK;
           if (!args.a_mn) {
-            tma_load_2d(a_dst, &tmA, fb, k0, tm * kBM);
-          } else {
+            if (J > 1)
+              tma_load_3d(a_dst, &tmA, fb, 0, tm * kBM, kb);
+            else
+              tma_load_2d(a_dst, &tmA, fb, k0, tm * kBM);
+          } else {  // two 64-wide halves, J k-blocks deep each
             tma_load_2d(a_dst, &tmA, fb, tm * kBM, k0);
-            tma_load_2d(a_dst + 8192, &tmA, fb, tm * kBM + 64, k0);
+            tma_load_2d(a_dst + J * 8192, &tmA, fb, tm * kBM + 64, k0);
           }
           if (!args.b_mn) {
-            tma_load_2d(b_dst, &tmB, fb, k0, tn * BN);
+            if (J > 1)
+              tma_load_3d(b_dst, &tmB, fb, 0, tn * BN, kb);
+            else
+              tma_load_2d(b_dst, &tmB, fb, k0, tn * BN);
           } else {
             if constexpr (BN >= 64) {
 #pragma unroll
               for (int j = 0; j < BN / 64; ++j)
-                tma_load_2d(b_dst + j * 8192, &tmB, fb, tn * BN + 64 * j, k0);
+                tma_load_2d(b_dst + j * J * 8192, &tmB, fb, tn * BN + 64 * j, k0);
             }
           }
           if (first) {
@@ -804,11 +815,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int s = 0, b = 0;
       uint32_t ph = 0, aph = 0;
       bool ok = true, any = false;
-      const uint32_t a_lbo = args.a_mn ? 8192u : 16u;
-      const uint32_t b_lbo = args.b_mn ? 8192u : 16u;
+      // an MN-major operand's 64-wide halves sit J k-blocks (J x 8 KiB) apart
+      const uint32_t a_lbo = args.a_mn ? uint32_t(J) * 8192u : 16u;
+      const uint32_t b_lbo = args.b_mn ? uint32_t(J) * 8192u : 16u;
       // advance per 16-deep k slice: 32 B along a K-major row, 16 rows (2 KiB) MN-major
       const uint32_t a_step = args.a_mn ? (2048u >> 4) : (32u >> 4);
       const uint32_t b_step = args.b_mn ? (2048u >> 4) : (32u >> 4);
+      // k-block j of a group: a whole block K-major, 64 k rows of each half MN-major
+      const uint32_t a_blk = args.a_mn ? 8192u : uint32_t(Cfg::kABytes);
+      const uint32_t b_blk = args.b_mn ? 8192u : uint32_t(Cfg::kBBytes);
       while (ok && it.next(W, u)) {
         // the epilogue releases each buffer once before its first use (after
         // seeding it, if asked) and once after each drain
@@ -819,19 +834,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(b * BN);
         const bool seeded = args.bias_init && u.kb0 == 0;  // accumulate onto the bias
-        for (int32_t kb = u.kb0; kb < u.kb1; ++kb) {
+        for (int32_t kb = u.kb0; kb < u.kb1; kb += J) {
           if (!wait_bounded(smem_u32(&full[s]), ph, wc, kSiteMmaFull)) {
             ok = false;
             break;
           }
           tc_fence_after();
           if (!any) trace_mark(args, blockIdx.x, kTraceFirstData);
-          const uint64_t adesc = make_sdesc_sw128(smem_u32(sA + s * Cfg::kABytes), a_lbo, 1024);
-          const uint64_t bdesc = make_sdesc_sw128(smem_u32(sB + s * Cfg::kBBytes), b_lbo, 1024);
+          const uint32_t a0 = smem_u32(sA + s * J * Cfg::kABytes);
+          const uint32_t b0 = smem_u32(sB + s * J * Cfg::kBBytes);
+          const int nj = u.kb1 - kb < J ? int(u.kb1 - kb) : J;
+#pragma unroll 1
+          for (int j = 0; j < nj; ++j) {
+            const uint64_t adesc = make_sdesc_sw128(a0 + uint32_t(j) * a_blk, a_lbo, 1024);
+            const uint64_t bdesc = make_sdesc_sw128(b0 + uint32_t(j) * b_blk, b_lbo, 1024);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            tc_mma_f16(d_tmem, adesc + uint64_t(kk * a_step), bdesc + uint64_t(kk * b_step),
-                       args.idesc, (kb > u.kb0 || kk > 0 || seeded) ? 1u : 0u);
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              tc_mma_f16(d_tmem, adesc + uint64_t(kk * a_step), bdesc + uint64_t(kk * b_step),
+                         args.idesc, (kb > u.kb0 || j > 0 || kk > 0 || seeded) ? 1u : 0u);
+          }
           any = true;
           tc_commit(smem_u32(&empty[s]));
           if (++s == S) {

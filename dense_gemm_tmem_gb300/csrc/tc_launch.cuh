@@ -36,6 +36,9 @@ cudaError_t launch_tc_inst(const TcLaunch& L) {
   }
   const int stages = L.args.stages > 0 ? L.args.stages : Cfg::kStages;
   if (stages > Cfg::kStages) return cudaErrorInvalidValue;
+  // whole groups of k-blocks; an MN-major box is at most 256 k deep
+  const int J = L.args.kgroup;
+  if (J < 1 || J > 4 || stages % J != 0) return cudaErrorInvalidValue;
   // a cluster split of a tile wider than 64 parks its partial in the ring
   if (s > 1 && BN > 64 &&
       int64_t(stages) * Cfg::kStageBytes < int64_t(kBM) * (BN + 4) * 4)

@@ -151,12 +151,14 @@ enum {
                                     whole tiles when 64-row tiles still fit one wave, else
                                     128; 64 or 128 forced (64: whole tiles, operands not
                                     swapped, tile width 32, 64 or 128) */
-  GEMM_OPT_K_GROUP = 16          /* k-blocks per TMA copy where the kernel groups them (the
-                                    64-row and two-SM kernels): -1 (default) the picker's
-                                    (up to 4, and 2 on the two-SM kernel, when K is a
-                                    multiple of 64 or both operands are MN-major); 1, 2 or
-                                    4 forced (rounded down to what the shape and kernel
-                                    allow) */
+  GEMM_OPT_K_GROUP = 16          /* k-blocks per TMA copy on the tensor-core kernels (the
+                                    ring's stages are taken that many at a time): -1
+                                    (default) the picker's, when K is a multiple of 64 or
+                                    both operands are MN-major: up to 4 on the 64-row
+                                    kernel, 2 on the two-SM kernel, 2 on the 128-row kernel
+                                    when its ring holds 6 k-blocks or more, else 1; 1 to 4
+                                    forced (rounded down to what the shape, kernel and ring
+                                    allow: at most 3 on the two-SM kernel) */
 };
 
 /* Creates a handle on CUDA device `device`.  Allocates, on that device, the

@@ -240,6 +240,45 @@ def test_tile64_k_groups_mn_major_ragged_k(g, dev):
     full_check(g, dev, p)
 
 
+ONE_SM_K_GROUP_CASES = [
+    # name, M, N, K, am, bm, odt, opts
+    ("whole_256", 520, 776, 1088, 0, 1, F16, {"kernel": TC, "tile_n": 256}),
+    ("whole_128_mn", 520, 776, 1088, 1, 0, F32, {"kernel": TC, "tile_n": 128}),
+    ("whole_64_rr", 520, 776, 1088, 0, 0, F32, {"kernel": TC, "tile_n": 64}),
+    ("whole_cc", 520, 776, 1088, 1, 1, F16, {"kernel": TC}),
+    ("streamk", 384, 512, 1088, 0, 1, F32, {"kernel": SK, "grid": 23}),
+    ("csplit_push", 512, 512, 1088, 0, 1, F32, {"kernel": SPLITC, "csplit": 4, "tile_n": 64}),
+    ("csplit_park", 512, 512, 1088, 0, 0, F16, {"kernel": SPLITC, "csplit": 4, "tile_n": 128}),
+    ("skinny", 16, 1024, 2048, 0, 0, F32, {}),
+    ("skinny_col", 40, 1536, 1024, 0, 1, F16, {}),
+]
+
+
+@pytest.mark.parametrize("case", ONE_SM_K_GROUP_CASES, ids=[c[0] for c in ONE_SM_K_GROUP_CASES])
+def test_one_sm_k_groups(g, dev, case):
+    """The 128-row one-SM kernel with 2 and 4 k-blocks per stage and TMA copy
+    against 1: whole tiles of every width and layout, Stream-K ranges that
+    start and end inside groups, cluster splits (pushed and parked partials)
+    whose ranks' ranges are not multiples of the group, and swapped skinny
+    products.  K = 1088 gives 17 k-blocks (a short last group).  Every
+    grouping gives the same bits and matches the oracle."""
+    _, M, N, K, am, bm, odt, opts = case
+    odt_b = B.GEMM_F16 if odt == F16 else B.GEMM_F32
+    p = problem(M, N, K, am, bm, F16, odt, True, 360 + M % 97)
+    outs = []
+    for kg in (1, 2, 4):
+        set_opts(g, k_group=kg, tile_m=128, **opts)
+        pl = g.plan(M, N, K, am, bm, B.GEMM_F16, odt_b)
+        assert pl["tile_m"] == 128 and pl["kernel"] != TC2
+        assert pl["k_group"] in (1, kg) and pl["stages"] % pl["k_group"] == 0
+        if kg > 1 and pl["stages"] >= 2 * kg:
+            assert pl["k_group"] == kg
+        outs.append(run(g, p, dev).cpu())
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    ref = oracle.gemm(p.A, p.B, p.bias, a_major=am, b_major=bm)
+    check(as_f64(outs[2]), ref, p)
+
+
 def test_tile64_unaligned_output(g, dev):
     """64-row tiles writing a C whose rows are not 16-byte aligned (the
     element-wise store path)."""
@@ -273,11 +312,12 @@ def test_lean_ring_for_wide_cluster_split(g, dev):
     """A cluster split over more than half the SMs runs with a ring short
     enough for two CTAs per SM where the kernel's registers allow it and the
     ring still keeps enough loads in flight (so the next launch's CTAs start
-    beside this one's): skinny M = 16 (16-wide swapped tiles, 5 stages)."""
+    beside this one's): skinny M = 16 (16-wide swapped tiles, 5 stages, one
+    k-block per copy: a short ring keeps its stages single)."""
     w = inputs.WORKLOADS["skinny_m16_4096"]
     pl = g.plan(w.M, w.N, w.K, w.a_major, w.b_major, B.GEMM_F16, B.GEMM_F32)
     assert pl["kernel"] == SPLITC and pl["grid"] > 76
-    assert pl["stages"] == 5
+    assert (pl["stages"], pl["k_group"]) == (5, 1)
     full_check(g, dev, w.make())
 
 

@@ -372,7 +372,8 @@ def test_picker_k_group():
         ((4096, 4096, 4096, 0, 1), (256, 2)),   # two-SM kernel: 2 per copy
         ((4096, 4096, 4104, 0, 1), (256, 1)),   # K-major operands, K % 64 != 0
         ((4096, 4096, 4104, 1, 0), (256, 2)),   # both MN-major
-        ((1024, 1024, 768, 0, 1), (128, 1)),    # one-SM 128-row kernel: 1
+        ((1024, 1024, 768, 0, 1), (128, 2)),    # one-SM 128-row kernel, 8-slot ring: 2
+        ((1024, 1024, 776, 0, 1), (128, 1)),    # K-major, K % 64 != 0
     ]
     for (M, N, K, am, bm), want in cases:
         rc, p = plan(M, N, K, am=am, bm=bm)
