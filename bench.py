@@ -106,7 +106,7 @@ def kernel_source_hash(files):
     return h.hexdigest()[:16]
 
 
-TRAFFIC_PLAN_KEYS = ("kernel", "tile_m", "tile_n", "grid", "group_m", "cluster_split")
+TRAFFIC_PLAN_KEYS = ("kernel", "tile_m", "tile_n", "grid", "group_m", "cluster_split", "k_group")
 
 
 def recorded_traffic(workload, plan):
