@@ -423,15 +423,15 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
         // Tile width and cluster size by the per-CTA cost: the operand bytes
         // it loads, (128 + w) x 128 B per k-block over ceil(I / s) k-blocks,
         // plus the fp32 partial bytes it exchanges, 128 x w x 4 B x (s-1)/s,
-        // weighted 3x (distributed shared memory moves them about that much
-        // slower per SM than TMA loads operands).  Widths: the picker's, and
-        // 64 for unswapped tiles wider than that.  Measured best on all of
-        // (graph replay, cold inputs, us per launch, picked vs the old rule's
-        // widest tile with the largest fitting split): 512x512x1024 7.3 vs 8.0,
-        // 512x512x2048 8.4 vs 9.2, 384x384x2048 7.6 vs 8.2, 512x512x8192 15.2
-        // vs 16.4, 256x256x1024 6.1 vs 7.2; unchanged where 128-wide tiles
-        // were best (512x1024x2048, 768x768x1536, 1024x1024x2048/8192,
-        // 256x512x4096).
+        // weighted 5x (distributed shared memory moves them that much slower
+        // per SM than TMA brings operands in copies of two k-blocks).
+        // Widths: the picker's, and 64 for unswapped tiles wider than that.
+        // Measured (graph replay, cold inputs, us per launch, every width and
+        // cluster size forced): the rule picks the fastest on 512x512x1024
+        // (6.9), 512x512x2048 (7.9), 384x384x2048 (7.1), 512x512x8192 (13.4),
+        // 512x1024x2048 (9.7: 64 wide in pairs), 768x768x1536 (9.0: 64 wide in
+        // pairs), 256x512x4096 (8.9), 1024x1024x2048 (12.6), 1024x1024x8192
+        // (24.6); 256x256x1024 5.9 against 5.8 for clusters of 8.
         int best_w = 0;
         double best_cost = 0;
         for (int w : {bn, (!swap && o.force_tile_n <= 0 && bn > 64) ? 64 : 0}) {
@@ -441,7 +441,7 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
           for (int sz : {8, 4, 2}) {
             if (!fits(tw, sz) || I < 2 * sz) continue;
             const double cost = double(kBM + w) * kBK * 2 * double(ceil_div(I, sz)) +
-                                3.0 * kBM * w * 4 * double(sz - 1) / sz;
+                                5.0 * kBM * w * 4 * double(sz - 1) / sz;
             if (cs == 0 || cost < best_cost) {
               best_w = w;
               cs = sz;

@@ -156,9 +156,13 @@ def test_picker_small_shapes():
     assert rc == 0 and p.kernel == B.GEMM_KERNEL_SPLITC
     assert (p.tile_n, p.tiles_m, p.tiles_n, p.k_iters) == (64, 4, 8, 16)
     assert (p.cluster_split, p.grid, p.sk_tiles, p.workspace_bytes) == (4, 128, 32, 0)
-    # the cost rule keeps 128-wide tiles where they load less per CTA
+    # 64-wide tiles in pairs exchange fewer partial bytes than 128-wide ones
+    # in clusters of 4 (measured 9.7 vs 10.1 us)
     rc, p = plan(512, 1024, 2048)
-    assert (p.kernel, p.tile_n, p.cluster_split, p.grid) == (B.GEMM_KERNEL_SPLITC, 128, 4, 128)
+    assert (p.kernel, p.tile_n, p.cluster_split, p.grid) == (B.GEMM_KERNEL_SPLITC, 64, 2, 128)
+    # the cost rule keeps 128-wide tiles where they load far less per CTA
+    rc, p = plan(1024, 1024, 2048)
+    assert (p.kernel, p.tile_n, p.cluster_split, p.grid) == (B.GEMM_KERNEL_SPLITC, 128, 2, 128)
     # deep K: 16 tiles in clusters of 8
     rc, p = plan(512, 512, 8192)
     assert rc == 0 and p.kernel == B.GEMM_KERNEL_SPLITC
