@@ -456,7 +456,8 @@ def test_cluster_split_narrow_unswapped(g, dev, csplit, am, bm, odt):
 
 
 @pytest.mark.parametrize("M,N,K,w", [(512, 512, 1024, 64), (384, 384, 2048, 64),
-                                     (256, 256, 1024, 64), (512, 1024, 2048, 128)])
+                                     (256, 256, 1024, 64), (512, 1024, 2048, 64),
+                                     (1024, 1024, 2048, 128)])
 def test_cluster_split_picker_widths(g, dev, M, N, K, w):
     """The picker's own cluster splits (width and size by per-CTA cost)."""
     p = problem(M, N, K, 0, 1, F16, F32, True, 180 + M + K)
