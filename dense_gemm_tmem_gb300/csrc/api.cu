@@ -301,7 +301,13 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
       p->sk_tiles = int32_t(sk2);
       p->a_mn_major = a_mn;
       p->b_mn_major = b_mn;
-      p->group_m = o.group_m > 0 ? o.group_m : 2048 / kPairBM;
+      // raster groups of 4096 rows of A (16 pair-tile rows), walked in the
+      // static order: measured with two-k-block copies (same box, us per
+      // launch, 20 / 400 launches of 8192^3): static 16 rows 606-608 / 660.9,
+      // static 8 rows 615 / 667.7, run-time order 8 rows 621 / 677.4, run-time
+      // 16 rows 616 / 674.9; 16384^3 static 16 rows 4658 / 5205 against
+      // run-time 8 rows 4688 / 5259.
+      p->group_m = o.group_m > 0 ? o.group_m : 4096 / kPairBM;
       // two partial slots per pair, each a 128 x 256 fp32 half per CTA
       p->workspace_bytes = sk2 > 0 ? int64_t(2) * np * 2 * kBM * kPairBN * 4 : 0;
       return GEMM_OK;
@@ -1119,11 +1125,11 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, co
   const int64_t c_pitch = N * (layout.out_dtype == GEMM_F16 ? 2 : 4);
   a.c_vec = (!swap && (reinterpret_cast<uintptr_t>(C) & 15) == 0 && c_pitch % 16 == 0) ? 1 : 0;
   a.bias_init = (h->opt.bias_init && bias) ? 1 : 0;
-  // Whole pair tiles are handed out at run time in tile order (a counter the
-  // pairs draw from), so the tiles in flight stay one compact block of the
-  // raster however the pairs drift apart; the split tail and the bias seeding
-  // keep the static schedule.
-  if (pair && plan.sk_tiles == 0 && !a.bias_init && h->opt.dyn_sched != 0)
+  // Asked for (GEMM_OPT_DYNAMIC_TILES), whole pair tiles are handed out at
+  // run time in tile order (a counter the pairs draw from), so the tiles in
+  // flight stay one compact block of the raster however the pairs drift
+  // apart; the split tail and the bias seeding keep the static schedule.
+  if (pair && plan.sk_tiles == 0 && !a.bias_init && h->opt.dyn_sched > 0)
     a.sched = h->tickets + dg::kTicketCap;
   a.stages = pair ? 0 : plan.stages;
   a.kgroup = kgroup;

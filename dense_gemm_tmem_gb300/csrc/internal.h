@@ -28,7 +28,7 @@ struct Options {
   int tma_store = -1;      // epilogue output by TMA store where C allows it: -1 for fp16
                            // output or more output tiles than CTAs, 1 always, 0 never
   int bias_init = 0;       // seed the accumulators with the bias
-  int dyn_sched = 1;       // two-SM kernel, whole tiles: tiles handed out at run time
+  int dyn_sched = 0;       // two-SM kernel, whole tiles: 1 tiles handed out at run time
   int stages = -1;         // one-SM kernel ring stages: -1 picker, n >= 1 forced
   int tile_m = -1;         // one-SM kernel tile rows: -1 picker, 64 or 128 forced
   int k_group = -1;        // k-blocks per TMA copy (64-row kernel): -1 picker, 1/2/4 forced

@@ -112,8 +112,9 @@ enum {
   GEMM_OPT_MIN_SPLIT_ITERS = 4,  /* fewest k-blocks per CTA when splitting (default: enough
                                     that a CTA reads 4x its fp32 partial tile in operands) */
   GEMM_OPT_FORCE_SWAP_AB = 5,    /* 0 or 1, or -1 for the picker's choice */
-  GEMM_OPT_GROUP_M = 6,          /* tile rows per raster group (default: 2048 rows of A,
-                                    i.e. 8 pair tiles or 16 one-SM tiles) */
+  GEMM_OPT_GROUP_M = 6,          /* tile rows per raster group (default: 4096 rows of A,
+                                    16 pair tiles, on the two-SM kernel; 2048 rows, 16
+                                    tiles, on the one-SM kernels) */
   GEMM_OPT_PAIR = 7,             /* two-SM kernel: 0 never, 1 whenever the shape allows
                                     (not swapped), -1 the picker's rule */
   GEMM_OPT_CLUSTER_SPLIT = 8,    /* cluster split: 0 never (Stream-K instead), 2/4/8 CTAs
@@ -134,12 +135,16 @@ enum {
                                     reduction from the bias (seeded into the accumulator
                                     before the first MMA) instead of adding it to the sum;
                                     0 (default): added to the finished fp32 sum */
-  GEMM_OPT_DYNAMIC_TILES = 13,   /* two-SM kernel with whole tiles: 1 (default) each pair
-                                    takes its next tile from a counter in the handle at run
-                                    time, so the tiles in flight stay in raster order; 0 the
-                                    static schedule gemm_work_units reports (pair c takes
-                                    tiles c, c + pairs, ...).  The split tail and the bias
-                                    seeding always use the static schedule. */
+  GEMM_OPT_DYNAMIC_TILES = 13,   /* two-SM kernel with whole tiles: 1 each pair takes its
+                                    next tile from a counter in the handle at run time, so
+                                    the tiles in flight stay in raster order (half the
+                                    DRAM reads of the static schedule at 16384^3 with
+                                    raster groups of 8); 0 (default) the static schedule
+                                    gemm_work_units reports (pair c takes tiles c, c +
+                                    pairs, ...), measured faster with raster groups of 16
+                                    once operands come in two-k-block copies.  The split
+                                    tail and the bias seeding always use the static
+                                    schedule. */
   GEMM_OPT_STAGES = 14,          /* one-SM tensor-core kernel: shared-memory ring stages.
                                     -1 (default) the picker's: all the ring holds, or, for a
                                     cluster split over more than half the SMs, as many as

@@ -355,13 +355,13 @@ def test_pair_grid_sizes(g, dev, grid):
 @pytest.mark.parametrize("odt", [F16, F32])
 def test_pair_dynamic_matches_static(g, dev, odt):
     """Two-SM kernel over several waves of whole tiles (9 x 17 pair tiles,
-    ragged on both sides): by default the pairs take tiles from a counter at
-    run time; with GEMM_OPT_DYNAMIC_TILES = 0, in the static order.  A tile's
-    k order depends on the tile alone, so both give the same bits, which
-    match the oracle; the counter resets itself at the end of a launch, so a
-    second launch gives them again."""
+    ragged on both sides): with GEMM_OPT_DYNAMIC_TILES = 1 the pairs take
+    tiles from a counter at run time; with 0 (the default), in the static
+    order.  A tile's k order depends on the tile alone, so both give the same
+    bits, which match the oracle; the counter resets itself at the end of a
+    launch, so a second launch gives them again."""
     p = problem(2048 + 40, 4096 + 8, 1032, 0, 1, F16, odt, True, 160)
-    set_opts(g, kernel=TC2)
+    set_opts(g, kernel=TC2, dyn=1)
     assert g.plan(p.M, p.N, p.K, 0, 1, B.GEMM_F16,
                   B.GEMM_F16 if odt == F16 else B.GEMM_F32)["dp_tiles"] == 9 * 17
     C_dyn = run(g, p, dev)

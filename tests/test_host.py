@@ -106,7 +106,7 @@ def test_picker_large_square_two_sm_tiles():
     assert (p.tiles_m, p.tiles_n, p.k_iters) == (32, 32, 128)
     assert (p.dp_tiles, p.sk_tiles, p.grid, p.workspace_bytes) == (1024, 0, SMS, 0)
     assert (p.swap_ab, p.a_mn_major, p.b_mn_major) == (0, 0, 0)
-    assert p.group_m == 8  # raster groups of 2048 rows of A (8 pair tiles)
+    assert p.group_m == 16  # raster groups of 4096 rows of A (16 pair tiles)
     rc, p = plan(16384, 16384, 16384, 0, 0, F16, F16)
     assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC2 and p.b_mn_major == 1
     assert p.dp_tiles == 64 * 64 and p.sk_tiles == 0 and p.workspace_bytes == 0
