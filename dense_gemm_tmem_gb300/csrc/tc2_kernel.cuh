@@ -493,7 +493,8 @@ __device__ __forceinline__ void tc2_split_half(const TcArgs& args, const CUtenso
         }
       }
     }
-    store_out<CW, OUT_F16, false>(args, tmC, stage, row >> 5, mm, row & 31, nbase + c * CW, acc);
+    store_out<CW, OUT_F16, false>(args, tmC, stage, row >> 5, mm, row & 31, nbase + c * CW, acc,
+                                  c == 0);
   }
   if (threadIdx.x == 64) atomicExch(ticket, 0);  // ready for the next launch
 }
@@ -571,7 +572,8 @@ __device__ __forceinline__ void tc2_epilogue(const TcArgs& args, uint64_t* acc_f
         float v[32];
         __syncwarp();
         tmem_load_chunk<32>(taddr + c * 32, v);
-        store_out<32, OUT_F16, false>(args, tmC, stage, q, mm, lane, nbase + c * 32, v);
+        store_out<32, OUT_F16, false>(args, tmC, stage, q, mm, lane, nbase + c * 32, v,
+                                      c == 0);
       }
     } else {
       tc2_split_half<OUT_F16>(args, tmC, stage, taddr, row, mm, nbase, u, rank, cluster_id,

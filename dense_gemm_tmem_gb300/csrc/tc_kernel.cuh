@@ -383,14 +383,24 @@ __device__ __forceinline__ void store_rows_vec(const TcArgs& a, float* sw, int32
 // expects (128-byte rows for fp32, 16-byte piece k at k ^ (row % 8); 64-byte
 // rows for fp16, piece k at k ^ ((row / 2) % 4)), which also keeps the shared
 // stores free of bank conflicts; lane 0 then issues one bulk store of the box.
-// Rows and columns past the matrix are dropped by the TMA unit.  The box is
-// reused only after the previous bulk store from it has read it.
+// Rows and columns past the matrix are dropped by the TMA unit.  fp16 boxes
+// (2 KiB) alternate between the two halves of the warp's 4 KiB, so the next
+// chunk is written while the TMA unit still reads the previous one (the unit
+// takes a few hundred cycles per copy); a box is reused only after the store
+// from it has read it.  `first` (the tile's first chunk, whose box the
+// previous tile's last store may still read) waits for every earlier store.
 template <bool OUT_F16>
 __device__ __forceinline__ void store_rows_tma(const CUtensorMap* tmC, const TcArgs& a,
                                                uint8_t* box, int32_t mrow0, int lane,
-                                               int32_t nn0, const float (&v)[32]) {
+                                               int32_t nn0, const float (&v)[32], bool first) {
   if (mrow0 >= a.Mm || nn0 >= a.Nm) return;  // the same for the whole warp
-  if (lane == 0) bulk_wait_read_all();
+  if constexpr (OUT_F16) box += ((nn0 >> 5) & 1) * 2048;
+  if (lane == 0) {
+    if (OUT_F16 && !first)
+      bulk_wait_read_1();
+    else
+      bulk_wait_read_all();
+  }
   __syncwarp();
   float o[32];
   const float* ob = out_bias(a);
@@ -442,13 +452,13 @@ __device__ __forceinline__ void store_rows_tma(const CUtensorMap* tmC, const TcA
 template <int CW, bool OUT_F16, bool TRANS>
 __device__ __forceinline__ void store_out(const TcArgs& a, const CUtensorMap* tmC,
                                           uint8_t* stage, int q, int32_t mm, int lane,
-                                          int32_t nn0, const float (&v)[CW]) {
+                                          int32_t nn0, const float (&v)[CW], bool first) {
   if constexpr (TRANS) {
     store_chunk_trans<CW, OUT_F16>(a, mm, nn0, v);
   } else {
     if constexpr (CW == 32) {
       if (a.c_tma) {
-        store_rows_tma<OUT_F16>(tmC, a, stage + q * 4096, mm - lane, lane, nn0, v);
+        store_rows_tma<OUT_F16>(tmC, a, stage + q * 4096, mm - lane, lane, nn0, v, first);
         return;
       }
     }
@@ -979,7 +989,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           float v[CW];
           __syncwarp();
           tmem_load_chunk<CW>(taddr + c * CW, v);
-          store_out<CW, OUT_F16, TRANS>(args, &tmC, stage, q, mm, lane, nbase + c * CW, v);
+          store_out<CW, OUT_F16, TRANS>(args, &tmC, stage, q, mm, lane, nbase + c * CW, v,
+                                        c == 0);
         }
       } else {
         const int32_t st = u.tile - W.dp_tiles;  // split-tile index
@@ -1059,7 +1070,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               }
             }
             store_out<CW, OUT_F16, TRANS>(args, &tmC, stage, q, mm, lane, nbase + c * CW,
-                                          acc);
+                                          acc, c == 0);
           }
           if (et == 0) atomicExch(&args.tickets[st], 0);  // ready for the next launch
         }
