@@ -252,14 +252,16 @@ int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
     const int64_t T2 = t2m * t2n;
     const int64_t I2 = ceil_div(K, kBK);
     bool use = forced_pair || o.pair == 1;
-    // Shallow products with few waves of pair tiles run faster as one-SM
-    // 128 x 256 whole tiles: a pair tile's prologue and exposed last epilogue
-    // weigh more when each tile is short.  Measured (graph replay, cold
-    // inputs, us per launch, one-SM whole vs two-SM): 2048x2048x1024 13.19 vs
-    // 14.31, 1024x4864x512 11.03 vs 12.28, 4096x4096x1024 31.89 vs 32.07;
-    // from K = 1536 the pairs are as fast or faster (2048^3 19.32 vs 19.40,
-    // 4096x2048x1536 24.77 vs 24.33, 4096x4096x2048 53.84 vs 49.48).
-    const bool shallow_few = K <= 1024 && T2 <= 4 * pairs;
+    // Shallow products with at most one wave of pair tiles run faster as
+    // one-SM 128 x 256 whole tiles: a pair tile's prologue and exposed
+    // epilogue weigh more when each tile is short and nothing overlaps them.
+    // Measured (graph replay, cold inputs, us per launch, one-SM whole vs
+    // two-SM): 2048x2048x1024 13.19 vs 14.31, 1024x4864x512 11.03 vs 12.28;
+    // with more waves the pairs win (4096x4096x1024, 3.4 waves: 1095 vs 1146
+    // TFLOP/s; 1280x5120x1024, 1.3 waves: 696 vs 708), and from K = 1536 the
+    // pairs are as fast or faster (2048^3 19.32 vs 19.40 us, 4096x2048x1536
+    // 24.77 vs 24.33).
+    const bool shallow_few = K <= 1024 && T2 <= pairs;
     if (!use && o.force_grid <= 0) use = 2 * T2 >= pairs && !shallow_few;
     if (use) {
       if (T2 > INT32_MAX / 2 || I2 > INT32_MAX / 2) return GEMM_ERR_UNSUPPORTED;

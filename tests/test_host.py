@@ -122,12 +122,12 @@ def test_picker_pair_rule():
     assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC2 and (p.grid, p.dp_tiles) == (128, 64)
     rc, p = plan(1024, 19 * 256, 4096)  # one wave: 76 = 4 x 19
     assert rc == 0 and p.kernel == B.GEMM_KERNEL_TC2 and p.grid == 152
-    # shallow (K <= 1024) with at most 4 waves of pair tiles: one-SM 128 x 256
+    # shallow (K <= 1024) with at most one wave of pair tiles: one-SM 128 x 256
     # whole tiles instead
     rc, p = plan(2048, 2048, 1024)
     assert (p.kernel, p.tile_m, p.tile_n, p.grid, p.dp_tiles) == (B.GEMM_KERNEL_TC, 128, 256, 128, 128)
-    rc, p = plan(1280, 5120, 1024)
-    assert (p.kernel, p.tile_n, p.dp_tiles) == (B.GEMM_KERNEL_TC, 256, 200)
+    rc, p = plan(1280, 5120, 1024)  # 100 pair tiles: 1.3 waves stay on pairs
+    assert p.kernel == B.GEMM_KERNEL_TC2
     rc, p = plan(2048, 2048, 2048)  # K = 2048: pairs
     assert p.kernel == B.GEMM_KERNEL_TC2
     rc, p = plan(8192, 8192, 1024)  # 1024 pair tiles: 13.5 waves stay on pairs
