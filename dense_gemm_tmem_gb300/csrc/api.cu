@@ -1114,24 +1114,23 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, co
   a.wait_limit_ns = h->opt.wait_limit_ns;
   a.a_mn = plan.a_mn_major;
   a.b_mn = plan.b_mn_major;
-  // Row-major output chunks of 32 columns leave by TMA store when C allows it.
-  // By default, fp32 output only for launches with more output tiles than
-  // CTAs: an fp32 single-wave launch measured faster with staged plain stores
-  // (graph replay, cold inputs, us per launch: 512^3 6.64 vs 6.92, 256^3 5.55
-  // vs 5.91, one 128 x 128 tile 4.04 vs 4.41).  fp16 output only for launches
-  // of 10 or more tiles per CTA (per pair on the two-SM kernel), where TMA
-  // stores measured even or a little ahead (8192^3 600.7 vs 601.4 us, 8192 x
-  // 8192 x 2048 156.9 vs 157.3); on fewer waves the plain stores measured
-  // faster (2048^3 18.9 vs 17.9 us, 2048 x 2048 x 1024 13.0 vs 12.1, 1536 x
-  // 2048 x 2048 18.5 vs 17.4, 4096^3 88.3 vs 87.4, 6144^3 258.4 vs 257.8).
+  // Row-major output chunks of 32 columns leave by TMA store when C allows it,
+  // by default only on launches of many waves: 4 or more output tiles per CTA
+  // (per pair on the two-SM kernel) for fp32 output, 10 or more for fp16.
+  // There TMA stores measured even or ahead (graph replay, cold inputs, us per
+  // launch, TMA vs plain: fp32 8192 x 8192 x 4096 312.2 vs 317.0, 6144^3 266.1
+  // vs 267.0; fp16 8192^3 600.7 vs 601.4, 8192 x 8192 x 2048 156.9 vs 157.3);
+  // on fewer waves the staged plain stores measured faster (fp32 4096 x 4096 x
+  // 1024 37.1 vs 34.6, 3072^3 41.4 vs 40.3, 512^3 6.64 vs 6.92, one 128 x 128
+  // tile 4.04 vs 4.41; fp16 2048^3 18.9 vs 17.9, 2048 x 2048 x 1024 13.0 vs
+  // 12.1, 4096^3 88.3 vs 87.4, 6144^3 258.4 vs 257.8).
   std::memset(&L.tmC, 0, sizeof(L.tmC));
   const int64_t out_tiles = int64_t(plan.tiles_m) * plan.tiles_n;
   const int64_t out_units = pair ? plan.grid / 2 : plan.grid;  // CTAs, or pairs
   const bool tma_wanted =
       h->opt.tma_store > 0 ||
       (h->opt.tma_store < 0 &&
-       (layout.out_dtype == GEMM_F16 ? out_tiles >= 10 * out_units
-                                     : out_tiles * (pair ? 2 : 1) > plan.grid));
+       out_tiles >= (layout.out_dtype == GEMM_F16 ? 10 : 4) * out_units);
   a.c_tma = (tma_wanted && !swap && plan.tile_n >= 32 && (pair || plan.tile_m == dg::kBM) &&
              plan.kernel != GEMM_KERNEL_SPLITC &&
              dg::encode_output(h, &L.tmC, C, M, N, layout.out_dtype == GEMM_F16))

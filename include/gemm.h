@@ -128,10 +128,9 @@ enum {
                                     the wave before it split evenly over the pairs */
   GEMM_OPT_TMA_STORE = 11,       /* row-major output tiles leave the tensor-core kernels by
                                     TMA store when C is 16-byte aligned with a row pitch that
-                                    is a multiple of 16 bytes: -1 (default) for fp32 output
-                                    on launches with more output tiles than CTAs and for
-                                    fp16 output on launches with 10 or more output tiles per
-                                    CTA (per CTA pair on the two-SM kernel), 1 always, 0
+                                    is a multiple of 16 bytes: -1 (default) on launches with
+                                    4 (fp32 output) or 10 (fp16 output) or more output tiles
+                                    per CTA (per CTA pair on the two-SM kernel), 1 always, 0
                                     never (plain stores) */
   GEMM_OPT_BIAS_INIT = 12,       /* 1: the tensor-core kernels start each tile's fp32
                                     reduction from the bias (seeded into the accumulator
