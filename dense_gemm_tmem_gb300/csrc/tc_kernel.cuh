@@ -17,10 +17,11 @@
 //                      k-block, hands the accumulator to the epilogue.  Warp 1
 //                      also allocates and frees TMEM.
 //   warps 2-5          epilogue: tcgen05.ld 32 lanes x 32 columns, + bias[n] in
-//                      fp32, one rounding to the output type, then a TMA store
-//                      of the warp's 32 x 32 block from a swizzled shared box
-//                      (plain stores where C cannot take TMA; lane-per-column
-//                      stores for swapped operands).  For a Stream-K partial
+//                      fp32, one rounding to the output type, then, on launches
+//                      of many waves, a TMA store of the warp's 32 x 32 block
+//                      from a swizzled shared box (otherwise, and where C cannot
+//                      take TMA, plain stores staged through padded shared rows;
+//                      lane-per-column stores for swapped operands).  For a Stream-K partial
 //                      unit: publish the fp32 partial, take a ticket, and the
 //                      last contributor sums all partials in ascending k order
 //                      before the same epilogue.  Each drained accumulator is
