@@ -41,7 +41,7 @@ class gemm_plan_t(ctypes.Structure):
         "kernel", "swap_ab", "tile_m", "tile_n", "tile_k", "stages", "grid", "tiles_m",
         "tiles_n", "k_iters", "dp_tiles", "sk_tiles", "a_mn_major", "b_mn_major", "group_m",
         "cluster_split")] + [("workspace_bytes", c_int64), ("k_group", c_int32),
-                             ("reserved", c_int32)]
+                             ("tma_store", c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

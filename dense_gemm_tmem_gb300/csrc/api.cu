@@ -196,8 +196,39 @@ int one_sm_k_group(const Options& o, int64_t K, bool a_mn, bool b_mn, int* stage
   return kg;
 }
 
+// Whether row-major output tiles leave by TMA store (C's base and row pitch
+// permitting, checked at launch): the tensor-core kernels that store 32-column
+// chunks of row-major tiles, by default only on launches of many waves, 4 or
+// more output tiles per CTA (per pair on the two-SM kernel) for fp32 output,
+// 10 or more for fp16.  There TMA stores measured even or ahead (graph replay,
+// cold inputs, us per launch, TMA vs plain: fp32 8192 x 8192 x 4096 312.2 vs
+// 317.0, 6144^3 266.1 vs 267.0; fp16 8192^3 600.7 vs 601.4, 8192 x 8192 x
+// 2048 156.9 vs 157.3); on fewer waves the staged plain stores measured
+// faster (fp32 4096 x 4096 x 1024 37.1 vs 34.6, 3072^3 41.4 vs 40.3, 512^3
+// 6.64 vs 6.92, one 128 x 128 tile 4.04 vs 4.41; fp16 2048^3 18.9 vs 17.9,
+// 2048 x 2048 x 1024 13.0 vs 12.1, 4096^3 88.3 vs 87.4, 6144^3 258.4 vs 257.8).
+int32_t plan_tma_store(const gemm_plan_t& p, const Options& o, bool out_f16) {
+  const bool pair = p.kernel == GEMM_KERNEL_TC2;
+  if (p.kernel != GEMM_KERNEL_TC && p.kernel != GEMM_KERNEL_STREAMK && !pair) return 0;
+  if (p.swap_ab || p.tile_n < 32 || (!pair && p.tile_m != kBM)) return 0;
+  if (o.tma_store >= 0) return o.tma_store > 0 ? 1 : 0;
+  const int64_t tiles = int64_t(p.tiles_m) * p.tiles_n;
+  const int64_t units = pair ? p.grid / 2 : p.grid;  // CTAs, or pairs
+  return tiles >= (out_f16 ? 10 : 4) * units ? 1 : 0;
+}
+
+int plan_for_shape(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
+                   const Options& o, gemm_plan_t* p);
+
 int plan_for(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
              const Options& o, gemm_plan_t* p) {
+  const int rc = plan_for_shape(M, N, K, L, num_sms, o, p);
+  if (rc == GEMM_OK) p->tma_store = plan_tma_store(*p, o, L.out_dtype == GEMM_F16);
+  return rc;
+}
+
+int plan_for_shape(int64_t M, int64_t N, int64_t K, gemm_layout_t L, int num_sms,
+                   const Options& o, gemm_plan_t* p) {
   if (!p) return GEMM_ERR_INVALID_ARG;
   std::memset(p, 0, sizeof(*p));
   p->k_group = 1;
@@ -745,10 +776,12 @@ int on_device(int device, F&& f) {
 void log_plan(const gemm_plan_t& p, int64_t M, int64_t N, int64_t K) {
   std::fprintf(stderr,
                "[gemm] M=%lld N=%lld K=%lld kernel=%d swap=%d tile=%dx%dx%d stages=%d "
-               "grid=%d tiles=%dx%d k_iters=%d dp=%d sk=%d a_mn=%d b_mn=%d\n",
+               "grid=%d tiles=%dx%d k_iters=%d dp=%d sk=%d a_mn=%d b_mn=%d k_group=%d "
+               "csplit=%d tma_store=%d\n",
                (long long)M, (long long)N, (long long)K, p.kernel, p.swap_ab, p.tile_m,
                p.tile_n, p.tile_k, p.stages, p.grid, p.tiles_m, p.tiles_n, p.k_iters,
-               p.dp_tiles, p.sk_tiles, p.a_mn_major, p.b_mn_major);
+               p.dp_tiles, p.sk_tiles, p.a_mn_major, p.b_mn_major, p.k_group, p.cluster_split,
+               p.tma_store);
 }
 
 }  // namespace
@@ -1114,25 +1147,10 @@ int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, co
   a.wait_limit_ns = h->opt.wait_limit_ns;
   a.a_mn = plan.a_mn_major;
   a.b_mn = plan.b_mn_major;
-  // Row-major output chunks of 32 columns leave by TMA store when C allows it,
-  // by default only on launches of many waves: 4 or more output tiles per CTA
-  // (per pair on the two-SM kernel) for fp32 output, 10 or more for fp16.
-  // There TMA stores measured even or ahead (graph replay, cold inputs, us per
-  // launch, TMA vs plain: fp32 8192 x 8192 x 4096 312.2 vs 317.0, 6144^3 266.1
-  // vs 267.0; fp16 8192^3 600.7 vs 601.4, 8192 x 8192 x 2048 156.9 vs 157.3);
-  // on fewer waves the staged plain stores measured faster (fp32 4096 x 4096 x
-  // 1024 37.1 vs 34.6, 3072^3 41.4 vs 40.3, 512^3 6.64 vs 6.92, one 128 x 128
-  // tile 4.04 vs 4.41; fp16 2048^3 18.9 vs 17.9, 2048 x 2048 x 1024 13.0 vs
-  // 12.1, 4096^3 88.3 vs 87.4, 6144^3 258.4 vs 257.8).
+  // Row-major output chunks of 32 columns leave by TMA store where the plan
+  // takes it (plan_tma_store) and C allows it.
   std::memset(&L.tmC, 0, sizeof(L.tmC));
-  const int64_t out_tiles = int64_t(plan.tiles_m) * plan.tiles_n;
-  const int64_t out_units = pair ? plan.grid / 2 : plan.grid;  // CTAs, or pairs
-  const bool tma_wanted =
-      h->opt.tma_store > 0 ||
-      (h->opt.tma_store < 0 &&
-       out_tiles >= (layout.out_dtype == GEMM_F16 ? 10 : 4) * out_units);
-  a.c_tma = (tma_wanted && !swap && plan.tile_n >= 32 && (pair || plan.tile_m == dg::kBM) &&
-             plan.kernel != GEMM_KERNEL_SPLITC &&
+  a.c_tma = (plan.tma_store &&
              dg::encode_output(h, &L.tmC, C, M, N, layout.out_dtype == GEMM_F16))
                 ? 1
                 : 0;

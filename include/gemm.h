@@ -98,7 +98,9 @@ typedef struct {
   int64_t workspace_bytes; /* fp32 partial-tile bytes the split needs */
   int32_t k_group;     /* k-blocks each TMA copy brings (the ring is taken k_group
                           stages at a time); 1 = one copy per operand and k-block */
-  int32_t reserved;    /* 0 */
+  int32_t tma_store;   /* 1: row-major output tiles leave by TMA store (where C's base is
+                          16-byte aligned and its row pitch a multiple of 16 bytes),
+                          0: plain stores (always for gemm_run_noalloc) */
 } gemm_plan_t;
 
 /* Options for tests and tuning (gemm_set_option).  Values < 0 restore the default. */

@@ -371,6 +371,29 @@ def test_shape_workload_spec():
             inputs.workload(bad)
 
 
+def test_picker_store_path():
+    """Row-major output leaves by TMA store only on launches of many waves: 10
+    or more output tiles per CTA (per pair on the two-SM kernel) for fp16
+    output, 4 or more for fp32; plain stores below, on the 64-row kernel, for
+    swapped operands (C written transposed), cluster splits and CUDA cores."""
+    cases = [  # (M, N, K, a_major, b_major, out dtype) -> (kernel, tma_store)
+        ((8192, 8192, 8192, 0, 1, F16), (B.GEMM_KERNEL_TC2, 1)),    # 1024 tiles on 76 pairs
+        ((16384, 16384, 16384, 0, 0, F16), (B.GEMM_KERNEL_TC2, 1)),
+        ((4096, 14336, 4096, 0, 1, F16), (B.GEMM_KERNEL_TC2, 1)),   # 896: 11.8 per pair
+        ((6144, 6144, 6144, 0, 1, F16), (B.GEMM_KERNEL_TC2, 0)),    # 576: 7.6 per pair
+        ((6144, 6144, 6144, 0, 1, F32), (B.GEMM_KERNEL_TC2, 1)),
+        ((4096, 4096, 4096, 0, 1, F32), (B.GEMM_KERNEL_TC2, 0)),    # 256: 3.4 per pair
+        ((2048, 2048, 2048, 0, 1, F16), (B.GEMM_KERNEL_TC2, 0)),
+        ((512, 512, 512, 0, 0, F32), (B.GEMM_KERNEL_TC, 0)),        # 64-row tiles
+        ((16, 4096, 4096, 0, 0, F32), (B.GEMM_KERNEL_SPLITC, 0)),   # swapped cluster split
+    ]
+    for (M, N, K, am, bm, odt), want in cases:
+        rc, p = plan(M, N, K, am=am, bm=bm, odt=odt)
+        assert rc == 0 and (p.kernel, p.tma_store) == want, (M, N, K, odt, p.as_dict())
+    rc, p = plan(2048, 2048, 2048, idt=F32, odt=F32)
+    assert rc == 0 and (p.kernel, p.tma_store) == (B.GEMM_KERNEL_SIMT, 0)
+
+
 def test_picker_k_group():
     """k-blocks per TMA copy on the 64-row kernel: up to 4, whole groups in
     the ring; a K-major operand needs K a multiple of 64 (its 3-D view holds
