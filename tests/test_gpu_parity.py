@@ -117,6 +117,28 @@ def test_tma_store_path_forced(g, dev, kernel, odt):
     full_check(g, dev, p)
 
 
+@pytest.mark.parametrize("kernel,grid,odt,want", [
+    (TC2, 4, F16, 1),    # 20 pair tiles on 2 pairs: 10 per pair, TMA stores
+    (TC2, 6, F16, 0),    # on 3 pairs: 6.7 per pair, plain stores
+    (TC2, 10, F32, 1),   # on 5 pairs: 4 per pair
+    (TC2, 12, F32, 0),   # on 6 pairs: 3.3 per pair
+    (TC, 8, F16, 1),     # 80 one-SM 128 x 128 tiles on 8 CTAs
+    (TC, 20, F32, 1),
+    (TC, 40, F32, 0),
+])
+def test_default_store_path_by_waves(g, dev, kernel, grid, odt, want):
+    """The default store path follows the waves per CTA (per pair): TMA stores
+    from 10 output tiles per CTA for fp16 output and from 4 for fp32, plain
+    stores below; either way the oracle's result."""
+    odt_b = B.GEMM_F16 if odt == F16 else B.GEMM_F32
+    M, N, K = 1280, 1024, 192
+    set_opts(g, kernel=kernel, grid=grid, tile_n=(-1 if kernel == TC2 else 128))
+    pl = g.plan(M, N, K, 0, 1, B.GEMM_F16, odt_b)
+    assert (pl["kernel"], pl["grid"], pl["tma_store"]) == (kernel, grid, want), pl
+    p = problem(M, N, K, 0, 1, F16, odt, True, 440 + grid + (odt == F32))
+    full_check(g, dev, p)
+
+
 @pytest.mark.parametrize("kernel", [TC, TC2])
 @pytest.mark.parametrize("odt", [F16, F32])
 def test_output_pitch_not_16_bytes(g, dev, kernel, odt):
