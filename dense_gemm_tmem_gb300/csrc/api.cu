@@ -928,7 +928,12 @@ int gemm_create(gemm_handle_t* out, int device) {
       // n == 0: clusters of s cannot be scheduled at all (-1 keeps the picker off them);
       // a failed query leaves the SMs / s estimate
       h->opt.csplit_clusters[s] = n > 0 ? std::min(n, h->num_sms / s) : n == 0 ? -1 : h->num_sms / s;
+      if (dg::log_enabled())
+        std::fprintf(stderr, "[gemm] device %d: clusters of %d resident at once: %d\n", device, s,
+                     n);
     }
+    if (dg::log_enabled())
+      std::fprintf(stderr, "[gemm] device %d: CTA pairs resident at once: %d\n", device, pairs);
     for (int bn : {16, 32, 64, 128})
       for (int t = 0; t < 2; ++t) {
         h->opt.lean_stages[dg::width_index(bn)][t] = dg::tc_lean_stages(bn, t != 0);
