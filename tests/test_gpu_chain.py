@@ -37,14 +37,16 @@ def chain_reference(A0, mats):
     return X.astype(np.float64)
 
 
-@pytest.mark.parametrize("opts", [{}, {"kernel": B.GEMM_KERNEL_STREAMK},
-                                  {"kernel": B.GEMM_KERNEL_SPLITC, "csplit": 4},
-                                  {"kernel": B.GEMM_KERNEL_TC2}])
+@pytest.mark.parametrize("opts,M", [({}, 384), ({"kernel": B.GEMM_KERNEL_STREAMK}, 384),
+                                    ({"kernel": B.GEMM_KERNEL_SPLITC, "csplit": 4}, 384),
+                                    ({"kernel": B.GEMM_KERNEL_TC2}, 384),
+                                    ({"tile_m": 64}, 384),   # 64-row tiles
+                                    ({}, 16)])               # swapped skinny cluster split
 @pytest.mark.parametrize("graph", [False, True])
-def test_dependent_chain(dev, opts, graph):
+def test_dependent_chain(dev, opts, M, graph):
     g = Gemm(dev)
     set_opts(g, **opts)
-    M, N, steps = 384, 512, 6
+    N, steps = 512, 6
     A0 = inputs.draw((M, N), 400, "int", inputs.F16, -1, 1)
     # sparse {-1,0,1} weights keep every intermediate a small integer
     rng = np.random.default_rng(401)
